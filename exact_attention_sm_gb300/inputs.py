@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the oracle checks.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic.  Every tensor is drawn on the CPU with
+``torch.Generator().manual_seed(seed)`` in float32 from N(0, 1), in the order
+Q, K, V (q, k_pages, v_pages for decode), then cast to the requested dtype.
+"""
+from __future__ import annotations
+
+import torch
+
+_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _gen(seed):
+    return torch.Generator().manual_seed(int(seed))
+
+
+def prefill_inputs(B, Hq, Hkv, Lq, Lk, d, dtype="bf16", seed=0):
+    """q [B,Hq,Lq,d], k and v [B,Hkv,Lk,d], N(0,1), contiguous, on the CPU."""
+    g = _gen(seed)
+    q = torch.randn(B, Hq, Lq, d, generator=g)
+    k = torch.randn(B, Hkv, Lk, d, generator=g)
+    v = torch.randn(B, Hkv, Lk, d, generator=g)
+    dt = _DT[dtype]
+    return q.to(dt), k.to(dt), v.to(dt)
+
+
+def sample_rows(B, Hq, Lq, n_random=4096, tile=128, seed=3):
+    """Rows (b, h, i) checked on large prefill problems.
+
+    The first ``tile`` query rows of (b=0, h=0), the last ``tile`` rows of
+    (b=B-1, h=Hq-1), and ``n_random`` rows drawn by
+    ``torch.randperm(B*Hq*Lq, generator=seed)``.
+    """
+    rows = [(0, 0, i) for i in range(min(tile, Lq))]
+    rows += [(B - 1, Hq - 1, i) for i in range(max(0, Lq - tile), Lq)]
+    total = B * Hq * Lq
+    pick = torch.randperm(total, generator=_gen(seed))[: min(n_random, total)].tolist()
+    for flat in pick:
+        b, rem = divmod(flat, Hq * Lq)
+        h, i = divmod(rem, Lq)
+        rows.append((b, h, i))
+    return rows
+
+
+def decode_lengths_uniform(B, lo, hi, seed=2):
+    """Per-request context lengths uniform in [lo, hi] (inclusive)."""
+    return torch.randint(lo, hi + 1, (B,), generator=_gen(seed)).tolist()
+
+
+def decode_inputs(seq_lens, Hq, Hkv, d, page_size=16, dtype="bf16", seed=0, perm_seed=1,
+                  extra_table_cols=0):
+    """Paged decode inputs with a shuffled block table.
+
+    The pool holds exactly sum_b ceil(len_b / page_size) pages.  A random
+    permutation of the pool (``torch.randperm(num_pages, generator=perm_seed)``)
+    is handed out to the requests in order; table entries past a request's
+    last page are -1.  Returns q [B,Hq,d], k_pages and v_pages
+    [num_pages, page_size, Hkv, d], block_table int32 [B, max_pages],
+    seq_lens int32 [B], all on the CPU.
+    """
+    B = len(seq_lens)
+    pages_per = [-(-int(n) // page_size) for n in seq_lens]
+    num_pages = max(1, sum(pages_per))
+    max_pages = max(1, max(pages_per)) + int(extra_table_cols)
+    perm = torch.randperm(num_pages, generator=_gen(perm_seed))
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages_per):
+        table[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    g = _gen(seed)
+    q = torch.randn(B, Hq, d, generator=g)
+    k_pages = torch.randn(num_pages, page_size, Hkv, d, generator=g)
+    v_pages = torch.randn(num_pages, page_size, Hkv, d, generator=g)
+    dt = _DT[dtype]
+    lens = torch.tensor([int(n) for n in seq_lens], dtype=torch.int32)
+    return q.to(dt), k_pages.to(dt), v_pages.to(dt), table, lens
+
+
+def merge_inputs(rows, S, d, seed=0, empty_frac=0.0):
+    """Random partial states: o_parts [rows,S,d] f32, lse_parts [rows,S] f32.
+
+    A fraction ``empty_frac`` of the (row, segment) states is marked empty
+    (LSE = -inf); the first row has every segment empty when empty_frac > 0.
+    """
+    g = _gen(seed)
+    o = torch.randn(rows, S, d, generator=g)
+    lse = torch.randn(rows, S, generator=g) * 4.0
+    if empty_frac > 0:
+        drop = torch.rand(rows, S, generator=g) < empty_frac
+        lse[drop] = float("-inf")
+        lse[0, :] = float("-inf")
+    return o, lse

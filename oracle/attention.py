@@ -1,0 +1,431 @@
+"""Float64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path (the CUDA library in
+``exact_attention_sm_gb300/csrc`` and its Python binding) imports, calls or
+links this module.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may use it.  It shares no code,
+constants or helpers with the CUDA path; the only thing both sides share are
+the seeded input generators in ``exact_attention_sm_gb300/inputs.py``, which
+hold none of the method's arithmetic.
+
+Every function is the plain definition (or the pages' algorithm, step by step)
+in float64 with numpy; ``@`` (a BLAS matmul) is the only library primitive used
+as a step.  Nothing is blocked, fused or reordered beyond what the cited
+passage states.
+
+Pages cited (by title; the short tag is used below):
+
+* [Lecture 4]   "Lecture 4 - Efficient attention kernels: FlashAttention and
+                FlashInfer" (Stanford CS349D course notes, semidirectx.com)
+* [Tiling blog] "The attention formula did not change, so why is it several
+                times faster? FlashAttention's tiling, online softmax and IO"
+                (zwjcode.cn blog)
+* [LLM book]    "10.3 FlashAttention: IO-aware algorithm design" (LLM
+                Internals book, yeasy.gitbook.io)
+* [CUDA book]   "FlashAttention and inference operators" (CUDA advanced
+                handbook, anrans.github.io ai-infra-handbooks)
+
+Parity pins (see tests/test_oracle_pins.py): every function below is pinned
+by at least one of worked examples printed on the pages, closed forms,
+brute force on tiny inputs, or torch's own float64 math attention.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+NEG_INF = -math.inf
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Softmax building blocks
+# --------------------------------------------------------------------------
+
+def safe_softmax(x):
+    """Numerically safe softmax of one row.
+
+    [Lecture 4] section 3.2 (online softmax): m(x) = max_i x_i,
+    f(x) = exp(x - m(x)), l(x) = sum_i f(x)_i, softmax(x) = f(x) / l(x).
+    Returns (softmax, m, l).
+    """
+    x = _f64(x)
+    m = float(x.max())
+    f = np.exp(x - m)
+    l = float(f.sum())
+    return f / l, m, l
+
+
+def online_softmax_stats(x, block):
+    """Stream a row in blocks of ``block`` values keeping only (m, l).
+
+    [Lecture 4] section 3.2: when a new block arrives, compute its local max
+    and local sum; if the overall max grows, the old l is multiplied by
+    exp(m_old - m_new) before the new block's contribution is added.
+    [LLM book] 10.3.2 "Online Softmax" states the same update element-wise.
+    Returns the final (m, l) and the list of (m, l) after each block.
+    """
+    x = _f64(x)
+    m, l = NEG_INF, 0.0
+    trace = []
+    for start in range(0, x.size, block):
+        xb = x[start:start + block]
+        mb = float(xb.max())
+        lb = float(np.exp(xb - mb).sum())
+        m_new = max(m, mb)
+        old_scale = 0.0 if m == NEG_INF else math.exp(m - m_new)
+        l = old_scale * l + math.exp(mb - m_new) * lb
+        m = m_new
+        trace.append((m, l))
+    return m, l, trace
+
+
+def merge_row_states(state1, state2):
+    """Merge two partial row states (m, l, a).
+
+    [Tiling blog] section 03 ("online softmax keeps only three states"):
+    m' = max(m, m_b); l' = exp(m - m') l + exp(m_b - m') l_b;
+    a' = exp(m - m') a + exp(m_b - m') a_b, where a is the not-yet-divided
+    weighted value sum.  An empty state has m = -inf, l = 0, a = 0.
+    """
+    m1, l1, a1 = state1
+    m2, l2, a2 = state2
+    m = max(m1, m2)
+    if m == NEG_INF:
+        return NEG_INF, 0.0, _f64(a1) * 0.0
+    c1 = 0.0 if m1 == NEG_INF else math.exp(m1 - m)
+    c2 = 0.0 if m2 == NEG_INF else math.exp(m2 - m)
+    return m, c1 * l1 + c2 * l2, c1 * _f64(a1) + c2 * _f64(a2)
+
+
+def block_state(scores, values):
+    """The (m, l, a) state of one block of scores with their value rows.
+
+    [Tiling blog] section 03: m_b = block max, l_b = sum exp(s - m_b),
+    a_b = sum exp(s - m_b) v.
+    """
+    s = _f64(scores)
+    v = _f64(values)
+    mb = float(s.max())
+    e = np.exp(s - mb)
+    return mb, float(e.sum()), e @ v
+
+
+# --------------------------------------------------------------------------
+# Dense attention: the definition the fused kernel must reproduce
+# --------------------------------------------------------------------------
+
+def attention_dense(q, k, v, scale, causal=False):
+    """Standard (materialising) attention for one head, in float64.
+
+    [Tiling blog] section 01: S = Q K^T * scale, P = softmax(S), O = P V,
+    with the scale applied to the scores before the max.  Causal masking
+    follows [Tiling blog] section 06: query i sees key j only if j <= i, and
+    masked scores are -inf before the max and the sum.  The per-row
+    log-sum-exp is LSE = m + ln l ([LLM book] 10.3.2, "LSE").
+
+    A row with no visible key (all -inf) has l = 0; its output is O = 0 and
+    LSE = -inf rather than NaN ([CUDA book] split-K merge exercise: skip
+    empty segments; [Tiling blog] section 11: all-masked rows give NaN if
+    unguarded).
+
+    q: [Lq, d], k: [Lk, d], v: [Lk, dv].  Returns (O [Lq, dv], LSE [Lq],
+    S [Lq, Lk], P [Lq, Lk]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lq, lk = q.shape[0], k.shape[0]
+    s = (q @ k.T) * scale
+    if causal:
+        i = np.arange(lq)[:, None]
+        j = np.arange(lk)[None, :]
+        s = np.where(j > i, NEG_INF, s)
+    if lk == 0:
+        m = np.full(lq, NEG_INF)
+    else:
+        m = s.max(axis=1)
+    live = np.isfinite(m)
+    m_safe = np.where(live, m, 0.0)
+    e = np.where(live[:, None], np.exp(s - m_safe[:, None]), 0.0)
+    l = e.sum(axis=1)
+    l_safe = np.where(l > 0, l, 1.0)
+    p = e / l_safe[:, None]
+    o = p @ v
+    lse = np.where(l > 0, m_safe + np.log(l_safe), NEG_INF)
+    return o, lse, s, p
+
+
+def attention_blockwise(q, k, v, scale, causal, block_rows, block_cols):
+    """FlashAttention-2 loop order, one head, float64.
+
+    [LLM book] 10.3.2 "tiled forward": for each Q row block i: m = -inf,
+    l = 0, O~ = 0; for each K/V column block j (skipped if the causal mask
+    hides all of it): S = Q_i K_j^T * scale, m_new = max(m, rowmax S),
+    l = l e^(m - m_new) + rowsum e^(S - m_new),
+    O~ = O~ e^(m - m_new) + e^(S - m_new) V_j, m = m_new; finally
+    O_i = O~ / l and LSE_i = m + ln l.  Masked entries inside a diagonal
+    block are -inf ([Tiling blog] section 06).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lq, lk = q.shape[0], k.shape[0]
+    o = np.zeros((lq, v.shape[1]))
+    lse = np.full(lq, NEG_INF)
+    for i0 in range(0, lq, block_rows):
+        i1 = min(i0 + block_rows, lq)
+        qi = q[i0:i1]
+        m = np.full(i1 - i0, NEG_INF)
+        l = np.zeros(i1 - i0)
+        acc = np.zeros((i1 - i0, v.shape[1]))
+        for j0 in range(0, lk, block_cols):
+            j1 = min(j0 + block_cols, lk)
+            if causal and j0 > i1 - 1:
+                continue  # whole block above the diagonal
+            s = (qi @ k[j0:j1].T) * scale
+            if causal:
+                ii = np.arange(i0, i1)[:, None]
+                jj = np.arange(j0, j1)[None, :]
+                s = np.where(jj > ii, NEG_INF, s)
+            m_new = np.maximum(m, s.max(axis=1))
+            live = np.isfinite(m_new)
+            m_new_safe = np.where(live, m_new, 0.0)
+            corr = np.where(np.isfinite(m), np.exp(m - m_new_safe), 0.0)
+            corr = np.where(live, corr, 1.0)
+            p = np.where(live[:, None], np.exp(s - m_new_safe[:, None]), 0.0)
+            l = l * corr + p.sum(axis=1)
+            acc = acc * corr[:, None] + p @ v[j0:j1]
+            m = m_new
+        nz = l > 0
+        o[i0:i1][nz] = acc[nz] / l[nz][:, None]
+        lse[i0:i1][nz] = m[nz] + np.log(l[nz])
+    return o, lse
+
+
+# --------------------------------------------------------------------------
+# Merge of attention states (the LSE merge operator)
+# --------------------------------------------------------------------------
+
+def merge_states(o_parts, lse_parts):
+    """Merge S partial attention states of one row.
+
+    [LLM book] 10.3.2 "LSE": two key segments with LSE_1, LSE_2 combine as
+    LSE = ln(e^LSE_1 + e^LSE_2) and the outputs are weighted by
+    e^(LSE_k - LSE).  [CUDA book] "Flash-Decoding and split-K": with
+    m = max_s m_s, weights w_s = e^(m_s - m) l_s, O = sum_s w_s O_s / l.
+    Written here in the LSE form with M = max_s LSE_s as the shift; a
+    segment with no keys (LSE = -inf) is skipped ([CUDA book] split-K merge
+    exercise).  If every segment is empty, O = 0 and LSE = -inf.
+
+    o_parts: [S, d] (each O_s already normalised), lse_parts: [S].
+    """
+    o_parts, lse_parts = _f64(o_parts), _f64(lse_parts)
+    live = np.isfinite(lse_parts)
+    if not live.any():
+        return np.zeros(o_parts.shape[1]), NEG_INF
+    big = float(lse_parts[live].max())
+    w = np.where(live, np.exp(np.where(live, lse_parts, 0.0) - big), 0.0)
+    total = float(w.sum())
+    o = (w[:, None] * np.where(live[:, None], o_parts, 0.0)).sum(axis=0) / total
+    return o, big + math.log(total)
+
+
+def merge_states_batched(o_parts, lse_parts):
+    """merge_states applied to every row: o_parts [rows, S, d], lse [rows, S]."""
+    o_parts, lse_parts = _f64(o_parts), _f64(lse_parts)
+    rows = o_parts.shape[0]
+    o = np.zeros((rows, o_parts.shape[2]))
+    lse = np.zeros(rows)
+    for r in range(rows):
+        o[r], lse[r] = merge_states(o_parts[r], lse_parts[r])
+    return o, lse
+
+
+# --------------------------------------------------------------------------
+# Batched prefill with grouped-query heads
+# --------------------------------------------------------------------------
+
+def kv_head_of(h, hq, hkv):
+    """GQA head mapping: query head h reads KV head h / (Hq / Hkv).
+
+    [CUDA book] "a paged decode attention kernel (with GQA)" and its GQA
+    exercise: with 32 query heads and 8 KV heads, each KV head serves
+    32 / 8 = 4 consecutive query heads.
+    """
+    return h // (hq // hkv)
+
+
+def prefill(q, k, v, scale, causal):
+    """Dense attention for every (batch, query head).
+
+    q: [B, Hq, Lq, d], k and v: [B, Hkv, Lk, d].  Returns O [B, Hq, Lq, d]
+    and LSE [B, Hq, Lq] (natural log), each head by attention_dense.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b_, hq, lq, _ = q.shape
+    hkv = k.shape[1]
+    o = np.zeros(q.shape[:3] + (v.shape[3],))
+    lse = np.zeros(q.shape[:3])
+    for b in range(b_):
+        for h in range(hq):
+            kh = kv_head_of(h, hq, hkv)
+            o[b, h], lse[b, h], _, _ = attention_dense(q[b, h], k[b, kh], v[b, kh], scale, causal)
+    return o, lse
+
+
+def prefill_rows(q, k, v, scale, causal, rows):
+    """Dense attention for selected query rows only.
+
+    rows: iterable of (b, h, i).  Row i of head h sees keys [0, Lk), or
+    [0, i] when causal ([Tiling blog] section 06).  Rows are grouped by
+    (b, h) so each group is one small dense problem with the masked scores
+    materialised.
+    """
+    rows = [tuple(int(x) for x in r) for r in rows]
+    hq, hkv = q.shape[1], k.shape[1]
+    out_o = np.zeros((len(rows), v.shape[3]))
+    out_lse = np.zeros(len(rows))
+    groups = {}
+    for n, (b, h, i) in enumerate(rows):
+        groups.setdefault((b, h), []).append((n, i))
+    for (b, h), items in groups.items():
+        kh = kv_head_of(h, hq, hkv)
+        idx = np.array([i for _, i in items])
+        qi = _f64(q[b, h][idx])
+        kk = _f64(k[b, kh])
+        vv = _f64(v[b, kh])
+        s = (qi @ kk.T) * scale
+        if causal:
+            s = np.where(np.arange(kk.shape[0])[None, :] > idx[:, None], NEG_INF, s)
+        m = s.max(axis=1)
+        live = np.isfinite(m)
+        m_safe = np.where(live, m, 0.0)
+        e = np.where(live[:, None], np.exp(s - m_safe[:, None]), 0.0)
+        l = e.sum(axis=1)
+        l_safe = np.where(l > 0, l, 1.0)
+        o = (e / l_safe[:, None]) @ vv
+        lse = np.where(l > 0, m_safe + np.log(l_safe), NEG_INF)
+        for (n, _), orow, lrow in zip(items, o, lse):
+            out_o[n] = orow
+            out_lse[n] = lrow
+    return out_o, out_lse
+
+
+# --------------------------------------------------------------------------
+# Paged KV cache and decode
+# --------------------------------------------------------------------------
+
+def paged_gather(pages, table_row, seq_len, kv_head):
+    """Logical-order K (or V) rows of one request and one KV head.
+
+    [CUDA book] "PagedAttention": token t lives in physical page
+    block_table[t / page_size], slot t % page_size.  pages has the layout
+    [num_pages, page_size, Hkv, d] ([CUDA book] paged decode listing; [LLM
+    book] 10.3.7 k_cache layout).  Table entries past ceil(seq_len /
+    page_size) are never read.
+    """
+    page_size = pages.shape[1]
+    out = np.zeros((seq_len, pages.shape[3]))
+    for t in range(seq_len):
+        page = int(table_row[t // page_size])
+        out[t] = pages[page, t % page_size, kv_head]
+    return out
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale):
+    """One query token per request against its paged KV cache.
+
+    q: [B, Hq, d]; k_pages, v_pages: [num_pages, page_size, Hkv, d];
+    block_table: [B, max_pages]; seq_lens: [B].  Gathers keys in logical
+    order (paged_gather) and applies attention_dense with Lq = 1 and no
+    mask.  Returns O [B, Hq, d] and LSE [B, Hq].
+    """
+    q = _f64(q)
+    k_pages = _f64(k_pages)
+    v_pages = _f64(v_pages)
+    b_, hq, _ = q.shape
+    hkv = k_pages.shape[2]
+    o = np.zeros(q.shape)
+    lse = np.zeros((b_, hq))
+    for b in range(b_):
+        n = int(seq_lens[b])
+        for kh in range(hkv):
+            kk = paged_gather(k_pages, block_table[b], n, kh)
+            vv = paged_gather(v_pages, block_table[b], n, kh)
+            heads = [h for h in range(hq) if kv_head_of(h, hq, hkv) == kh]
+            oo, ll, _, _ = attention_dense(q[b, heads], kk, vv, scale, False)
+            o[b, heads] = oo
+            lse[b, heads] = ll
+    return o, lse
+
+
+def decode_split_states(q_row, keys, values, scale, chunk):
+    """Split-KV partial states of one query row (Flash-Decoding).
+
+    [LLM book] 10.3.7 and [CUDA book] "Flash-Decoding and split-K": the keys
+    are cut along their length into segments of ``chunk`` tokens; each
+    segment yields its own normalised output O_s and LSE_s.  Returns
+    (o_parts [S, d], lse_parts [S]).
+    """
+    n = keys.shape[0]
+    nsplit = max(1, -(-n // chunk))
+    o_parts = np.zeros((nsplit, values.shape[1]))
+    lse_parts = np.full(nsplit, NEG_INF)
+    for s in range(nsplit):
+        lo, hi = s * chunk, min((s + 1) * chunk, n)
+        if hi > lo:
+            oo, ll, _, _ = attention_dense(_f64(q_row)[None, :], keys[lo:hi], values[lo:hi], scale)
+            o_parts[s], lse_parts[s] = oo[0], ll[0]
+    return o_parts, lse_parts
+
+
+# --------------------------------------------------------------------------
+# Split planning (host integer logic)
+# --------------------------------------------------------------------------
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
+    """Choose the KV chunk length of each request for split-KV decode.
+
+    Returns (chunk [B], splits [B]) with splits_b = ceil(len_b / chunk_b)
+    (at least 1) and every chunk a multiple of page_size.
+
+    Reading of the pages ([Lecture 4] sections 4.2 and 0.5, exercise 6):
+    one work unit is (request, KV head, segment); in the lecture's simple
+    GPU model each unit's time is proportional to the tokens it reads and
+    ``slots`` units run at once, so a plan costs
+    waves * (tokens of the largest unit), waves = ceil(units / slots).
+    * If the batch already has B * Hkv >= slots units, no request is split
+      ("when the batch is large there are enough work units; splitting only
+      adds merge overhead").
+    * Otherwise the candidate segment counts are the exercise's
+      S = 1, 2, 4, ..., 64; S gives the chunk
+      C = ceil(ceil(max_len / S) / page_size) * page_size, and request b
+      gets ceil(len_b / C) segments.  The cheapest plan wins; on a tie the
+      smaller S (fewer segments, less merging) wins.  This picks 8 segments
+      for 2 requests x 16384 tokens x 8 KV heads on 132 SMs, the
+      exercise's answer, and 16 segments (16x faster) for 1 x 32K.
+    * num_splits > 0 forces at most that many segments per request:
+      chunk_b = ceil(ceil(len_b / num_splits) / page_size) * page_size.
+    """
+    lens = [int(x) for x in seq_lens]
+    bsz = len(lens)
+    if num_splits > 0:
+        chunk = [max(page_size, _cdiv(_cdiv(n, num_splits), page_size) * page_size) for n in lens]
+        return chunk, [max(1, _cdiv(n, c)) for n, c in zip(lens, chunk)]
+    longest = max([1] + lens)
+    best_c, best_cost = max(page_size, _cdiv(longest, page_size) * page_size), None
+    if bsz * num_kv_heads < slots:
+        s = 1
+        while s <= 64:
+            c = max(page_size, _cdiv(_cdiv(longest, s), page_size) * page_size)
+            units = num_kv_heads * sum(max(1, _cdiv(n, c)) for n in lens)
+            cost = _cdiv(units, slots) * c
+            if best_cost is None or cost < best_cost:
+                best_c, best_cost = c, cost
+            s *= 2
+    return [best_c] * bsz, [max(1, _cdiv(n, best_c)) for n in lens]

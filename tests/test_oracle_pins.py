@@ -1,0 +1,362 @@
+"""Pins for the float64 oracle against things other than itself.
+
+Each test checks one oracle function against values printed on the pages
+(tests/golden/worked_examples.json), closed forms, brute force on tiny
+inputs, or an independent library routine (torch's float64 math attention,
+scipy's logsumexp / softmax).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import attention as orc
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")))
+
+
+def close(got, want, decimals):
+    tol = 10.0 ** (-decimals)
+    return abs(float(got) - float(want)) <= tol
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_safe_and_online_softmax_lecture_exercise_1():
+    g = GOLD["lecture_exercise_1"]
+    p, m, l = orc.safe_softmax(g["x"])
+    for got, want in zip(p, g["softmax"]):
+        assert close(got, want, g["decimals"]["softmax"])
+    m_final, l_final, trace = orc.online_softmax_stats(g["x"], 1)
+    for (tm, tl), want in zip(trace, g["trace"]):
+        assert tm == want["m"]
+        assert close(tl, want["l"], g["decimals"]["l"])
+    assert m_final == m and abs(l_final - l) < 1e-15
+
+
+def test_block_merge_tiling_blog_section_04():
+    g = GOLD["tiling_blog_two_merges"]
+    s, v = np.array(g["scores"], float), np.array(g["values"], float)[:, None]
+    b0, b1 = g["blocks"]
+    st0 = orc.block_state(s[b0], v[b0])
+    assert st0[0] == g["after_first_block"]["m"]
+    assert close(st0[1], g["after_first_block"]["l"], g["decimals"]["l"])
+    assert close(st0[2][0], g["after_first_block"]["a"], g["decimals"]["a"])
+    st = orc.merge_row_states(st0, orc.block_state(s[b1], v[b1]))
+    assert st[0] == g["after_merge"]["m"]
+    assert close(st[1], g["after_merge"]["l"], g["decimals"]["l"])
+    assert close(st[2][0], g["after_merge"]["a"], g["decimals"]["a"])
+    assert close(st[2][0] / st[1], g["o"], g["decimals"]["o"])
+    # the same row through the dense definition: d = 1, q = 1, k = scores
+    o, lse, _, _ = orc.attention_dense([[1.0]], s[:, None], v, 1.0)
+    assert close(o[0, 0], g["o"], g["decimals"]["o"])
+
+
+@pytest.mark.parametrize("name", ["llm_book_max_not_refreshed", "llm_book_max_refreshed"])
+def test_online_update_llm_book(name):
+    g = GOLD[name]
+    s, v = np.array(g["scores"], float), np.array(g["values"], float)[:, None]
+    b0, b1 = g["blocks"]
+    st0 = orc.block_state(s[b0], v[b0])
+    assert st0[0] == g["after_first_block"]["m"]
+    assert close(st0[1], g["after_first_block"]["l"], g["decimals"]["l"])
+    assert close(st0[2][0], g["after_first_block"]["o_tilde"], g["decimals"]["o_tilde"])
+    st = orc.merge_row_states(st0, orc.block_state(s[b1], v[b1]))
+    assert close(st[1], g["final"]["l"], g["decimals"]["l"])
+    assert close(st[2][0], g["final"]["o_tilde"], g["decimals"]["o_tilde"])
+    assert close(st[2][0] / st[1], g["o"], g["decimals"]["o"])
+    if "correction" in g:
+        assert close(math.exp(st0[0] - st[0]), g["correction"], g["decimals"]["correction"])
+    # blockwise FA2 order with one-column blocks reproduces the same output
+    for bc in (1, 2, 3):
+        o, _ = orc.attention_blockwise([[1.0]], s[:, None], v, 1.0, False, 1, bc)
+        assert close(o[0, 0], g["o"], g["decimals"]["o"])
+
+
+def test_weights_and_lse_llm_book():
+    g = GOLD["llm_book_softmax_weights_and_lse"]
+    s, v = np.array(g["scores"], float), np.array(g["values"], float)[:, None]
+    o, lse, _, p = orc.attention_dense([[1.0]], s[:, None], v, 1.0)
+    for got, want in zip(p[0], g["weights"]):
+        assert close(got, want, g["decimals"]["weights"])
+    assert close(o[0, 0], g["o"], g["decimals"]["o"])
+    assert close(lse[0], g["lse"], g["decimals"]["lse"])
+    # the LSE merge of the two segments [1,3] | [2] gives the same O and LSE
+    parts_o, parts_l = [], []
+    for idx in ([0, 1], [2]):
+        oo, ll, _, _ = orc.attention_dense([[1.0]], s[idx][:, None], v[idx], 1.0)
+        parts_o.append(oo[0]); parts_l.append(ll[0])
+    mo, ml = orc.merge_states(np.array(parts_o), np.array(parts_l))
+    assert close(mo[0], g["o"], g["decimals"]["o"])
+    assert close(ml, g["lse"], g["decimals"]["lse"])
+
+
+def test_cuda_book_exercise_1():
+    g = GOLD["cuda_book_exercise_1"]
+    (s0, s1), (v0, v1) = g["blocks_scores"], g["blocks_values"]
+    st0 = orc.block_state(s0, np.array(v0, float)[:, None])
+    assert st0[0] == g["after_first_block"]["m"]
+    assert close(st0[1], g["after_first_block"]["l"], g["decimals"]["l"])
+    assert close(st0[2][0], g["after_first_block"]["o_tilde"], g["decimals"]["o_tilde"])
+    st = orc.merge_row_states(st0, orc.block_state(s1, np.array(v1, float)[:, None]))
+    assert st[0] == g["after_second_block"]["m"]
+    assert close(st[1], g["after_second_block"]["l"], g["decimals"]["l"])
+    assert close(st[2][0], g["after_second_block"]["o_tilde"], g["decimals"]["o_tilde"])
+    assert close(st[2][0] / st[1], g["o"], g["decimals"]["o"])
+    # direct computation printed beside it
+    s = np.array(s0 + s1, float)
+    assert close(np.exp(s).sum(), g["direct_weight_sum"], g["decimals"]["direct_weight_sum"])
+    for got, want in zip(np.exp(s), g["direct_weights_unnormalised"]):
+        assert abs(got - want) / want < 1e-3
+    # the split-K merge of the two normalised segment outputs (LSE form)
+    o0, l0, _, _ = orc.attention_dense([[1.0]], np.array(s0, float)[:, None], np.array(v0, float)[:, None], 1.0)
+    o1, l1, _, _ = orc.attention_dense([[1.0]], np.array(s1, float)[:, None], np.array(v1, float)[:, None], 1.0)
+    mo, _ = orc.merge_states(np.array([o0[0], o1[0]]), np.array([l0[0], l1[0]]))
+    assert close(mo[0], g["o"], g["decimals"]["o"])
+
+
+# ---------------------------------------------------------------- dense attention vs a library
+
+def _sdpa64(q, k, v, scale, causal):
+    """torch's math attention in float64 (independent code path)."""
+    q, k, v = (torch.as_tensor(np.asarray(x, np.float64)) for x in (q, k, v))
+    hq, hkv = q.shape[-3], k.shape[-3]
+    if hq != hkv:
+        k = k.repeat_interleave(hq // hkv, dim=-3)
+        v = v.repeat_interleave(hq // hkv, dim=-3)
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    with sdpa_kernel(SDPBackend.MATH):
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+    s = (q @ k.transpose(-1, -2)) * scale
+    if causal:
+        lq, lk = s.shape[-2], s.shape[-1]
+        mask = torch.ones(lq, lk, dtype=torch.bool).triu(1)
+        s = s.masked_fill(mask, -math.inf)
+    return o.numpy(), torch.logsumexp(s, dim=-1).numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("lq,lk", [(17, 17), (64, 64), (1, 9), (33, 70)])
+def test_dense_matches_torch_math_attention(causal, lq, lk):
+    if causal and lq != lk:
+        pytest.skip("causal is defined for square problems here")
+    rng = np.random.default_rng(11)
+    q, k, v = rng.standard_normal((lq, 32)), rng.standard_normal((lk, 32)), rng.standard_normal((lk, 24))
+    o, lse, s, p = orc.attention_dense(q, k, v, 0.3, causal)
+    o_ref, lse_ref = _sdpa64(q[None], k[None], v[None], 0.3, causal)
+    assert np.abs(o - o_ref[0]).max() < 1e-12
+    assert np.abs(lse - lse_ref[0]).max() < 1e-12
+    assert np.abs(lse - scipy.special.logsumexp(s, axis=1)).max() < 1e-12
+    assert np.abs(p - scipy.special.softmax(s, axis=1)).max() < 1e-13
+
+
+def test_prefill_gqa_matches_torch_math_attention():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((2, 8, 40, 16))
+    k = rng.standard_normal((2, 2, 40, 16))
+    v = rng.standard_normal((2, 2, 40, 16))
+    for causal in (False, True):
+        o, lse = orc.prefill(q, k, v, 0.25, causal)
+        o_ref, lse_ref = _sdpa64(q, k, v, 0.25, causal)
+        assert np.abs(o - o_ref).max() < 1e-12
+        assert np.abs(lse - lse_ref).max() < 1e-12
+        rows = [(1, 7, 39), (0, 0, 0), (1, 3, 17), (0, 5, 1)]
+        ro, rl = orc.prefill_rows(q, k, v, 0.25, causal, rows)
+        for n, (b, h, i) in enumerate(rows):
+            assert np.abs(ro[n] - o_ref[b, h, i]).max() < 1e-12
+            assert abs(rl[n] - lse_ref[b, h, i]) < 1e-12
+
+
+# ---------------------------------------------------------------- invariants and closed forms
+
+def test_invariants_rows_sum_to_one_and_hull():
+    rng = np.random.default_rng(3)
+    q, k, v = rng.standard_normal((50, 8)), rng.standard_normal((50, 8)), rng.standard_normal((50, 8))
+    for causal in (False, True):
+        o, lse, s, p = orc.attention_dense(q, k, v, 1.0 / math.sqrt(8), causal)
+        assert np.abs(p.sum(axis=1) - 1.0).max() < 1e-14
+        m = s.max(axis=1)
+        l = np.exp(s - m[:, None]).sum(axis=1)
+        assert np.abs(lse - (m + np.log(l))).max() < 1e-13
+        assert (lse >= m - 1e-15).all()
+        for i in range(50):
+            vis = v[: i + 1] if causal else v
+            assert (o[i] >= vis.min(axis=0) - 1e-12).all() and (o[i] <= vis.max(axis=0) + 1e-12).all()
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(4)
+    k, v = rng.standard_normal((20, 8)), rng.standard_normal((20, 8))
+    # q = 0: uniform weights, O = mean of the visible values, LSE = ln(#visible)
+    o, lse, _, _ = orc.attention_dense(np.zeros((20, 8)), k, v, 0.5, True)
+    for i in range(20):
+        assert np.abs(o[i] - v[: i + 1].mean(axis=0)).max() < 1e-13
+        assert abs(lse[i] - math.log(i + 1)) < 1e-13
+    # causal row 0 sees only key 0
+    q = rng.standard_normal((20, 8))
+    o, lse, s, _ = orc.attention_dense(q, k, v, 0.5, True)
+    assert np.abs(o[0] - v[0]).max() < 1e-15 and abs(lse[0] - 0.5 * q[0] @ k[0]) < 1e-14
+    # one key: O = v_0
+    o, _, _, _ = orc.attention_dense(q, k[:1], v[:1], 0.5, False)
+    assert np.abs(o - v[0]).max() < 1e-15
+    # identical keys: O = mean(V)
+    o, _, _, _ = orc.attention_dense(q, np.tile(k[:1], (20, 1)), v, 0.5, False)
+    assert np.abs(o - v.mean(axis=0)).max() < 1e-13
+    # no keys at all: O = 0, LSE = -inf (no NaN)
+    o, lse, _, _ = orc.attention_dense(q, k[:0], v[:0], 0.5, False)
+    assert (o == 0).all() and np.isneginf(lse).all()
+
+
+# ---------------------------------------------------------------- orderings (brute force)
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("length", [1, 7, 64])
+def test_blockwise_orders_equal_dense(causal, length):
+    """[Lecture 4] 3.3: tiled and dense agree for several tile sizes."""
+    rng = np.random.default_rng(length)
+    q, k, v = (rng.standard_normal((length, 16)) for _ in range(3))
+    o_ref, lse_ref, _, _ = orc.attention_dense(q, k, v, 0.25, causal)
+    for br in (1, 3, 16, length):
+        for bc in (1, 3, 16, length):
+            o, lse = orc.attention_blockwise(q, k, v, 0.25, causal, br, bc)
+            assert np.abs(o - o_ref).max() < 1e-13
+            assert np.abs(lse - lse_ref).max() < 1e-13
+
+
+@pytest.mark.parametrize("segments", [2, 8, 64])
+def test_split_then_merge_equals_dense(segments):
+    """[Lecture 4] 4.3: one query, 10^4 keys, 2/8/64 segments, FP64 ~1e-16."""
+    rng = np.random.default_rng(segments)
+    q = rng.standard_normal(64)
+    k, v = rng.standard_normal((10000, 64)), rng.standard_normal((10000, 64))
+    o_ref, lse_ref, _, _ = orc.attention_dense(q[None], k, v, 0.125)
+    chunk = -(-10000 // segments)
+    op, lp = orc.decode_split_states(q, k, v, 0.125, chunk)
+    assert op.shape[0] == segments
+    o, lse = orc.merge_states(op, lp)
+    assert np.abs(o - o_ref[0]).max() < 1e-14
+    assert abs(lse - lse_ref[0]) < 1e-12
+    # commutative: reversed and shuffled orders agree in double
+    o2, lse2 = orc.merge_states(op[::-1], lp[::-1])
+    perm = rng.permutation(segments)
+    o3, lse3 = orc.merge_states(op[perm], lp[perm])
+    assert np.abs(o2 - o).max() < 1e-14 and np.abs(o3 - o).max() < 1e-14
+    assert abs(lse2 - lse) < 1e-12 and abs(lse3 - lse) < 1e-12
+    # associative: merging merged halves gives the same state
+    h = segments // 2
+    oa, la = orc.merge_states(op[:h], lp[:h])
+    ob, lb = orc.merge_states(op[h:], lp[h:])
+    o4, lse4 = orc.merge_states(np.array([oa, ob]), np.array([la, lb]))
+    assert np.abs(o4 - o).max() < 1e-14 and abs(lse4 - lse) < 1e-12
+
+
+def test_merge_skips_empty_segments():
+    rng = np.random.default_rng(9)
+    op, lp = rng.standard_normal((4, 8)), rng.standard_normal(4)
+    lp2 = lp.copy(); lp2[2] = -math.inf
+    op2 = op.copy(); op2[2] = np.nan  # contents of an empty segment must not be read
+    o, lse = orc.merge_states(op2, lp2)
+    o_ref, lse_ref = orc.merge_states(op[[0, 1, 3]], lp[[0, 1, 3]])
+    assert np.abs(o - o_ref).max() < 1e-15 and abs(lse - lse_ref) < 1e-15
+    o, lse = orc.merge_states(op, np.full(4, -math.inf))
+    assert (o == 0).all() and lse == -math.inf
+    assert abs(orc.merge_states(op[:1], lp[:1])[1] - lp[0]) < 1e-15
+
+
+# ---------------------------------------------------------------- paging and GQA
+
+def test_bsr_page_tables_lecture_5_2():
+    g = GOLD["lecture_bsr_page_tables"]
+    bs = g["block_size"]
+    num_pages = max(max(t) for t in g["tables"]) + 1
+    # page p, slot s of KV head 0 holds the integer 1000 * p + s (exact in float)
+    pages = np.zeros((num_pages, bs, 1, 2))
+    for p in range(num_pages):
+        for s in range(bs):
+            pages[p, s, 0] = [1000 * p + s, p]
+    indices, indptr = [], [0]
+    for n, table in zip(g["seq_lens"], g["tables"]):
+        rows = orc.paged_gather(pages, table, n, 0)
+        assert rows.shape[0] == n
+        used = []
+        for t in range(n):
+            assert rows[t, 0] == 1000 * table[t // bs] + t % bs
+            if not used or used[-1] != int(rows[t, 1]):
+                used.append(int(rows[t, 1]))
+        indices += used
+        indptr.append(len(indices))
+    assert indices == g["indices"] and indptr == g["indptr"]
+
+
+def test_gqa_mapping_cuda_book_exercise_3():
+    g = GOLD["gqa_head_sharing"]
+    heads = [orc.kv_head_of(h, g["num_heads"], g["num_kv_heads"]) for h in range(g["num_heads"])]
+    for kh in range(g["num_kv_heads"]):
+        assert heads.count(kh) == g["group"]
+        assert heads[kh * g["group"]: (kh + 1) * g["group"]] == [kh] * g["group"]
+
+
+def test_decode_paged_equals_contiguous_attention():
+    """[Lecture 4] 5.2: attention over the paged layout equals attention over
+    the same keys stored contiguously (max diff 0)."""
+    rng = np.random.default_rng(21)
+    lens, page, hkv, hq, d = [1, 17, 40, 64], 16, 2, 8, 32
+    contig_k = [rng.standard_normal((hkv, n, d)) for n in lens]
+    contig_v = [rng.standard_normal((hkv, n, d)) for n in lens]
+    npages = sum(-(-n // page) for n in lens)
+    perm = rng.permutation(npages)
+    kp = np.zeros((npages, page, hkv, d)); vp = np.zeros_like(kp)
+    table = -np.ones((4, 4), dtype=np.int64)
+    off = 0
+    for b, n in enumerate(lens):
+        for i in range(-(-n // page)):
+            table[b, i] = perm[off]; off += 1
+            for s in range(page):
+                t = i * page + s
+                if t < n:
+                    kp[table[b, i], s] = contig_k[b][:, t]
+                    vp[table[b, i], s] = contig_v[b][:, t]
+    q = rng.standard_normal((4, hq, d))
+    o, lse = orc.decode_paged(q, kp, vp, table, lens, 0.2)
+    for b, n in enumerate(lens):
+        o_ref, lse_ref = _sdpa64(q[b][:, None, :], contig_k[b], contig_v[b], 0.2, False)
+        assert np.abs(o[b] - o_ref[:, 0]).max() < 1e-12
+        assert np.abs(lse[b] - lse_ref[:, 0]).max() < 1e-12
+
+
+# ---------------------------------------------------------------- split planning
+
+def test_plan_lecture_exercise_6():
+    g = GOLD["lecture_exercise_6_split_count"]
+    chunk, splits = orc.plan_splits(g["seq_lens"], g["num_kv_heads"], g["slots"], 16)
+    assert splits == [g["best_splits"]] * len(g["seq_lens"])
+
+
+def test_plan_lecture_split_kv_speedup():
+    g = GOLD["lecture_split_kv_speedup"]
+    chunk, splits = orc.plan_splits(g["seq_lens"], g["num_kv_heads"], g["slots"], 16)
+    units = g["num_kv_heads"] * sum(splits)
+    assert units <= g["slots"]
+    # lecture model: time = waves x tokens per unit; unsplit = one unit of 32K
+    assert g["seq_lens"][0] // chunk[0] == g["speedup"]
+
+
+def test_plan_invariants():
+    rng = np.random.default_rng(2)
+    for _ in range(50):
+        lens = rng.integers(0, 140000, size=int(rng.integers(1, 9))).tolist()
+        hkv = int(rng.choice([1, 2, 8]))
+        slots = int(rng.choice([132, 152, 304, 608]))
+        for forced in (0, 1, 3, 64):
+            chunk, splits = orc.plan_splits(lens, hkv, slots, 16, forced)
+            for n, c, s in zip(lens, chunk, splits):
+                assert c % 16 == 0 and c >= 16 and s >= 1
+                assert s * c >= n and (s - 1) * c < max(n, 1)
+                if forced:
+                    assert s <= forced
+    # enough units already: nothing is split
+    assert orc.plan_splits([1024] * 256, 8, 152, 16)[1] == [1] * 256
