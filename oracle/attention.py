@@ -409,15 +409,16 @@ def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
       smaller S (fewer segments, less merging) wins.  This picks 8 segments
       for 2 requests x 16384 tokens x 8 KV heads on 132 SMs, the
       exercise's answer, and 16 segments (16x faster) for 1 x 32K.
-    * num_splits > 0 forces at most that many segments per request:
-      chunk_b = ceil(ceil(len_b / num_splits) / page_size) * page_size.
+    * num_splits > 0 forces at most that many segments per request, with
+      one chunk for all requests:
+      C = ceil(ceil(max_len / num_splits) / page_size) * page_size.
     """
     lens = [int(x) for x in seq_lens]
     bsz = len(lens)
-    if num_splits > 0:
-        chunk = [max(page_size, _cdiv(_cdiv(n, num_splits), page_size) * page_size) for n in lens]
-        return chunk, [max(1, _cdiv(n, c)) for n, c in zip(lens, chunk)]
     longest = max([1] + lens)
+    if num_splits > 0:
+        c = max(page_size, _cdiv(_cdiv(longest, num_splits), page_size) * page_size)
+        return [c] * bsz, [max(1, _cdiv(n, c)) for n in lens]
     best_c, best_cost = max(page_size, _cdiv(longest, page_size) * page_size), None
     if bsz * num_kv_heads < slots:
         s = 1
