@@ -317,7 +317,7 @@ def prefill_rows(q, k, v, scale, causal, rows):
 # --------------------------------------------------------------------------
 
 def paged_gather(pages, table_row, seq_len, kv_head):
-    """Logical-order K (or V) rows of one request and one KV head.
+    """Logical-order K (or V) rows of one request and one KV head, in float64.
 
     [CUDA book] "PagedAttention": token t lives in physical page
     block_table[t / page_size], slot t % page_size.  pages has the layout
@@ -326,11 +326,10 @@ def paged_gather(pages, table_row, seq_len, kv_head):
     page_size) are never read.
     """
     page_size = pages.shape[1]
-    out = np.zeros((seq_len, pages.shape[3]))
-    for t in range(seq_len):
-        page = int(table_row[t // page_size])
-        out[t] = pages[page, t % page_size, kv_head]
-    return out
+    t = np.arange(int(seq_len))
+    page_of_token = np.asarray(table_row)[t // page_size].astype(np.int64)
+    slot_of_token = t % page_size
+    return _f64(pages[page_of_token, slot_of_token, kv_head])
 
 
 def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale):
@@ -342,8 +341,6 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale):
     mask.  Returns O [B, Hq, d] and LSE [B, Hq].
     """
     q = _f64(q)
-    k_pages = _f64(k_pages)
-    v_pages = _f64(v_pages)
     b_, hq, _ = q.shape
     hkv = k_pages.shape[2]
     o = np.zeros(q.shape)
