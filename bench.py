@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on one GB300 (or N replicas).
+
+One step = one call of the hot path on one batch of synthetic, seeded
+N(0,1) input already resident in device memory:
+
+* main workload (the line's ``value``): GPT-2-medium-shaped causal bf16
+  prefill with LSE, B=64, H=16, L=1024, d=64 -> causal-aware attention
+  TFLOP/s = 4*B*H*L*L*d*(1/2) / t.
+* secondary workloads (``workloads``): the other shapes of the same operator
+  (fp32 single head, Llama-3-8B GQA prefill at 8K and 32K, batched paged
+  decode B=256 x 1024, long-context split-KV decode B=4), each with its own
+  metric (TFLOP/s for prefill, unique KV GB/s for decode) and roofline.
+
+Timing: W warm-up steps, then exactly K timed steps; before every timed step
+a 256 MiB buffer is written to flush L2 (outside the step's events); each
+step is timed with CUDA events on the stream the kernels are launched on;
+barrier + synchronize on both sides; max over ranks.  ``--impl reference``
+times the float64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOPS & paged-decode KV GB/s on 1 GB300, % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOADS = {
+    "gpt2-medium-prefill": dict(kind="prefill", B=64, Hq=16, Hkv=16, L=1024, d=64, causal=True,
+                                dtype="bf16"),
+    "single-head-f32-causal": dict(kind="prefill", B=1, Hq=1, Hkv=1, L=256, d=64, causal=True,
+                                   dtype="f32"),
+    "single-head-f32": dict(kind="prefill", B=1, Hq=1, Hkv=1, L=256, d=64, causal=False,
+                            dtype="f32"),
+    "llama3-8b-prefill-8k": dict(kind="prefill", B=1, Hq=32, Hkv=8, L=8192, d=128, causal=True,
+                                 dtype="bf16"),
+    "llama3-8b-prefill-32k": dict(kind="prefill", B=1, Hq=32, Hkv=8, L=32768, d=128, causal=True,
+                                  dtype="bf16"),
+    "decode-b256-ctx1024": dict(kind="decode", B=256, Hq=32, Hkv=8, d=128, lens="1024x256"),
+    "decode-b4-long-splitkv": dict(kind="decode", B=4, Hq=32, Hkv=8, d=128, lens="uniform"),
+}
+MAIN = "gpt2-medium-prefill"
+
+
+def describe(name):
+    w = WORKLOADS[name]
+    if w["kind"] == "prefill":
+        return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} L={w['L']} d={w['d']} "
+                f"{'causal' if w['causal'] else 'non-causal'} {w['dtype']} + LSE")
+    lens = "ctx 1024 each" if w["lens"] == "1024x256" else "ctx U[4096,131072] seed 2"
+    return f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, {lens}, 16-token shuffled pages"
+
+
+def decode_lens(w):
+    from exact_attention_sm_gb300 import inputs
+    if w["lens"] == "1024x256":
+        return [1024] * w["B"]
+    return inputs.decode_lengths_uniform(w["B"], 4096, 131072, seed=2)
+
+
+def prefill_flops(w, rows=None):
+    """Causal-aware attention FLOPs: 4 * d per (query, visible key) pair; the
+    x1/2 convention for causal (the CUDA handbook's FlashAttention listing)."""
+    L, d = w["L"], w["d"]
+    if rows is None:
+        per_head = L * L * (0.5 if w["causal"] else 1.0)
+        return 4.0 * d * w["B"] * w["Hq"] * per_head
+    return float(sum(4.0 * d * ((i + 1) if w["causal"] else L) for (_, _, i) in rows))
+
+
+def decode_bytes(w, lens):
+    """Unique KV bytes: sum_b len_b * Hkv * d * 2 (K and V) * 2 bytes."""
+    return float(sum(lens)) * w["Hkv"] * w["d"] * 2 * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "exact_attention_sm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"prefill": ["prefill_sm103.cu", "common.cuh"],
+                  "prefill_f32": ["prefill_f32.cu", "common.cuh"],
+                  "decode": ["decode_paged.cu", "common.cuh"]}
+
+
+def traffic_for(workload, kind):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    e = table.get(workload)
+    if not e or e.get("source_sha") != source_sha(KERNEL_SOURCES[kind]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi sampler around the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if self.proc is None or not self.out:
+            return None
+        rows = []
+        for line in self.out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, x in enumerate(r) if x == "Active"})
+        top = max(r[0] for r in rows)
+        loaded = sorted(r[0] for r in rows if r[0] >= 0.5 * top)
+        return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    n = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), n
+
+
+def reduce_max(value, backend_ready):
+    """Max over ranks (identity when not distributed)."""
+    if not backend_ready:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(backend_ready):
+    if backend_ready:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def make_step(name, torch, ea, inputs):
+    """Allocates the workload's inputs on the GPU and returns
+    (step_fn, launches_per_step, work, unit_kind, lens)."""
+    w = WORKLOADS[name]
+    if w["kind"] == "prefill":
+        q, k, v = inputs.prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["L"], w["L"], w["d"], w["dtype"],
+                                        seed=0, device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty(w["B"], w["Hq"], w["L"], dtype=torch.float32, device="cuda")
+        scale = 1.0 / math.sqrt(w["d"])
+
+        def step():
+            ea.attn_fwd(q, k, v, causal=w["causal"], scale=scale, out=o, lse=lse)
+        return step, 1, prefill_flops(w), "flops", None
+    lens = decode_lens(w)
+    q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0,
+                                                device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(w["B"], w["Hq"], dtype=torch.float32, device="cuda")
+    chunk, smax = ea.attn_decode_plan(lens, w["Hkv"], 16, 0)
+    nbytes = ea.attn_decode_workspace_bytes(w["B"], w["Hq"], w["d"], smax)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+
+    def step():
+        ea.attn_decode_paged(q, kp, vp, table, sl, seq_lens_host=lens, out=o, lse=lse,
+                             workspace=ws)
+    return step, (1 if smax == 1 else 2), decode_bytes(w, lens), "bytes", (lens, chunk, smax)
+
+
+def time_steps(torch, step, steps, warmup, flush):
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def measure(name, torch, ea, inputs, steps, warmup, flush, peaks, peak_src):
+    step, launches, work, kind, extra = make_step(name, torch, ea, inputs)
+    ms = time_steps(torch, step, steps, warmup, flush)
+    mean_ms = sum(ms) / len(ms)
+    w = WORKLOADS[name]
+    if kind == "flops":
+        value = work / (mean_ms * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        if w["dtype"] == "bf16":
+            roof = {"bound": "tensor", "achieved": value, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+        else:
+            # fp32 FFMA on CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz max clock
+            roof = {"bound": "alu", "achieved": value, "peak": 152 * 128 * 2 * 2.07e9 / 1e12,
+                    "unit": "TFLOP/s", "peak_source": "fp32 FMA: 152 SM x 128 lanes x 2 x 2.07 GHz"}
+        tkind = "prefill" if w["dtype"] == "bf16" else "prefill_f32"
+    else:
+        value = work / (mean_ms * 1e-3) / 1e9
+        unit = "GB/s"
+        roof = {"bound": "hbm", "achieved": value, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"hbm_gbs of {peak_src}"}
+        tkind = "decode"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_for(name, tkind)
+    out = {"workload": describe(name), "value": value, "unit": unit, "ms_per_step": mean_ms,
+           "ms_min": min(ms), "launches_per_step": launches, "roofline": roof,
+           "algorithmic_" + kind: work}
+    if extra is not None:
+        out["split_plan"] = {"chunk": extra[1], "max_splits": extra[2]}
+    return out, step, launches, work
+
+
+def e2e_prefill(torch, ea, steps, warmup):
+    """Same metric through the public API with host (pinned) buffers: every
+    step copies q, k, v host->device, runs attn_fwd, copies O and LSE back."""
+    from exact_attention_sm_gb300 import inputs
+    w = WORKLOADS[MAIN]
+    q, k, v = inputs.prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["L"], w["L"], w["d"], "bf16",
+                                    seed=0, device="cuda")
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty_like(hq).pin_memory()
+    hl = torch.empty(w["B"], w["Hq"], w["L"], dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    do = torch.empty_like(q)
+    dl = torch.empty(w["B"], w["Hq"], w["L"], dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(w["d"])
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ea.attn_fwd(dq, dk, dv, causal=True, scale=scale, out=do, lse=dl)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return {"value": prefill_flops(w) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(name, budget_s):
+    """Times the float64 oracle, as it stands, on a bounded sample of the
+    workload; returns (value in the workload's unit, seconds, sample text)."""
+    import numpy as np
+    from exact_attention_sm_gb300 import inputs
+    from oracle import attention as orc
+    w = WORKLOADS[name]
+    if w["kind"] == "prefill":
+        q, k, v = inputs.prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["L"], w["L"], w["d"],
+                                        w["dtype"], seed=0)
+        qn, kn, vn = (t.float().numpy() for t in (q, k, v))
+        rows = inputs.sample_rows(w["B"], w["Hq"], w["L"], n_random=100000, seed=3)
+        done, flops, t0 = 0, 0.0, time.perf_counter()
+        while done < len(rows) and time.perf_counter() - t0 < budget_s:
+            batch = rows[done:done + 256]
+            orc.prefill_rows(qn, kn, vn, 1.0 / math.sqrt(w["d"]), w["causal"], batch)
+            flops += prefill_flops(w, batch)
+            done += len(batch)
+        dt = time.perf_counter() - t0
+        return flops / dt / 1e12, dt, f"{done} sampled query rows (seeded), each the full dense row"
+    lens = decode_lens(w)
+    nreq = 1 if w["lens"] != "1024x256" else 16
+    q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0)
+    qn, kpn, vpn = (t.float().numpy() for t in (q, kp, vp))
+    done, nbytes, t0 = 0, 0.0, time.perf_counter()
+    while done < len(lens) and time.perf_counter() - t0 < budget_s:
+        idx = list(range(done, min(done + nreq, len(lens))))
+        orc.decode_paged(qn[idx], kpn, vpn, table.numpy()[idx], [lens[i] for i in idx],
+                         1.0 / math.sqrt(w["d"]))
+        nbytes += decode_bytes(w, [lens[i] for i in idx])
+        done += len(idx)
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt, f"{done} of {len(lens)} requests, all heads"
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    per_step = []
+    for _ in range(args.warmup):
+        oracle_sample(MAIN, 1.0)
+    sample = ""
+    for _ in range(args.steps):
+        v, dt, sample = oracle_sample(MAIN, args.ref_budget)
+        per_step.append((v, dt))
+    value = sum(v for v, _ in per_step) / len(per_step)
+    ms = sum(dt for _, dt in per_step) / len(per_step) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": describe(MAIN), "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args):
+    import torch
+    rank, local_rank, world = dist_env()
+    dist_ready = False
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+        dist_ready = True
+    else:
+        torch.cuda.set_device(0)
+    import exact_attention_sm_gb300 as ea
+    from exact_attention_sm_gb300 import inputs
+    ea.lib()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    main_name = args.workload
+    barrier(dist_ready)
+    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as clk:
+        res, step, launches, work = measure(main_name, torch, ea, inputs, args.steps, args.warmup,
+                                            flush, peaks, peak_src)
+    torch.cuda.synchronize()
+    barrier(dist_ready)
+    total_s = res["ms_per_step"] * args.steps * 1e-3
+    total_s = reduce_max(total_s, dist_ready)
+    unit = res["unit"]
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    value = world * work * args.steps / total_s / scale
+
+    secondary = []
+    if not args.main_only and world == 1:
+        for name in WORKLOADS:
+            if name == main_name:
+                continue
+            try:
+                r, _, _, _ = measure(name, torch, ea, inputs, args.steps, args.warmup, flush, peaks,
+                                     peak_src)
+            except Exception as exc:  # report, do not hide
+                r = {"workload": describe(name), "error": str(exc)}
+            secondary.append(r)
+            torch.cuda.empty_cache()
+    e2e = None
+    if WORKLOADS[main_name]["kind"] == "prefill" and main_name == MAIN:
+        e2e = e2e_prefill(torch, ea, args.steps, args.warmup)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        v, dt, sample = oracle_sample(main_name, args.cpu_budget)
+        cpu = {"value": v, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{sample}; {dt:.1f} s of CPU time"}
+    w = WORKLOADS[main_name]
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": w.get("dtype", "bf16"), "data": "synthetic",
+        "config": {"workload": res["workload"],
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches * args.steps, "clocks": clk.summary(),
+        "workloads": secondary,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=MAIN, choices=sorted(WORKLOADS))
+    ap.add_argument("--main-only", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=2.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

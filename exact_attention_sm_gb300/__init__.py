@@ -1,0 +1,180 @@
+"""GB300 (sm_103a) exact attention: thin Python binding over libattn.so.
+
+Every function below only marshals arguments (torch tensors -> device
+pointers and sizes) and calls the C ABI declared in ``include/attn.h``; all
+arithmetic runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_F32, ATTN_BF16 = 0, 1
+STATUS = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_WORKSPACE",
+    4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_DEVICE_TIMEOUT", 6: "ATTN_ERR_BAD_INDEX",
+}
+
+# Every symbol include/attn.h declares, with its ctypes signature.
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_decode_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
+    "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F,
+                               _P, _SZ, _I, _P]),
+    "attn_merge_states": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P]),
+    "attn_get_device_status": (_I, [_P]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_version": (_I, []),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def lib():
+    """The loaded libattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m exact_attention_sm_gb300.build`")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(h, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = h
+    return _lib
+
+
+def _check(status, where):
+    if status != 0:
+        raise AttnError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t, name):
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, want_lse=True, stream=None):
+    """Prefill attention. q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] -> (o [B,Hq,Lq,d], lse [B,Hq,Lq] fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, Lq, dtype=torch.float32, device=q.device)
+    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, Lk, d,
+                        int(bool(causal)), float(scale), _dtype_code(q), _stream(stream))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_decode_plan(seq_lens_host, num_kv_heads, page_size=16, num_splits=0, slots=0):
+    """Host planner: returns (chunk, max_splits) for the given context lengths."""
+    lens = (ctypes.c_int32 * len(seq_lens_host))(*[int(x) for x in seq_lens_host])
+    chunk, smax = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = lib().attn_decode_plan(ctypes.cast(lens, ctypes.c_void_p), len(seq_lens_host),
+                                int(num_kv_heads), int(page_size), int(num_splits), int(slots),
+                                ctypes.byref(chunk), ctypes.byref(smax))
+    _check(st, "attn_decode_plan")
+    return chunk.value, smax.value
+
+
+def attn_decode_workspace_bytes(B, Hq, d, max_splits):
+    return int(lib().attn_decode_workspace_bytes(int(B), int(Hq), int(d), int(max_splits)))
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=None,
+                      num_splits=0, scale=None, out=None, lse=None, workspace=None,
+                      want_lse=True, stream=None):
+    """Paged GQA decode. q [B,Hq,d]; k/v_pages [num_pages,page,Hkv,d]; block_table int32
+    [B,max_pages]; seq_lens int32 [B] on the device; seq_lens_host: list/array or None.
+    Allocates the split workspace when none is given. Returns (o [B,Hq,d], lse [B,Hq])."""
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"),
+                 (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _need(t, n)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    host_arr = None
+    if seq_lens_host is not None:
+        host_arr = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens_host])
+    if workspace is None and num_splits != 1:
+        if seq_lens_host is None:
+            seq_lens_host = seq_lens.cpu().tolist()
+        _, smax = attn_decode_plan(seq_lens_host, Hkv, page_size, num_splits)
+        nbytes = attn_decode_workspace_bytes(B, Hq, d, smax)
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_decode_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+        None if host_arr is None else ctypes.cast(host_arr, ctypes.c_void_p), page_size,
+        int(num_splits), _ptr(out), _ptr(lse), B, Hq, Hkv, d, block_table.shape[1], num_pages,
+        float(scale), _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
+    _check(st, "attn_decode_paged")
+    return out, lse
+
+
+def attn_merge_states(o_parts, lse_parts, out_dtype=torch.bfloat16, out=None, lse=None,
+                      want_lse=True, stream=None):
+    """LSE merge. o_parts [rows,S,d] fp32, lse_parts [rows,S] fp32 -> (o [rows,d], lse [rows])."""
+    _need(o_parts, "o_parts")
+    _need(lse_parts, "lse_parts")
+    rows, S, d = o_parts.shape
+    if out is None:
+        out = torch.empty(rows, d, dtype=out_dtype, device=o_parts.device)
+    if lse is None and want_lse:
+        lse = torch.empty(rows, dtype=torch.float32, device=o_parts.device)
+    st = lib().attn_merge_states(_ptr(o_parts), _ptr(lse_parts), rows, S, d, _ptr(out), _ptr(lse),
+                                 _dtype_code(out), _stream(stream))
+    _check(st, "attn_merge_states")
+    return out, lse
+
+
+def attn_get_device_status(stream=None):
+    """Reads and clears the device status word; returns the status name."""
+    return STATUS.get(lib().attn_get_device_status(_stream(stream)), "?")

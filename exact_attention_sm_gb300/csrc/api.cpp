@@ -1,0 +1,201 @@
+// C ABI entry points: host-side validation, split planning and launch
+// selection.  Every check happens before anything is enqueued, so an invalid
+// call touches no memory.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+#include "attn.h"
+
+namespace attn_host {
+int* device_status_ptr();
+int num_sms();
+int decode_ctas_per_sm();
+attn_status_t launch_prefill_f32(const float*, const float*, const float*, float*, float*, int, int,
+                                 int, int, int, int, int, float, cudaStream_t);
+attn_status_t launch_prefill_bf16(const void*, const void*, const void*, void*, float*, int, int,
+                                  int, int, int, int, int, float, cudaStream_t);
+attn_status_t launch_decode_bf16(const void*, const void*, const void*, const int32_t*,
+                                 const int32_t*, int, int, int, void*, float*, float*, float*, int,
+                                 int, int, int, int, int, float, cudaStream_t);
+attn_status_t launch_merge(const float*, const float*, int, int, int, void*, float*, attn_dtype_t,
+                           cudaStream_t);
+}  // namespace attn_host
+
+namespace {
+
+constexpr int kMaxPlannedSplits = 64;  // largest segment count the planner tries
+constexpr size_t kAlign = 256;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Split planner ("Lecture 4" sections 4.2 / 5.6 and exercise 6; the reading
+// is spelled out in attn.h): returns the shared chunk length C and the largest
+// per-request segment count.
+void plan(const int32_t* lens, int B, int Hkv, int page, int num_splits, int slots, int32_t* chunk,
+          int32_t* max_splits) {
+  int64_t longest = 1;
+  for (int b = 0; b < B; ++b) longest = std::max<int64_t>(longest, lens[b]);
+  int64_t best_c = std::max<int64_t>(page, cdiv(longest, page) * page);
+  if (num_splits > 0) {
+    best_c = std::max<int64_t>(page, cdiv(cdiv(longest, num_splits), page) * page);
+  } else if ((int64_t)B * Hkv < slots) {
+    int64_t best_cost = -1;
+    for (int s = 1; s <= kMaxPlannedSplits; s *= 2) {
+      const int64_t c = std::max<int64_t>(page, cdiv(cdiv(longest, s), page) * page);
+      int64_t units = 0;
+      for (int b = 0; b < B; ++b) units += std::max<int64_t>(1, cdiv(lens[b], c));
+      units *= Hkv;
+      const int64_t cost = cdiv(units, slots) * c;
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_c = c;
+      }
+    }
+  }
+  int64_t smax = 1;
+  for (int b = 0; b < B; ++b) smax = std::max<int64_t>(smax, cdiv(lens[b], best_c));
+  *chunk = static_cast<int32_t>(best_c);
+  *max_splits = static_cast<int32_t>(smax);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+    case ATTN_ERR_BAD_INDEX: return "ATTN_ERR_BAD_INDEX";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                       attn_dtype_t dtype, attn_stream_t stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (causal && Lq != Lk) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_F32)
+    return attn_host::launch_prefill_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                         static_cast<const float*>(v), static_cast<float*>(o), lse,
+                                         B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0, scale, st);
+  return attn_host::launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0,
+                                        scale, st);
+}
+
+attn_status_t attn_decode_plan(const int32_t* seq_lens_host, int B, int Hkv, int page_size,
+                               int num_splits, int slots, int32_t* chunk_out,
+                               int32_t* max_splits_out) {
+  if (!seq_lens_host || !chunk_out || !max_splits_out) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hkv <= 0 || page_size <= 0 || num_splits < 0) return ATTN_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens_host[b] < 0) return ATTN_ERR_INVALID_ARG;
+  if (slots <= 0) {
+    const int sms = attn_host::num_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    slots = sms * attn_host::decode_ctas_per_sm();
+  }
+  plan(seq_lens_host, B, Hkv, page_size, num_splits, slots, chunk_out, max_splits_out);
+  return ATTN_OK;
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_splits) {
+  if (B <= 0 || Hq <= 0 || d <= 0 || max_splits <= 1) return 0;
+  const size_t states = (size_t)B * Hq * max_splits;
+  return round_up(states * d * sizeof(float), kAlign) + round_up(states * sizeof(float), kAlign);
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                const int32_t* seq_lens_host, int page_size, int num_splits,
+                                void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                int max_pages_per_seq, int num_pages, float scale,
+                                void* workspace, size_t workspace_bytes, attn_dtype_t dtype,
+                                attn_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_pages_per_seq <= 0 || num_pages <= 0 ||
+      num_splits < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128 || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  int32_t chunk = max_pages_per_seq * page_size, smax = 1;
+  if (num_splits != 1) {
+    std::vector<int32_t> host_lens;
+    const int32_t* lens = seq_lens_host;
+    if (lens == nullptr) {
+      host_lens.resize(B);
+      if (cudaMemcpyAsync(host_lens.data(), seq_lens, sizeof(int32_t) * B, cudaMemcpyDeviceToHost,
+                          st) != cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      lens = host_lens.data();
+    }
+    for (int b = 0; b < B; ++b)
+      if (lens[b] < 0 || (int64_t)lens[b] > (int64_t)max_pages_per_seq * page_size)
+        return ATTN_ERR_INVALID_ARG;
+    int slots = 1;
+    if (num_splits == 0) {
+      const int sms = attn_host::num_sms();
+      if (sms <= 0) return ATTN_ERR_CUDA;
+      slots = sms * attn_host::decode_ctas_per_sm();
+    }
+    plan(lens, B, Hkv, page_size, num_splits, slots, &chunk, &smax);
+  }
+  if (smax > 65535) return ATTN_ERR_UNSUPPORTED;
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  if (smax > 1) {
+    const size_t need = attn_decode_workspace_bytes(B, Hq, d, smax);
+    if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return ATTN_ERR_WORKSPACE;
+    part_o = static_cast<float*>(workspace);
+    part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        round_up((size_t)B * Hq * smax * d * sizeof(float), kAlign));
+  }
+  attn_status_t s = attn_host::launch_decode_bf16(q, k_pages, v_pages, block_table, seq_lens,
+                                                  page_size, chunk, smax, o, lse, part_o, part_lse,
+                                                  B, Hq, Hkv, d, max_pages_per_seq, num_pages,
+                                                  scale, st);
+  if (s != ATTN_OK || smax == 1) return s;
+  return attn_host::launch_merge(part_o, part_lse, B * Hq, smax, d, o, lse, dtype, st);
+}
+
+attn_status_t attn_merge_states(const float* o_parts, const float* lse_parts, int rows, int S,
+                                int d, void* o_out, float* lse_out, attn_dtype_t out_dtype,
+                                attn_stream_t stream) {
+  if (!o_parts || !lse_parts || !o_out) return ATTN_ERR_INVALID_ARG;
+  if (rows <= 0 || S <= 0 || d <= 0 || d % 4 != 0) return ATTN_ERR_INVALID_ARG;
+  if (d > 512) return ATTN_ERR_UNSUPPORTED;
+  if (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(o_out)) return ATTN_ERR_INVALID_ARG;
+  if (rows > 65535 * 4) return ATTN_ERR_UNSUPPORTED;
+  return attn_host::launch_merge(o_parts, lse_parts, rows, S, d, o_out, lse_out, out_dtype,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -12,16 +12,21 @@ import torch
 _DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
-def _gen(seed):
-    return torch.Generator().manual_seed(int(seed))
+def _gen(seed, device="cpu"):
+    return torch.Generator(device=device).manual_seed(int(seed))
 
 
-def prefill_inputs(B, Hq, Hkv, Lq, Lk, d, dtype="bf16", seed=0):
-    """q [B,Hq,Lq,d], k and v [B,Hkv,Lk,d], N(0,1), contiguous, on the CPU."""
-    g = _gen(seed)
-    q = torch.randn(B, Hq, Lq, d, generator=g)
-    k = torch.randn(B, Hkv, Lk, d, generator=g)
-    v = torch.randn(B, Hkv, Lk, d, generator=g)
+def prefill_inputs(B, Hq, Hkv, Lq, Lk, d, dtype="bf16", seed=0, device="cpu"):
+    """q [B,Hq,Lq,d], k and v [B,Hkv,Lk,d], N(0,1), contiguous.
+
+    device="cpu" (the default, used for every oracle comparison) draws with the
+    CPU generator; device="cuda" draws with the CUDA generator of the same seed
+    (a different stream of numbers with the same distribution, used where only
+    timing matters)."""
+    g = _gen(seed, device)
+    q = torch.randn(B, Hq, Lq, d, generator=g, device=device)
+    k = torch.randn(B, Hkv, Lk, d, generator=g, device=device)
+    v = torch.randn(B, Hkv, Lk, d, generator=g, device=device)
     dt = _DT[dtype]
     return q.to(dt), k.to(dt), v.to(dt)
 
@@ -50,7 +55,7 @@ def decode_lengths_uniform(B, lo, hi, seed=2):
 
 
 def decode_inputs(seq_lens, Hq, Hkv, d, page_size=16, dtype="bf16", seed=0, perm_seed=1,
-                  extra_table_cols=0):
+                  extra_table_cols=0, device="cpu"):
     """Paged decode inputs with a shuffled block table.
 
     The pool holds exactly sum_b ceil(len_b / page_size) pages.  A random
@@ -58,7 +63,9 @@ def decode_inputs(seq_lens, Hq, Hkv, d, page_size=16, dtype="bf16", seed=0, perm
     is handed out to the requests in order; table entries past a request's
     last page are -1.  Returns q [B,Hq,d], k_pages and v_pages
     [num_pages, page_size, Hkv, d], block_table int32 [B, max_pages],
-    seq_lens int32 [B], all on the CPU.
+    seq_lens int32 [B].  The table is always built on the CPU; device="cuda"
+    draws q/k/v with the CUDA generator (timing only) and returns all five on
+    the GPU.
     """
     B = len(seq_lens)
     pages_per = [-(-int(n) // page_size) for n in seq_lens]
@@ -70,13 +77,13 @@ def decode_inputs(seq_lens, Hq, Hkv, d, page_size=16, dtype="bf16", seed=0, perm
     for b, n in enumerate(pages_per):
         table[b, :n] = perm[off:off + n].to(torch.int32)
         off += n
-    g = _gen(seed)
-    q = torch.randn(B, Hq, d, generator=g)
-    k_pages = torch.randn(num_pages, page_size, Hkv, d, generator=g)
-    v_pages = torch.randn(num_pages, page_size, Hkv, d, generator=g)
+    g = _gen(seed, device)
+    q = torch.randn(B, Hq, d, generator=g, device=device)
+    k_pages = torch.randn(num_pages, page_size, Hkv, d, generator=g, device=device)
+    v_pages = torch.randn(num_pages, page_size, Hkv, d, generator=g, device=device)
     dt = _DT[dtype]
     lens = torch.tensor([int(n) for n in seq_lens], dtype=torch.int32)
-    return q.to(dt), k_pages.to(dt), v_pages.to(dt), table, lens
+    return (q.to(dt), k_pages.to(dt), v_pages.to(dt), table.to(device), lens.to(device))
 
 
 def merge_inputs(rows, S, d, seed=0, empty_frac=0.0):

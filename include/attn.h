@@ -1,0 +1,193 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) exact-attention library (libattn.so).
+ *
+ * Exact scaled-dot-product attention O = softmax(Q K^T * scale) V, computed
+ * as fused kernels that never write the L x L score matrix to device memory,
+ * plus its memory-bound decode form over a paged, grouped-query KV cache and
+ * the LSE merge operator that combines split-KV partial states.
+ *
+ * Pages the operations follow (cited by title below):
+ *   [Lecture 4]   "Lecture 4 - Efficient attention kernels: FlashAttention and
+ *                 FlashInfer" (Stanford CS349D course notes)
+ *   [Tiling blog] "The attention formula did not change, so why is it several
+ *                 times faster? FlashAttention's tiling, online softmax and IO"
+ *   [LLM book]    "10.3 FlashAttention: IO-aware algorithm design"
+ *   [CUDA book]   "FlashAttention and inference operators" (CUDA advanced
+ *                 handbook)
+ *
+ * Conventions shared by every call
+ *   - Every tensor pointer is a DEVICE pointer to a dense, row-major
+ *     (contiguous) array in the layout stated per call; the caller allocates,
+ *     owns and frees all of them, including any workspace.  The library never
+ *     allocates or frees device memory and keeps no per-call state.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on it and returns; results are valid once the
+ *     stream has synchronised.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a status and touches no memory.  A launch failure
+ *     returns ATTN_ERR_CUDA.  Problems found on the device (a block-table
+ *     entry outside [0, num_pages), a bounded wait that ran out) do not fault:
+ *     the kernel skips the access, records the error in a device status word
+ *     and the next attn_get_device_status() call reports it.
+ *   - dtype ATTN_BF16: bf16 inputs and outputs, fp32 accumulation, fp32 LSE.
+ *     dtype ATTN_F32: fp32 everywhere (computed on CUDA cores in fp32).
+ *   - LSE is the natural-log log-sum-exp of the scaled scores of a row,
+ *     LSE = m + ln(l) ([LLM book] 10.3.2 "LSE").  A row that sees no key gets
+ *     O = 0 and LSE = -inf (never NaN).
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* null pointer, size <= 0, Hq % Hkv != 0, ... */
+  ATTN_ERR_UNSUPPORTED = 2,    /* valid but not implemented (d, page size, causal Lq != Lk) */
+  ATTN_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+  ATTN_ERR_CUDA = 4,           /* a CUDA runtime call or a launch failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out (device status) */
+  ATTN_ERR_BAD_INDEX = 6       /* a block-table entry was out of range (device status) */
+} attn_status_t;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/*
+ * attn_fwd - fused prefill attention forward with per-row LSE.
+ *
+ * Computes, for every batch b and query head h (KV head h / (Hq / Hkv),
+ * [CUDA book] GQA exercise):
+ *   S = Q_bh K_b,kvh^T * scale, P = softmax(S), O_bh = P V_b,kvh
+ * ([Tiling blog] section 01), row by row with the online softmax over K/V
+ * tiles ([LLM book] 10.3.2 tiled forward, FlashAttention-2 order).  With
+ * causal != 0 query i sees key j only when j <= i; K/V tiles entirely above
+ * the diagonal are skipped and diagonal tiles are masked element-wise
+ * ([Tiling blog] section 06).
+ *
+ *   q   [B, Hq,  Lq, d]   input, dtype
+ *   k   [B, Hkv, Lk, d]   input, dtype
+ *   v   [B, Hkv, Lk, d]   input, dtype
+ *   o   [B, Hq,  Lq, d]   output, dtype (written in full)
+ *   lse [B, Hq,  Lq]      output, fp32, natural log; may be NULL
+ *   d in {64, 128}; Hq % Hkv == 0; B, Hq, Hkv, Lq, Lk >= 1.
+ *   causal requires Lq == Lk (ATTN_ERR_UNSUPPORTED otherwise).
+ *   scale: usually 1/sqrt(d); must be finite and > 0.
+ *   bf16 pointers must be 16-byte aligned (tensor-memory-access copies).
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                       attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_decode_plan - host-side split-KV planner (no device work).
+ *
+ * Chooses one chunk length C (a multiple of page_size) shared by every
+ * request; request b is cut into max(1, ceil(len_b / C)) segments.
+ * Reading of [Lecture 4] section 4.2, section 5.6 and exercise 6: a work
+ * unit is (request, KV head, segment); units run `slots` at a time; a plan
+ * costs ceil(units / slots) * C.  If B * Hkv >= slots nothing is split.
+ * Otherwise S = 1, 2, 4, ..., 64 segments (of the longest request) are
+ * tried and the cheapest wins, ties going to fewer segments.
+ * num_splits > 0 forces C = ceil(ceil(max_len / num_splits) / page_size) *
+ * page_size instead.  slots <= 0 means "ask the current device": SM count x
+ * resident decode CTAs per SM.
+ *
+ *   seq_lens_host [B]  host array of context lengths (>= 0)
+ *   chunk_out          host scalar: C
+ *   max_splits_out     host scalar: max_b segments (the workspace's S)
+ */
+attn_status_t attn_decode_plan(const int32_t* seq_lens_host, int B, int Hkv, int page_size,
+                               int num_splits, int slots, int32_t* chunk_out,
+                               int32_t* max_splits_out);
+
+/*
+ * attn_decode_workspace_bytes - bytes of workspace attn_decode_paged needs
+ * when the plan has `max_splits` segments per request (0 when max_splits
+ * <= 1: the decode kernel then writes O and LSE directly).  Layout: fp32
+ * partial outputs [B*Hq, max_splits, d] followed by fp32 partial LSE
+ * [B*Hq, max_splits], 256-byte aligned.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_splits);
+
+/*
+ * attn_decode_paged - one query token per request against a paged KV cache.
+ *
+ * For request b and query head h (KV head h / (Hq / Hkv)) the keys are
+ * tokens t < seq_lens[b]; token t lives in page block_table[b][t / page_size],
+ * slot t % page_size ([CUDA book] "PagedAttention"; cache layout of
+ * [LLM book] 10.3.7).  With more than one segment per request (split-KV,
+ * Flash-Decoding: [LLM book] 10.3.7, [CUDA book] "Flash-Decoding and
+ * split-K") each segment's normalised O_s and LSE_s go to the workspace and
+ * are combined by the LSE merge (attn_merge_states) in ascending segment
+ * order, so results are bitwise reproducible.
+ *
+ *   q            [B, Hq, d]                          input, dtype
+ *   k_pages      [num_pages, page_size, Hkv, d]      input, dtype
+ *   v_pages      [num_pages, page_size, Hkv, d]      input, dtype
+ *   block_table  [B, max_pages_per_seq] int32        input; entries at or past
+ *                ceil(seq_lens[b] / page_size) are never read (may be -1)
+ *   seq_lens     [B] int32 (device)                  input, 0 <= len <=
+ *                max_pages_per_seq * page_size
+ *   seq_lens_host [B] int32 (host) or NULL           lengths for the planner;
+ *                when NULL and num_splits != 1 the library copies seq_lens
+ *                to the host and synchronises `stream` first.
+ *   page_size    16 (ATTN_ERR_UNSUPPORTED otherwise)
+ *   num_splits   0 = planner's choice, >= 1 forces at most that many segments
+ *   o            [B, Hq, d] output, dtype;  lse [B, Hq] fp32 output or NULL
+ *   workspace    device buffer of >= attn_decode_workspace_bytes(B, Hq, d, S)
+ *                bytes for the plan's S (may be NULL when S == 1)
+ *   d == 128 for bf16; d in {64, 128} for fp32 is not offered (bf16 only).
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                const int32_t* seq_lens_host, int page_size, int num_splits,
+                                void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                int max_pages_per_seq, int num_pages, float scale,
+                                void* workspace, size_t workspace_bytes, attn_dtype_t dtype,
+                                attn_stream_t stream);
+
+/*
+ * attn_merge_states - the LSE merge operator over S partial states per row.
+ *
+ * For each row r: M = max_s LSE[r,s] over non-empty states, w_s =
+ * exp(LSE[r,s] - M), O[r] = sum_s w_s O_parts[r,s] / sum_s w_s,
+ * LSE[r] = M + ln(sum_s w_s) ([LLM book] 10.3.2 "LSE"; [CUDA book]
+ * "Flash-Decoding and split-K" and its merge exercise).  States with
+ * LSE = -inf are skipped (their O is not read); a row whose states are all
+ * empty gets O = 0, LSE = -inf.  Summation runs in ascending s with no
+ * atomics ([Lecture 4] 4.3 and 5.6 on determinism).
+ *
+ *   o_parts   [rows, S, d] fp32 input     lse_parts [rows, S] fp32 input
+ *   o_out     [rows, d] output in out_dtype   lse_out [rows] fp32 or NULL
+ *   d % 4 == 0, 1 <= d <= 512, S >= 1.
+ */
+attn_status_t attn_merge_states(const float* o_parts, const float* lse_parts, int rows, int S,
+                                int d, void* o_out, float* lse_out, attn_dtype_t out_dtype,
+                                attn_stream_t stream);
+
+/*
+ * attn_get_device_status - waits for `stream`, then reads and clears the
+ * device status word shared by all kernels of this library on the current
+ * device.  Returns ATTN_OK, ATTN_ERR_BAD_INDEX or ATTN_ERR_DEVICE_TIMEOUT
+ * (the first recorded), or ATTN_ERR_CUDA if the stream itself failed.
+ */
+attn_status_t attn_get_device_status(attn_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* attn_status_string(attn_status_t status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

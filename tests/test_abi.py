@@ -1,0 +1,120 @@
+"""CPU-only checks of the C ABI: the library loads, exports every declared
+symbol, rejects invalid arguments on the host before launching anything, and
+its split planner agrees bit-exactly with the oracle's reading."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import exact_attention_sm_gb300 as ea
+from oracle import attention as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ea.lib()
+    names = declared_symbols()
+    assert set(names) == set(ea.SIGNATURES), names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.attn_version() >= 100
+
+
+def test_status_strings():
+    for code, name in ea.STATUS.items():
+        assert ea.lib().attn_status_string(code).decode() == name
+
+
+def fwd(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=4, Hkv=2, Lq=8, Lk=8, d=64,
+                causal=0, scale=0.125, dtype=ea.ATTN_BF16)
+    args.update(kw)
+    return ea.lib().attn_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                             args["Hq"], args["Hkv"], args["Lq"], args["Lk"], args["d"],
+                             args["causal"], args["scale"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(B=0), 1), (dict(Lk=0), 1), (dict(Hkv=3), 1),
+    (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(dtype=7), 1),
+    (dict(d=96), 2), (dict(causal=1, Lq=4), 2), (dict(q=MISALIGNED), 1),
+])
+def test_attn_fwd_rejects_on_host(kw, status):
+    assert fwd(**kw) == status
+
+
+def dec(**kw):
+    lens = (ctypes.c_int32 * 2)(100, 40)
+    args = dict(q=FAKE, k=FAKE, v=FAKE, table=FAKE, lens=FAKE, lens_host=ctypes.cast(lens, ctypes.c_void_p),
+                page=16, splits=4, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, d=128, max_pages=7,
+                num_pages=14, scale=0.1, ws=None, ws_bytes=0, dtype=ea.ATTN_BF16)
+    args.update(kw)
+    a = args
+    return ea.lib().attn_decode_paged(a["q"], a["k"], a["v"], a["table"], a["lens"], a["lens_host"],
+                                      a["page"], a["splits"], a["o"], a["lse"], a["B"], a["Hq"],
+                                      a["Hkv"], a["d"], a["max_pages"], a["num_pages"], a["scale"],
+                                      a["ws"], a["ws_bytes"], a["dtype"], None)
+
+
+def test_decode_rejects_on_host():
+    assert dec(q=None) == 1
+    assert dec(table=None) == 1
+    assert dec(Hkv=3) == 1
+    assert dec(splits=-1) == 1
+    assert dec(page=32) == 2
+    assert dec(d=64) == 2
+    assert dec(dtype=ea.ATTN_F32) == 2
+    assert dec(max_pages=2) == 1          # a length exceeds max_pages * page_size
+    assert dec() == 3                     # 4 forced segments need a workspace
+    need = ea.attn_decode_workspace_bytes(2, 8, 128, 4)
+    assert need >= 2 * 8 * 4 * 129 * 4
+    assert dec(ws=ctypes.c_void_p(0x20000), ws_bytes=need - 1) == 3
+    assert dec(ws=ctypes.c_void_p(0x20010), ws_bytes=need) == 3  # not 256-byte aligned
+    assert ea.attn_decode_workspace_bytes(2, 8, 128, 1) == 0
+
+
+def test_merge_rejects_on_host():
+    m = ea.lib().attn_merge_states
+    assert m(None, FAKE, 4, 2, 128, FAKE, None, ea.ATTN_BF16, None) == 1
+    assert m(FAKE, FAKE, 4, 2, 6, FAKE, None, ea.ATTN_BF16, None) == 1
+    assert m(FAKE, FAKE, 0, 2, 128, FAKE, None, ea.ATTN_BF16, None) == 1
+    assert m(FAKE, FAKE, 4, 2, 1024, FAKE, None, ea.ATTN_BF16, None) == 2
+    assert m(MISALIGNED, FAKE, 4, 2, 128, FAKE, None, ea.ATTN_BF16, None) == 1
+
+
+def test_planner_matches_oracle_bit_exact():
+    rng = np.random.default_rng(7)
+    cases = [([16384, 16384], 8, 132), ([32768], 8, 132), ([1024] * 256, 8, 456),
+             ([0], 8, 456), ([5, 0, 17], 1, 10)]
+    for _ in range(300):
+        b = int(rng.integers(1, 9))
+        hi = int(rng.choice([50, 5000, 140000]))
+        cases.append((rng.integers(0, hi, size=b).tolist(), int(rng.choice([1, 2, 4, 8])),
+                      int(rng.choice([132, 152, 304, 456, 608]))))
+    for lens, hkv, slots in cases:
+        for forced in (0, 1, 2, 5, 64):
+            chunk, smax = ea.attn_decode_plan(lens, hkv, 16, forced, slots)
+            o_chunk, o_splits = orc.plan_splits(lens, hkv, slots, 16, forced)
+            assert chunk == o_chunk[0], (lens, hkv, slots, forced)
+            assert smax == max(o_splits), (lens, hkv, slots, forced)
+
+
+def test_planner_config5_lengths_fill_the_gpu():
+    from exact_attention_sm_gb300 import inputs
+    lens = inputs.decode_lengths_uniform(4, 4096, 131072, seed=2)
+    chunk, smax = ea.attn_decode_plan(lens, 8, 16, 0, 152 * 3)
+    units = 8 * sum(max(1, -(-n // chunk)) for n in lens)
+    assert units >= 152 and chunk % 16 == 0
