@@ -1,0 +1,84 @@
+"""bf16 prefill (TMA + tcgen05 + TMEM kernel) against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_sm_gb300 as ea
+from exact_attention_sm_gb300 import inputs
+from oracle import attention as orc
+from tests.gpu_util import check_lse, check_o, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def full_case(B, Hq, Hkv, Lq, Lk, d, causal, seed=0):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Lq, Lk, d, "bf16", seed)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = ea.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ea.attn_get_device_status() == "ATTN_OK"
+    o_ref, lse_ref = orc.prefill(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, causal)
+    check_o(to_np(o), o_ref, "bf16")
+    check_lse(to_np(lse), lse_ref, "bf16")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [1, 17, 128, 129, 300, 640])
+def test_small_shapes(d, causal, L):
+    full_case(2, 4, 2, L, L, d, causal, seed=L + d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_rectangular_non_causal(d):
+    full_case(1, 4, 1, 200, 777, d, False, seed=1)
+    full_case(1, 2, 2, 513, 64, d, False, seed=2)
+
+
+def sampled_case(B, Hq, Hkv, L, d, causal):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, L, L, d, "bf16", seed=0)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = ea.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ea.attn_get_device_status() == "ATTN_OK"
+    rows = inputs.sample_rows(B, Hq, L)
+    o_ref, lse_ref = orc.prefill_rows(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                                      scale, causal, rows)
+    idx = torch.tensor(rows)
+    got_o = o[idx[:, 0], idx[:, 1], idx[:, 2]]
+    got_l = lse[idx[:, 0], idx[:, 1], idx[:, 2]]
+    check_o(to_np(got_o), o_ref, "bf16")
+    check_lse(to_np(got_l), lse_ref, "bf16")
+    # properties that hold for every row
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    return o, lse
+
+
+def test_gpt2_medium_shape_B64_H16_L1024_d64_causal():
+    sampled_case(64, 16, 16, 1024, 64, True)
+
+
+def test_llama3_8b_shape_L8192_gqa_causal():
+    sampled_case(1, 32, 8, 8192, 128, True)
+
+
+def test_llama3_8b_shape_L32768_gqa_causal():
+    sampled_case(1, 32, 8, 32768, 128, True)
+
+
+def test_prefill_is_deterministic():
+    q, k, v = (t.cuda() for t in inputs.prefill_inputs(2, 8, 2, 1000, 1000, 128, "bf16", seed=4))
+    outs = [ea.attn_fwd(q, k, v, causal=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_lse_optional():
+    q, k, v = (t.cuda() for t in inputs.prefill_inputs(1, 2, 2, 256, 256, 64, "bf16", seed=5))
+    o1, _ = ea.attn_fwd(q, k, v, causal=True, want_lse=False)
+    o2, _ = ea.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
