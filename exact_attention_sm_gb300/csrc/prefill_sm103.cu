@@ -36,7 +36,8 @@
 //
 // Every wait is bounded: after ~2 s the waiting role records
 // ATTN_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag, drains its own
-// in-flight copies / MMAs and the CTA frees its TMEM and exits.
+// in-flight copies / MMAs and the CTA frees its TMEM and exits.  CTAs that
+// start while the device status word holds a timeout return at once.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -124,9 +125,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    // After a timeout anywhere on the device the remaining CTAs do no work
+    // until the host has read (and cleared) the status word.
+    *abort_flag = (status != nullptr &&
+                   *reinterpret_cast<volatile int*>(status) == ATTN_ERR_DEVICE_TIMEOUT) ? 2 : 0;
     fence_mbar_init();
   }
+  __syncthreads();
+  if (*abort_flag == 2) return;
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
