@@ -30,6 +30,8 @@ SIGNATURES = {
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                _P, _SZ, _I, _P]),
+    "attn_decode_paged_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I,
+                                       _I, _F, _I, _P]),
     "attn_merge_states": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P]),
     "attn_get_device_status": (_I, [_P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),

@@ -154,6 +154,49 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
                                 attn_stream_t stream);
 
 /*
+ * attn_decode_paged_noalloc - attn_decode_paged for callers that cannot
+ * allocate device memory.  No counterpart in the source pages: this is a
+ * convenience of this library.
+ *
+ * Who needs it: code that is handed only its inputs and outputs and is not
+ * allowed to call cudaMalloc or any other allocator - for example a plugin
+ * inside a host framework that owns all device memory through its own pool,
+ * or a latency-critical path where an allocation (and the device-wide
+ * synchronisation cudaMalloc can imply) is not acceptable.  Such a caller
+ * cannot provide the split-KV workspace that attn_decode_paged wants.
+ *
+ * Instead of a caller-provided workspace this call uses one fixed scratch
+ * array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES bytes that lives inside the
+ * library as a static device variable: every GPU that loads libattn.so holds
+ * it until the process exits.  The call itself allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ *   Arguments are those of attn_decode_paged minus the workspace, with one
+ *   difference: seq_lens_host must not be NULL unless num_splits == 1 (the
+ *   split planner runs on the host and this call will not allocate a host
+ *   copy either).
+ *   Returns ATTN_ERR_WORKSPACE, touching no memory, when the plan needs more
+ *   than ATTN_DECODE_NOALLOC_SCRATCH_BYTES (attn_decode_workspace_bytes(B,
+ *   Hq, d, S) for the plan's S); use attn_decode_paged with your own
+ *   workspace for such sizes.
+ *   The first call on a device looks up the scratch array's device address
+ *   (one cudaGetSymbolAddress per device, with that device current); make
+ *   that first call before any stream capture.
+ *   All calls on a device share the one scratch array, and it keeps whatever
+ *   the last call wrote (every used entry is overwritten before it is read,
+ *   so nothing needs clearing).  Calls whose kernels overlap on the GPU (on
+ *   different streams, or from different host threads) race on that array:
+ *   serialise them.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        const int32_t* seq_lens_host, int page_size,
+                                        int num_splits, void* o, float* lse, int B, int Hq,
+                                        int Hkv, int d, int max_pages_per_seq, int num_pages,
+                                        float scale, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
  * attn_merge_states - the LSE merge operator over S partial states per row.
  *
  * For each row r: M = max_s LSE[r,s] over non-empty states, w_s =
