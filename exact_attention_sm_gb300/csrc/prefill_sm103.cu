@@ -90,15 +90,72 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Packed two-lane fp32 FMA / add (one instruction for two lanes of work).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 struct Item {
   int bh, qt[2], n[2];  // n[1] == 0: tile B is absent
 };
 
-__device__ __forceinline__ Item decode_item(int it, int BH, int num_pairs, int num_qt, int n_kv,
-                                            int causal) {
+// Work-item order and assignment.
+//  * Long causal rows (more than kGroupedMaxPairs pairs per head): items are
+//    listed heaviest pair first across all heads and dealt round-robin to the
+//    persistent CTAs, which keeps them balanced.
+//  * Short rows or non-causal: items are listed head by head and every CTA
+//    takes one contiguous run of them, so the pairs of a head run back to back
+//    on the same SM and re-read that head's K/V from L2; each run spans whole
+//    heads (up to its ends), so every CTA gets a similar mix of pair weights.
+constexpr int kGroupedMaxPairs = 16;
+
+struct Schedule {
+  bool grouped;
+  int first, last, step;  // items first, first+step, ... < last
+};
+
+__device__ __forceinline__ Schedule make_schedule(int num_items, int num_pairs, int causal) {
+  Schedule sc;
+  sc.grouped = !causal || num_pairs <= kGroupedMaxPairs;
+  if (sc.grouped) {
+    sc.first = static_cast<int>(static_cast<long long>(num_items) * blockIdx.x / gridDim.x);
+    sc.last = static_cast<int>(static_cast<long long>(num_items) * (blockIdx.x + 1) / gridDim.x);
+    sc.step = 1;
+  } else {
+    sc.first = blockIdx.x;
+    sc.last = num_items;
+    sc.step = gridDim.x;
+  }
+  return sc;
+}
+
+__device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int num_pairs, int num_qt,
+                                            int n_kv, int causal) {
   Item w;
-  const int pair = num_pairs - 1 - it / BH;  // heaviest pairs first
-  w.bh = it % BH;
+  int pair;
+  if (grouped) {
+    w.bh = it / num_pairs;
+    pair = num_pairs - 1 - it % num_pairs;
+  } else {
+    pair = num_pairs - 1 - it / BH;
+    w.bh = it % BH;
+  }
   w.qt[0] = 2 * pair;
   w.qt[1] = 2 * pair + 1;
   w.n[0] = causal ? min(n_kv, w.qt[0] + 1) : n_kv;
@@ -140,6 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_items = BH * num_pairs;
   const int n_kv = (Lk + BN - 1) / BN;
   const int group = Hq / Hkv;
+  const Schedule sched = make_schedule(num_items, num_pairs, causal);
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -172,7 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -182,8 +240,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int g = 0;                // K/V tiles issued (ring position)
       int nq[2] = {0, 0};       // Q tiles issued per slot
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < num_items; it += gridDim.x) {
-        const Item w = decode_item(it, BH, num_pairs, num_qt, n_kv, causal);
+      for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+        const Item w = decode_item(it, sched.grouped, BH, num_pairs, num_qt, n_kv, causal);
         const int bh_kv = (w.bh / Hq) * Hkv + (w.bh % Hq) / group;
         const int nmax = max(w.n[0], w.n[1]);
         // K/V tile j of this item into the next ring slot.
@@ -270,8 +328,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       };
 
-      for (int it = blockIdx.x; ok && it < num_items; it += gridDim.x) {
-        const Item w = decode_item(it, BH, num_pairs, num_qt, n_kv, causal);
+      for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+        const Item w = decode_item(it, sched.grouped, BH, num_pairs, num_qt, n_kv, causal);
         const int nmax = max(w.n[0], w.n[1]);
         // First QK^T of each present tile.
         if (!mbar_wait(&k_full[g % NS], (g / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
@@ -321,7 +379,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     // ------------------------------------------------------------ softmax warps
     const int x = (warp - 4) >> 2;     // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
@@ -331,8 +389,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t o_addr = tmem + lane_off + C::O_COL + x * D;
     int ns = 0, nitem = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < num_items; it += gridDim.x) {
-      const Item w = decode_item(it, BH, num_pairs, num_qt, n_kv, causal);
+    for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+      const Item w = decode_item(it, sched.grouped, BH, num_pairs, num_qt, n_kv, causal);
       const int n = w.n[x];
       if (n == 0) continue;
       const int grow = w.qt[x] * BM + row;
@@ -355,43 +413,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < BN; ++c)
             if (j * BN + c > kmax) s[c] = -INFINITY;
         }
-        float mt = fmaxf(s[0], s[1]);
+        // Row max as 8 independent chains (short dependency depth).
+        float mx[8];
 #pragma unroll
-        for (int c = 2; c < BN; c += 2) mt = fmax3(mt, s[c], s[c + 1]);
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+        for (int c = 16; c < BN; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7]));
         const float mt_s = mt * scale_log2;
         float alpha = 1.f;
         if (mt_s > m_s + kRescaleThreshold) {
           alpha = ex2(m_s - mt_s);  // 0 on the first tile (m_s = -inf)
           m_s = mt_s;
         }
+        // p = 2^(s * scale * log2e - m): paired FMAs, MUFU ex2, paired adds
+        // into 4 independent row-sum chains; P goes to TMEM in 16-column
+        // chunks (8 bf16x2 words) over S's own columns as soon as a chunk is
+        // packed, which keeps few registers live next to S.
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_s, -m_s);
+        float2 rs[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int ch = 0; ch < BN / 16; ++ch) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int c = 0; c < 16; c += 2) {
+            float2 t = ffma2(make_float2(s[ch * 16 + c], s[ch * 16 + c + 1]), sc2, nm2);
+            t.x = ex2(t.x);
+            t.y = ex2(t.y);
+            rs[(c >> 1) & 3] = fadd2(rs[(c >> 1) & 3], t);
+            pk[c >> 1] = attn::pack_bf16x2(t.x, t.y);
+          }
+          tmem_st8(s_addr + ch * 8, pk);
+        }
+        const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+        const float2 r = fadd2(r01, r23);
+        l = l * alpha + (r.x + r.y);
         if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
-          // PV of the previous tile completed before S of this one (issue order).
+          // O <- alpha O before PV of this tile is issued; PV of the previous
+          // tile completed before S of this one (issue order).
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(o_addr + c * 32, r);
+            uint32_t o32[32];
+            tmem_ld32(o_addr + c * 32, o32);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(o_addr + c * 32, r);
+            for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+            tmem_st32(o_addr + c * 32, o32);
           }
         }
-        const float neg_m = -m_s;
-        float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = ex2(fmaf(s[half * 64 + c], scale_log2, neg_m));
-            const float p1 = ex2(fmaf(s[half * 64 + c + 1], scale_log2, neg_m));
-            rs0 += p0;
-            rs1 += p1;
-            pk[c >> 1] = attn::pack_bf16x2(p0, p1);
-          }
-          tmem_st32(s_addr + half * 32, pk);  // P columns 0..63 alias S
-        }
-        l = l * alpha + (rs0 + rs1);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[x]);
