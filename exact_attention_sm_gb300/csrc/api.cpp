@@ -6,6 +6,8 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <functional>
+#include <queue>
 #include <vector>
 
 #include "attn.h"
@@ -27,12 +29,40 @@ attn_status_t launch_merge(const float*, const float*, int, int, int, void*, flo
 
 namespace {
 
-constexpr int kMaxPlannedSplits = 64;  // largest segment count the planner tries
 constexpr size_t kAlign = 256;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Time of a split plan in the lecture's simple model ("Lecture 4", sections
+// 0.5 and 4.2): a non-empty unit (request, KV head, segment) costs its token
+// count plus kUnitOverheadTokens (launching it and merging its partial
+// state) and `slots` workers take the units in launch order (segment
+// fastest, then KV head, then request), each as soon as it is free.  Returns
+// when the last worker finishes.
+constexpr int64_t kUnitOverheadTokens = 64;
+
+int64_t plan_makespan(const int32_t* lens, int B, int Hkv, int slots, int64_t chunk) {
+  int64_t smax = 1;
+  for (int b = 0; b < B; ++b) smax = std::max<int64_t>(smax, cdiv(lens[b], chunk));
+  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> free_at;
+  for (int i = 0; i < slots; ++i) free_at.push(0);
+  for (int b = 0; b < B; ++b)
+    for (int k = 0; k < Hkv; ++k)
+      for (int64_t s = 0; s < smax; ++s) {
+        const int64_t tokens = std::max<int64_t>(0, std::min<int64_t>(lens[b], (s + 1) * chunk) - s * chunk);
+        const int64_t t = free_at.top();
+        free_at.pop();
+        free_at.push(t + (tokens > 0 ? tokens + kUnitOverheadTokens : 0));
+      }
+  int64_t last = 0;
+  while (!free_at.empty()) {
+    last = std::max(last, free_at.top());
+    free_at.pop();
+  }
+  return last;
+}
 
 // Split planner ("Lecture 4" sections 4.2 / 5.6 and exercise 6; the reading
 // is spelled out in attn.h): returns the shared chunk length C and the largest
@@ -45,15 +75,12 @@ void plan(const int32_t* lens, int B, int Hkv, int page, int num_splits, int slo
   if (num_splits > 0) {
     best_c = std::max<int64_t>(page, cdiv(cdiv(longest, num_splits), page) * page);
   } else if ((int64_t)B * Hkv < slots) {
-    int64_t best_cost = -1;
-    for (int s = 1; s <= kMaxPlannedSplits; s *= 2) {
+    int64_t best_t = -1;
+    for (int64_t s = 1; (int64_t)B * Hkv * s <= 16LL * slots; s *= 2) {
       const int64_t c = std::max<int64_t>(page, cdiv(cdiv(longest, s), page) * page);
-      int64_t units = 0;
-      for (int b = 0; b < B; ++b) units += std::max<int64_t>(1, cdiv(lens[b], c));
-      units *= Hkv;
-      const int64_t cost = cdiv(units, slots) * c;
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
+      const int64_t t = plan_makespan(lens, B, Hkv, slots, c);
+      if (best_t < 0 || t < best_t) {
+        best_t = t;
         best_c = c;
       }
     }
@@ -193,7 +220,7 @@ attn_status_t attn_merge_states(const float* o_parts, const float* lse_parts, in
   if (d > 512) return ATTN_ERR_UNSUPPORTED;
   if (out_dtype != ATTN_F32 && out_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(o_parts) || !aligned16(o_out)) return ATTN_ERR_INVALID_ARG;
-  if (rows > 65535 * 4) return ATTN_ERR_UNSUPPORTED;
+  if (rows > 0x7fffffff / 2) return ATTN_ERR_UNSUPPORTED;
   return attn_host::launch_merge(o_parts, lse_parts, rows, S, d, o_out, lse_out, out_dtype,
                                  reinterpret_cast<cudaStream_t>(stream));
 }

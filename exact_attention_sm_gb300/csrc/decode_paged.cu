@@ -1,4 +1,4 @@
-// Paged grouped-query decode attention, bf16, head dim 128, on CUDA cores.
+// Paged grouped-query decode attention, bf16, head dim 128.
 //
 // Follows "FlashAttention and inference operators" (CUDA advanced handbook):
 // "PagedAttention" (token t lives in page block_table[t / 16], slot t % 16),
@@ -6,285 +6,407 @@
 // emits a normalised partial output plus its LSE), and the improvements that
 // chapter lists for its teaching kernel: one CTA serves every query head that
 // shares a KV head so each K/V byte is read once (the GQA exercise), 128-bit
-// loads converted to fp32 in registers, and online softmax while scanning with
-// no score buffer in shared memory.
+// bf16 reads with fp32 arithmetic, and online softmax while scanning with no
+// score buffer.
 //
-// Work decomposition.  CTA = (segment s, KV head, request b), 4 warps.  The
-// segment's pages are dealt round-robin to the warps; each warp keeps its own
-// online-softmax state and the 4 states are merged at the end.  Inside a warp
-// the two half-warps take the even / odd slots of a page and lane l (of 16)
-// owns dims [8l, 8l+8): one 16-byte load per lane and token, a 256-byte
-// contiguous row per half-warp.  The partial dot products of the 8 tokens x HG
-// heads of a half-warp are reduced across its 16 lanes with a transposed
-// butterfly (each step halves the values a lane carries), which needs far
-// fewer shuffles than reducing each value separately; the probabilities are
-// then gathered back to every lane for the P.V update.
+// GB300 layout.  CTA = (segment, KV head [x head group], request) with one
+// producer warp and 4 consumer warps:
+//   * producer: walks the segment's block-table entries (read 32 at a time by
+//     the warp) and, per page, issues two 4-D TMA copies (the page's 16 K rows
+//     and 16 V rows of this KV head, 4 KB each) into an 8-stage shared-memory
+//     ring guarded by mbarriers.  Up to 64 KB per CTA are in flight, which is
+//     what keeps HBM busy; an out-of-range table entry is reported in the
+//     device status word and its page is treated as empty (never read).
+//   * consumers: page i of the segment goes to consumer warp i % 4.  Inside a
+//     warp, 4 groups of 8 lanes each take one token at a time and lane l (of
+//     8) owns dims [16l, 16l+16): two 16-byte shared loads per row.  Scores
+//     use the mixed-precision FMA (bf16 x bf16 + fp32), so neither q nor K is
+//     converted; the 4 tokens x HG heads partial dot products of a group are
+//     reduced over its 8 lanes with a transposed butterfly (each step halves
+//     the values a lane carries), and the probabilities, rounded to bf16 like
+//     the tensor-core path's P, come back with one shuffle per pair of tokens.
+//   * online softmax in the base-2 domain with a conditional rescale: the
+//     running max only moves when a page's max exceeds it by more than 8, so
+//     the accumulators are rarely rescaled (the result is unchanged because
+//     l and O share the same stale max).
+//   * at the end the 4 consumer warps' states are merged in shared memory
+//     (the LSE merge within the CTA) and the CTA writes the final O and LSE
+//     (one segment) or its normalised partial state for the merge kernel.
+#include <cuda.h>
+
 #include "common.cuh"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
 
 namespace {
 
+using namespace sm103;
+
 constexpr int D = 128;
 constexpr int PAGE = 16;
-constexpr int NW = 4;  // warps per CTA
+constexpr int NCW = 4;                      // consumer warps
+constexpr int HG = 4;                       // query heads per CTA (padded when the group is smaller)
+constexpr int NUM_THREADS = 32 * (NCW + 1);
+constexpr int NST = 8;                      // ring stages (one page of K and V each)
+constexpr int PAGE_BYTES = PAGE * D * 2;    // 4 KB: 16 rows of one KV head
+constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
+constexpr int SMEM_BYTES = NST * STAGE_BYTES + 1024;
 constexpr unsigned FULL = 0xffffffffu;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kRescaleThreshold = 8.0f;
 
-template <int HG>
-struct Lanes {
-  static constexpr int NV = 8 * HG;                  // (token, head) values per half-warp per page
-  static constexpr int NF = NV >= 16 ? NV / 16 : 1;  // values a lane holds after the reduction
-};
-
-// Transposed butterfly over the 16 lanes of a half-warp.  On return lane l16
-// holds the full sums of value indices idx(l16, e), e < NF:
-//   HG=4: idx = 2*l16 + e;  HG=2: idx = l16;  HG=1: idx = l16 >> 1.
-template <int NV>
-__device__ __forceinline__ void transposed_reduce(float (&v)[NV], int l16) {
-  int n = NV;
-#pragma unroll
-  for (int bit = 3; bit >= 0; --bit) {
-    const int off = 1 << bit;
-    if (n >= 2) {
-      const bool upper = (l16 >> bit) & 1;
-#pragma unroll
-      for (int i = 0; i < NV / 2; ++i) {
-        if (i < n / 2) {
-          const float send = upper ? v[i] : v[i + n / 2];
-          const float keep = upper ? v[i + n / 2] : v[i];
-          v[i] = keep + __shfl_xor_sync(FULL, send, off);
-        }
-      }
-      n /= 2;
-    } else {
-      v[0] += __shfl_xor_sync(FULL, v[0], off);
-    }
-  }
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-template <int HG>
-__device__ __forceinline__ int value_index(int l16, int e) {
-  if (HG == 4) return 2 * l16 + e;
-  if (HG == 2) return l16;
-  return l16 >> 1;
+// acc + lo/hi bf16 halves of a * lo/hi bf16 halves of b, fp32 accumulate.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+// p (the low / high bf16 half of pw) times both bf16 halves of v, fp32 accumulate.
+__device__ __forceinline__ void fma_plo_v(uint32_t pw, uint32_t v, float& c0, float& c1) {
+  asm("{\n\t.reg .b16 pl, ph, vl, vh;\n\tmov.b32 {pl, ph}, %2;\n\tmov.b32 {vl, vh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, pl, vl, %0;\n\tfma.rn.f32.bf16 %1, pl, vh, %1;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(pw), "r"(v));
+}
+__device__ __forceinline__ void fma_phi_v(uint32_t pw, uint32_t v, float& c0, float& c1) {
+  asm("{\n\t.reg .b16 pl, ph, vl, vh;\n\tmov.b32 {pl, ph}, %2;\n\tmov.b32 {vl, vh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, ph, vl, %0;\n\tfma.rn.f32.bf16 %1, ph, vh, %1;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(pw), "r"(v));
 }
 
-// Lane (within the half-warp) that holds value x after transposed_reduce, and
-// which of its NF registers.
-template <int HG>
-__device__ __forceinline__ int owner_lane(int x) {
-  if (HG == 4) return x >> 1;
-  if (HG == 2) return x;
-  return x << 1;
-}
-
-// Reduce over the lanes that hold the same head (and across both halves).
-template <int HG, bool IS_MAX>
-__device__ __forceinline__ float head_allreduce(float x) {
-  constexpr int kBits = HG == 4 ? 2 : (HG == 2 ? 3 : 4);  // low lane bits that do not select the head
-#pragma unroll
-  for (int bit = 0; bit < kBits; ++bit) {
-    const float y = __shfl_xor_sync(FULL, x, 1 << bit);
-    x = IS_MAX ? fmaxf(x, y) : x + y;
-  }
-  const float y = __shfl_xor_sync(FULL, x, 16);
-  return IS_MAX ? fmaxf(x, y) : x + y;
-}
-
-template <int HG>
-__device__ __forceinline__ int lane_of_head(int h) {
-  return HG == 4 ? 4 * h : (HG == 2 ? 8 * h : 0);
-}
-
-template <int HG>
-__global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_pages,
-    const __nv_bfloat16* __restrict__ v_pages, const int32_t* __restrict__ block_table,
-    const int32_t* __restrict__ seq_lens, int chunk, int max_splits,
-    __nv_bfloat16* __restrict__ o, float* __restrict__ lse, float* __restrict__ part_o,
-    float* __restrict__ part_lse, int Hq, int Hkv, int max_pages, int num_pages,
-    float scale_log2, int* status) {
-  using L = Lanes<HG>;
-  constexpr int NV = L::NV, NF = L::NF;
-  __shared__ float sm_m[NW][HG];
-  __shared__ float sm_l[NW][HG];
-  __shared__ __align__(16) float sm_acc[NW][HG][D];
+__global__ void __launch_bounds__(NUM_THREADS, 3)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
+                       const int32_t* __restrict__ seq_lens, int chunk, int max_splits,
+                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                       float* __restrict__ part_o, float* __restrict__ part_lse, int Hq, int Hkv,
+                       int max_pages, int num_pages, float scale_log2, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* ring = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  __shared__ uint64_t full[NST], empty[NST];
+  __shared__ int skip[NST];
+  __shared__ float sm_m[NCW][HG];
+  __shared__ float sm_l[NCW][HG];
+  __shared__ __align__(16) float sm_acc[NCW][HG][D];
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
 
   const int s = blockIdx.x;
   const int group = Hq / Hkv;
-  const int groups_per_kvh = group / HG;
+  const int groups_per_kvh = (group + HG - 1) / HG;
   const int kvh = blockIdx.y / groups_per_kvh;
-  const int h0 = kvh * group + (blockIdx.y % groups_per_kvh) * HG;
+  const int gi = blockIdx.y % groups_per_kvh;
+  const int h0 = kvh * group + gi * HG;
+  const int nh = min(HG, group - gi * HG);  // real heads in this CTA (the rest is padding)
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, l16 = lane & 15;
 
-  const int len = seq_lens[b];
+  // A length past the table's capacity is reported and clamped, so the
+  // block-table row is never read out of bounds.
+  int len = seq_lens[b];
+  if (len < 0 || len > max_pages * PAGE) {
+    if (threadIdx.x == 0) attn::record_status(status, ATTN_ERR_BAD_INDEX);
+    len = len < 0 ? 0 : max_pages * PAGE;
+  }
   const int t_begin = s * chunk;
   const int t_end = min(len, t_begin + chunk);
-
-  float qf[HG][8];
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    const uint4 w = *reinterpret_cast<const uint4*>(q + ((size_t)b * Hq + h0 + h) * D + 8 * l16);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      qf[h][2 * j] = attn::bf16_lo(ws[j]) * scale_log2;
-      qf[h][2 * j + 1] = attn::bf16_hi(ws[j]) * scale_log2;
-    }
-  }
-
-  float acc[HG][8];
-  float m_run[HG];
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    m_run[h] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[h][j] = 0.f;
-  }
-  float l_own = 0.f;
-  const int own_h = value_index<HG>(l16, 0) / 8;
-
-  const size_t slot_stride = (size_t)Hkv * D;
   const int p_begin = t_begin / PAGE;
-  const int p_end = t_end > t_begin ? (t_end + PAGE - 1) / PAGE : p_begin;
+  const int n_pages = t_end > t_begin ? (t_end + PAGE - 1) / PAGE - p_begin : 0;
 
-  for (int p = p_begin + warp; p < p_end; p += NW) {
-    const int page = block_table[(size_t)b * max_pages + p];
-    if (page < 0 || page >= num_pages) {
-      if (lane == 0) attn::record_status(status, ATTN_ERR_BAD_INDEX);
-      continue;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
-    const size_t base = ((size_t)page * PAGE * Hkv + kvh) * D + 8 * l16;
-    uint4 kr[8], vr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) kr[i] = attn::ld_stream_v4(k_pages + base + (2 * i + half) * slot_stride);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) vr[i] = attn::ld_stream_v4(v_pages + base + (2 * i + half) * slot_stride);
-
-    float part[NV];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t ks[4] = {kr[i].x, kr[i].y, kr[i].z, kr[i].w};
-      float kf[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        kf[2 * j] = attn::bf16_lo(ks[j]);
-        kf[2 * j + 1] = attn::bf16_hi(ks[j]);
-      }
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        float a = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a = fmaf(qf[h][j], kf[j], a);
-        part[h * 8 + i] = a;
-      }
-    }
-    transposed_reduce<NV>(part, l16);
-
-    const int valid = t_end - p * PAGE;  // slots < valid hold tokens of this segment (>= 1)
-    float mx = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < NF; ++e) {
-      const int slot = 2 * (value_index<HG>(l16, e) % 8) + half;
-      if (slot >= valid) part[e] = -INFINITY;
-      mx = fmaxf(mx, part[e]);
-    }
-    mx = head_allreduce<HG, true>(mx);
-
-    float m_own = 0.f;
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      const float pm = __shfl_sync(FULL, mx, lane_of_head<HG>(h));
-      const float m_new = fmaxf(m_run[h], pm);
-      const float alpha = exp2f(m_run[h] - m_new);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[h][j] *= alpha;
-      if (h == own_h) {
-        l_own *= alpha;
-        m_own = m_new;
-      }
-      m_run[h] = m_new;
-    }
-    float pv[NF];
-#pragma unroll
-    for (int e = 0; e < NF; ++e) {
-      pv[e] = exp2f(part[e] - m_own);
-      if (HG > 1 || (l16 & 1) == 0) l_own += pv[e];
-    }
-
-    if (valid < PAGE) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (2 * i + half >= valid) vr[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t vs[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
-      float vf[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        vf[2 * j] = attn::bf16_lo(vs[j]);
-        vf[2 * j + 1] = attn::bf16_hi(vs[j]);
-      }
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        const int x = h * 8 + i;
-        const float pw = __shfl_sync(FULL, pv[NF > 1 ? (x & 1) : 0], (lane & 16) | owner_lane<HG>(x));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[h][j] = fmaf(pw, vf[j], acc[h][j]);
-      }
-    }
-  }
-
-  // Combine the two half-warps (same dims, different slots), then the warps.
-#pragma unroll
-  for (int h = 0; h < HG; ++h)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[h][j] += __shfl_xor_sync(FULL, acc[h][j], 16);
-  const float l_head = head_allreduce<HG, false>(l_own);
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    const float lh = __shfl_sync(FULL, l_head, lane_of_head<HG>(h));
-    if (lane == 0) {
-      sm_m[warp][h] = m_run[h];
-      sm_l[warp][h] = lh;
-    }
-    if (half == 0) {
-      *reinterpret_cast<float4*>(&sm_acc[warp][h][8 * l16]) =
-          make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-      *reinterpret_cast<float4*>(&sm_acc[warp][h][8 * l16 + 4]) =
-          make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
-    }
+    abort_flag_s = 0;
+    fence_mbar_init();
   }
   __syncthreads();
 
-  const int t = threadIdx.x;  // output dim
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    float big = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) big = fmaxf(big, sm_m[w][h]);
-    float lsum = 0.f, osum = 0.f;
-    if (big != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float c = exp2f(sm_m[w][h] - big);
-        lsum = fmaf(c, sm_l[w][h], lsum);
-        osum = fmaf(c, sm_acc[w][h][t], osum);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    bool ok = true;
+    int issued = 0;
+    const int32_t* row = block_table + static_cast<size_t>(b) * max_pages + p_begin;
+    for (int i0 = 0; ok && i0 < n_pages; i0 += 32) {
+      const int entry = i0 + lane < n_pages ? row[i0 + lane] : 0;
+      const int cnt = min(32, n_pages - i0);
+      for (int k = 0; k < cnt; ++k) {
+        const int page = __shfl_sync(FULL, entry, k);
+        const int i = i0 + k, st = i % NST;
+        if (lane == 0) {
+          if (i >= NST && !mbar_wait(&empty[st], ((i / NST) + 1) & 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
+          } else if (page < 0 || page >= num_pages) {
+            attn::record_status(status, ATTN_ERR_BAD_INDEX);
+            skip[st] = 1;
+            mbar_arrive(&full[st]);  // an empty page: nothing is read
+            issued = i + 1;
+          } else {
+            skip[st] = 0;
+            uint8_t* dst = ring + st * STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
+            tma_load_4d(dst, &tm_k, &full[st], 0, kvh, 0, page);
+            tma_load_4d(dst + PAGE_BYTES, &tm_v, &full[st], 0, kvh, 0, page);
+            issued = i + 1;
+          }
+        }
+        ok = __shfl_sync(FULL, ok, 0);
+        if (!ok) break;
       }
     }
-    const bool empty = !(lsum > 0.f);
-    const float out = empty ? 0.f : osum / lsum;
-    const float row_lse = empty ? -INFINITY : (big + log2f(lsum)) * attn::kLn2;
-    const size_t row = (size_t)b * Hq + h0 + h;
-    if (max_splits == 1) {
-      o[row * D + t] = __float2bfloat16_rn(out);
-      if (t == 0 && lse != nullptr) lse[row] = row_lse;
-    } else {
-      part_o[(row * max_splits + s) * D + t] = out;
-      if (t == 0) part_lse[row * max_splits + s] = row_lse;
+    if (lane == 0) {
+      if (!ok) {
+        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      int no_abort = 0;
+      for (int i = issued > NST ? issued - NST : 0; i < issued; ++i)
+        mbar_wait(&full[i % NST], (i / NST) & 1, &no_abort, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int cw = warp - 1;
+    const int grp = lane >> 3;       // token group within the warp
+    const int l8 = lane & 7;         // owns dims [16 l8, 16 l8 + 16)
+    const int own_h = l8 >> 1;       // head of the values this lane holds after the reduction
+    uint32_t qw[HG][8];
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      const int hq = h0 + min(h, nh - 1);  // padded heads reuse a real head's q
+      const uint4* qp = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq) * D + 16 * l8);
+      const uint4 a = qp[0], c = qp[1];
+      qw[h][0] = a.x; qw[h][1] = a.y; qw[h][2] = a.z; qw[h][3] = a.w;
+      qw[h][4] = c.x; qw[h][5] = c.y; qw[h][6] = c.z; qw[h][7] = c.w;
+    }
+    float acc[HG][16];
+    float m_run[HG];
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      m_run[h] = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[h][j] = 0.f;
+    }
+    float l_own = 0.f;
+    bool ok = true;
+
+    for (int i = cw; i < n_pages; i += NCW) {
+      const int st = i % NST;
+      ok = __all_sync(FULL, mbar_wait(&full[st], (i / NST) & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      if (!skip[st]) {
+        const uint8_t* kst = ring + st * STAGE_BYTES + l8 * 32;
+        const uint8_t* vst = kst + PAGE_BYTES;
+        const int valid = t_end - (p_begin + i) * PAGE;  // slots < valid hold tokens (>= 1)
+
+        // Partial dots of this lane's 16 dims: value index x = h * 4 + tt.
+        float part[HG * 4];
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          const int slot = grp + 4 * tt;
+          const uint4 k0 = *reinterpret_cast<const uint4*>(kst + slot * 256);
+          const uint4 k1 = *reinterpret_cast<const uint4*>(kst + slot * 256 + 16);
+          const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+          for (int h = 0; h < HG; ++h) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              a0 = fma_bf16_lo(qw[h][w], kw[w], a0);
+              a1 = fma_bf16_hi(qw[h][w], kw[w], a1);
+            }
+            part[h * 4 + tt] = a0 + a1;
+          }
+        }
+        // Transposed butterfly over the 8 lanes of the group (bits 2, 1, 0).
+        {
+          int n = HG * 4;
+#pragma unroll
+          for (int bit = 2; bit >= 0; --bit) {
+            const bool upper = (l8 >> bit) & 1;
+#pragma unroll
+            for (int x = 0; x < HG * 2; ++x) {
+              if (x < n / 2) {
+                const float send = upper ? part[x] : part[x + n / 2];
+                const float keep = upper ? part[x + n / 2] : part[x];
+                part[x] = keep + __shfl_xor_sync(FULL, send, 1 << bit);
+              }
+            }
+            n /= 2;
+          }
+        }
+        // Lane now holds x = 2 * l8 + e (e = 0, 1): head l8 / 2, tokens 2 (l8 & 1) + e.
+        float sv[2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tt = 2 * (l8 & 1) + e;
+          sv[e] = (grp + 4 * tt < valid) ? part[e] * scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sv[e]);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+        float m_own = 0.f;
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float pm = __shfl_sync(FULL, mx, 2 * h);
+          if (pm > m_run[h] + kRescaleThreshold) {  // warp-uniform
+            const float alpha = ex2(m_run[h] - pm);  // 0 on the first page (m_run = -inf)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[h][j] *= alpha;
+            if (h == own_h) l_own *= alpha;
+            m_run[h] = pm;
+          }
+          if (h == own_h) m_own = m_run[h];
+        }
+        const float p0 = ex2(sv[0] - m_own), p1 = ex2(sv[1] - m_own);
+        l_own += p0 + p1;
+        const uint32_t pw = attn::pack_bf16x2(p0, p1);
+
+#pragma unroll
+        for (int tp = 0; tp < 2; ++tp) {        // token pair (tokens 2tp, 2tp+1)
+          uint32_t ph[HG];
+#pragma unroll
+          for (int h = 0; h < HG; ++h) ph[h] = __shfl_sync(FULL, pw, (lane & ~7) | (2 * h + tp));
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tt = 2 * tp + e;
+            const int slot = grp + 4 * tt;
+            uint4 v0 = *reinterpret_cast<const uint4*>(vst + slot * 256);
+            uint4 v1 = *reinterpret_cast<const uint4*>(vst + slot * 256 + 16);
+            if (slot >= valid) {  // rows past the segment may hold anything
+              v0 = make_uint4(0u, 0u, 0u, 0u);
+              v1 = v0;
+            }
+            const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int h = 0; h < HG; ++h)
+#pragma unroll
+              for (int w = 0; w < 8; ++w) {
+                if (e == 0) fma_plo_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
+                else fma_phi_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
+              }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (!ok) {
+      if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+
+    // Combine the 4 token groups of the warp, then the consumer warps.
+#pragma unroll
+    for (int h = 0; h < HG; ++h)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        acc[h][j] += __shfl_xor_sync(FULL, acc[h][j], 8);
+        acc[h][j] += __shfl_xor_sync(FULL, acc[h][j], 16);
+      }
+    float lsum = l_own;
+    lsum += __shfl_xor_sync(FULL, lsum, 1);
+    lsum += __shfl_xor_sync(FULL, lsum, 8);
+    lsum += __shfl_xor_sync(FULL, lsum, 16);
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      const float lh = __shfl_sync(FULL, lsum, 2 * h);
+      if (lane == 0) {
+        sm_m[cw][h] = m_run[h];
+        sm_l[cw][h] = lh;
+      }
+      if (grp == 0) {
+        float4* dst = reinterpret_cast<float4*>(&sm_acc[cw][h][16 * l8]);
+        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+        dst[2] = make_float4(acc[h][8], acc[h][9], acc[h][10], acc[h][11]);
+        dst[3] = make_float4(acc[h][12], acc[h][13], acc[h][14], acc[h][15]);
+      }
+    }
+    named_barrier(1, NCW * 32);
+
+    const int t = threadIdx.x - 32;  // output dim
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      if (h >= nh) break;
+      float big = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) big = fmaxf(big, sm_m[w][h]);
+      float lw = 0.f, ow = 0.f;
+      if (big != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          const float c = ex2(sm_m[w][h] - big);
+          lw = fmaf(c, sm_l[w][h], lw);
+          ow = fmaf(c, sm_acc[w][h][t], ow);
+        }
+      }
+      const bool empty_row = !(lw > 0.f);
+      const float out = empty_row ? 0.f : ow / lw;
+      const float row_lse = empty_row ? -INFINITY : (big + log2f(lw)) * attn::kLn2;
+      const size_t r = static_cast<size_t>(b) * Hq + h0 + h;
+      if (max_splits == 1) {
+        o[r * D + t] = __float2bfloat16_rn(out);
+        if (t == 0 && lse != nullptr) lse[r] = row_lse;
+      } else {
+        part_o[(r * max_splits + s) * D + t] = out;
+        if (t == 0) part_lse[r * max_splits + s] = row_lse;
+      }
     }
   }
+}
+
+// k_pages / v_pages [num_pages, 16, Hkv, 128] bf16 as a 4-D tensor
+// {128, Hkv, 16, num_pages}; box {128, 1, 16, 1} = one page of one KV head.
+bool make_page_map(CUtensorMap* m, const void* base, int Hkv, int num_pages) {
+  attn_host::EncodeTiledFn enc = attn_host::encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(PAGE), static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(Hkv) * D * 2,
+                                 static_cast<cuuint64_t>(PAGE) * Hkv * D * 2};
+  const cuuint32_t box[4] = {D, 1, PAGE, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool set_smem_attr() {
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return false;
+    done = true;
+  }
+  return true;
 }
 
 }  // namespace
@@ -297,8 +419,9 @@ int decode_ctas_per_sm() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_bf16_kernel<4>, NW * 32, 0) !=
-            cudaSuccess ||
+    if (!set_smem_attr() ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_bf16_kernel, NUM_THREADS,
+                                                      SMEM_BYTES) != cudaSuccess ||
         n < 1)
       n = 1;
     cached[dev] = n;
@@ -313,23 +436,15 @@ attn_status_t launch_decode_bf16(const void* q, const void* k_pages, const void*
                                  int num_pages, float scale, cudaStream_t stream) {
   if (d != D || page_size != PAGE) return ATTN_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
-  const int hg = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
-  dim3 grid(max_splits, Hkv * (group / hg), B);
-  int* st = device_status_ptr();
-  const float sl2 = scale * attn::kLog2e;
-  auto args = [&](auto kern) {
-    kern<<<grid, NW * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_pages),
-        static_cast<const __nv_bfloat16*>(v_pages), block_table, seq_lens, chunk, max_splits,
-        static_cast<__nv_bfloat16*>(o), lse, part_o, part_lse, Hq, Hkv, max_pages, num_pages, sl2,
-        st);
-  };
-  if (hg == 4)
-    args(decode_bf16_kernel<4>);
-  else if (hg == 2)
-    args(decode_bf16_kernel<2>);
-  else
-    args(decode_bf16_kernel<1>);
+  if (!set_smem_attr()) return ATTN_ERR_CUDA;
+  CUtensorMap mk, mv;
+  if (!make_page_map(&mk, k_pages, Hkv, num_pages) || !make_page_map(&mv, v_pages, Hkv, num_pages))
+    return ATTN_ERR_CUDA;
+  dim3 grid(max_splits, Hkv * ((group + HG - 1) / HG), B);
+  decode_bf16_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+      mk, mv, static_cast<const __nv_bfloat16*>(q), block_table, seq_lens, chunk, max_splits,
+      static_cast<__nv_bfloat16*>(o), lse, part_o, part_lse, Hq, Hkv, max_pages, num_pages,
+      scale * attn::kLog2e, device_status_ptr());
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

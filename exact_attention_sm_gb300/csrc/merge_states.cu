@@ -4,82 +4,122 @@
 // with LSE_k combine as LSE = ln(sum_k e^LSE_k) and O = sum_k e^(LSE_k - LSE) O_k.
 // "FlashAttention and inference operators" (CUDA handbook), split-K merge
 // exercise: one row per worker, segments with no keys are skipped.
-// Evaluated with M = max_k LSE_k as the shift, ascending k, no atomics, so the
-// result is bitwise reproducible ("Lecture 4", sections 4.3 and 5.6).
+// Evaluated with M = max_k LSE_k as the shift, in an order fixed by the
+// problem size alone and with no atomics, so the result is bitwise
+// reproducible ("Lecture 4", sections 4.3 and 5.6).
 //
-// One warp per row; lane `l` owns dims 4l + 128c.  Every load is a 16-byte
-// vector and a row's segments are read in order.
+// One CTA (4 warps) per row.  The states of the row are dealt to the warps
+// (warp w takes s = w, w + 4, ...), each warp keeps 4 states' loads in flight
+// and lane l owns dims 4l + 128c; the 4 warp partials are then added in warp
+// order.  The summation order is fixed by (S, d) alone, so results are
+// bitwise reproducible.
 #include "common.cuh"
 
 namespace {
 
+constexpr int NW = 4;
+constexpr int UNROLL = 4;
+
 template <int C, bool BF16_OUT>
-__global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ o_parts,
-                                                    const float* __restrict__ lse_parts, int rows,
-                                                    int S, int d, void* __restrict__ o_out,
-                                                    float* __restrict__ lse_out) {
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float* lp = lse_parts + (size_t)row * S;
+__global__ void __launch_bounds__(NW * 32) merge_kernel(const float* __restrict__ o_parts,
+                                                        const float* __restrict__ lse_parts,
+                                                        int S, int d, void* __restrict__ o_out,
+                                                        float* __restrict__ lse_out) {
+  __shared__ float red[NW];
+  __shared__ __align__(16) float4 part_acc[NW][C * 32];
+  __shared__ float part_w[NW];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* lp = lse_parts + static_cast<size_t>(row) * S;
+  const float* op = o_parts + static_cast<size_t>(row) * S * d;
 
   float big = -INFINITY;
-  for (int s = lane; s < S; s += 32) big = fmaxf(big, lp[s]);
+  for (int s = threadIdx.x; s < S; s += NW * 32) big = fmaxf(big, lp[s]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) big = fmaxf(big, __shfl_xor_sync(0xffffffffu, big, off));
+  if (lane == 0) red[warp] = big;
+  __syncthreads();
+  big = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
 
   float4 acc[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (big != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float ls = lp[s];
-      if (ls == -INFINITY) continue;  // empty segment: its O is never read
-      const float w = expf(ls - big);
-      wsum += w;
-      const float* op = o_parts + ((size_t)row * S + s) * d;
+    for (int s0 = warp; s0 < S; s0 += NW * UNROLL) {
+      float w[UNROLL];
+      float4 x[UNROLL][C];
 #pragma unroll
-      for (int c = 0; c < C; ++c) {
-        const int j = 4 * lane + 128 * c;
-        if (j < d) {
-          const float4 x = *reinterpret_cast<const float4*>(op + j);
-          acc[c].x = fmaf(w, x.x, acc[c].x);
-          acc[c].y = fmaf(w, x.y, acc[c].y);
-          acc[c].z = fmaf(w, x.z, acc[c].z);
-          acc[c].w = fmaf(w, x.w, acc[c].w);
+      for (int u = 0; u < UNROLL; ++u) {
+        const int s = s0 + u * NW;
+        const float ls = s < S ? lp[s] : -INFINITY;
+        w[u] = ls == -INFINITY ? 0.f : expf(ls - big);  // empty segment: weight 0, O never read
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          const int j = 4 * lane + 128 * c;
+          x[u][c] = (w[u] > 0.f && j < d)
+                        ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(s) * d + j)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        wsum += w[u];
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          acc[c].x = fmaf(w[u], x[u][c].x, acc[c].x);
+          acc[c].y = fmaf(w[u], x[u][c].y, acc[c].y);
+          acc[c].z = fmaf(w[u], x[u][c].z, acc[c].z);
+          acc[c].w = fmaf(w[u], x[u][c].w, acc[c].w);
         }
       }
     }
   }
-  const bool empty = !(wsum > 0.f);
-  const float inv = empty ? 0.f : 1.f / wsum;
+#pragma unroll
+  for (int c = 0; c < C; ++c) part_acc[warp][c * 32 + lane] = acc[c];
+  if (lane == 0) part_w[warp] = wsum;
+  __syncthreads();
+  if (warp != 0) return;
+
+  float total = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) total += part_w[w];
+  const bool empty = !(total > 0.f);
+  const float inv = empty ? 0.f : 1.f / total;
 #pragma unroll
   for (int c = 0; c < C; ++c) {
     const int j = 4 * lane + 128 * c;
     if (j >= d) continue;
-    const float4 r = make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv);
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float4 p = part_acc[w][c * 32 + lane];
+      r.x += p.x;
+      r.y += p.y;
+      r.z += p.z;
+      r.w += p.w;
+    }
+    r = make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
     if (BF16_OUT) {
       uint2 packed = make_uint2(attn::pack_bf16x2(r.x, r.y), attn::pack_bf16x2(r.z, r.w));
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + (size_t)row * d + j) = packed;
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + static_cast<size_t>(row) * d + j) = packed;
     } else {
-      *reinterpret_cast<float4*>(static_cast<float*>(o_out) + (size_t)row * d + j) = r;
+      *reinterpret_cast<float4*>(static_cast<float*>(o_out) + static_cast<size_t>(row) * d + j) = r;
     }
   }
-  if (lane == 0 && lse_out != nullptr) lse_out[row] = empty ? -INFINITY : big + logf(wsum);
+  if (lane == 0 && lse_out != nullptr) lse_out[row] = empty ? -INFINITY : big + logf(total);
 }
 
 template <bool BF16_OUT>
 void launch(const float* o_parts, const float* lse_parts, int rows, int S, int d, void* o_out,
             float* lse_out, cudaStream_t stream) {
-  const int blocks = (rows + 3) / 4;
   const int c = (d + 127) / 128;
   if (c == 1)
-    merge_kernel<1, BF16_OUT><<<blocks, 128, 0, stream>>>(o_parts, lse_parts, rows, S, d, o_out, lse_out);
+    merge_kernel<1, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out, lse_out);
   else if (c == 2)
-    merge_kernel<2, BF16_OUT><<<blocks, 128, 0, stream>>>(o_parts, lse_parts, rows, S, d, o_out, lse_out);
+    merge_kernel<2, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out, lse_out);
   else
-    merge_kernel<4, BF16_OUT><<<blocks, 128, 0, stream>>>(o_parts, lse_parts, rows, S, d, o_out, lse_out);
+    merge_kernel<4, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out, lse_out);
 }
 
 }  // namespace

@@ -91,10 +91,13 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * Chooses one chunk length C (a multiple of page_size) shared by every
  * request; request b is cut into max(1, ceil(len_b / C)) segments.
  * Reading of [Lecture 4] section 4.2, section 5.6 and exercise 6: a work
- * unit is (request, KV head, segment); units run `slots` at a time; a plan
- * costs ceil(units / slots) * C.  If B * Hkv >= slots nothing is split.
- * Otherwise S = 1, 2, 4, ..., 64 segments (of the longest request) are
- * tried and the cheapest wins, ties going to fewer segments.
+ * unit is (request, KV head, segment) and costs its token count plus a
+ * fixed 64 tokens (launch and merge overhead; the pages give no figure);
+ * `slots` workers take the units in launch order (segment fastest), each
+ * as soon as it is free, and a plan costs the time the last one finishes.  If
+ * B * Hkv >= slots nothing is split.  Otherwise S = 1, 2, 4, ... segments
+ * (of the longest request, while B * Hkv * S <= 16 * slots) are tried and
+ * the cheapest wins, ties going to fewer segments.
  * num_splits > 0 forces C = ceil(ceil(max_len / num_splits) / page_size) *
  * page_size instead.  slots <= 0 means "ask the current device": SM count x
  * resident decode CTAs per SM.
@@ -125,8 +128,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_splits);
  * [LLM book] 10.3.7).  With more than one segment per request (split-KV,
  * Flash-Decoding: [LLM book] 10.3.7, [CUDA book] "Flash-Decoding and
  * split-K") each segment's normalised O_s and LSE_s go to the workspace and
- * are combined by the LSE merge (attn_merge_states) in ascending segment
- * order, so results are bitwise reproducible.
+ * are combined by the LSE merge (attn_merge_states) in a fixed order, so
+ * results are bitwise reproducible.
  *
  *   q            [B, Hq, d]                          input, dtype
  *   k_pages      [num_pages, page_size, Hkv, d]      input, dtype
@@ -204,8 +207,10 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_pages, cons
  * LSE[r] = M + ln(sum_s w_s) ([LLM book] 10.3.2 "LSE"; [CUDA book]
  * "Flash-Decoding and split-K" and its merge exercise).  States with
  * LSE = -inf are skipped (their O is not read); a row whose states are all
- * empty gets O = 0, LSE = -inf.  Summation runs in ascending s with no
- * atomics ([Lecture 4] 4.3 and 5.6 on determinism).
+ * empty gets O = 0, LSE = -inf.  The summation order is fixed by (S, d)
+ * alone (states dealt round-robin to 4 warps, the warps then added in
+ * order) and uses no atomics, so results are bitwise reproducible
+ * ([Lecture 4] 4.3 and 5.6 on determinism).
  *
  *   o_parts   [rows, S, d] fp32 input     lse_parts [rows, S] fp32 input
  *   o_out     [rows, d] output in out_dtype   lse_out [rows] fp32 or NULL

@@ -385,29 +385,55 @@ def _cdiv(a, b):
     return -(-a // b)
 
 
+UNIT_OVERHEAD_TOKENS = 64
+
+
+def plan_makespan(seq_lens, num_kv_heads, slots, chunk):
+    """Time of one split plan in the lecture's simple GPU model.
+
+    [Lecture 4] section 0.5 / 4.2: a work unit (request, KV head, segment)
+    takes time proportional to the tokens it reads, plus a fixed
+    UNIT_OVERHEAD_TOKENS for launching it and merging its partial state (the
+    lecture: splitting "only adds merge overhead" once there is enough work;
+    the pages give no number, 64 tokens is this reading's).  ``slots``
+    workers take the units in launch order (segment fastest, then KV head,
+    then request), each worker taking the next unit as soon as it is free;
+    the plan costs the time the last worker finishes.  With equal units this
+    is waves * unit length, the exercise's arithmetic.  Empty units cost 0.
+    """
+    import heapq
+    lens = [int(x) for x in seq_lens]
+    smax = max([1] + [_cdiv(n, chunk) for n in lens])
+    free = [0] * slots
+    for n in lens:
+        for _ in range(num_kv_heads):
+            for s in range(smax):
+                tokens = max(0, min(n, (s + 1) * chunk) - s * chunk)
+                t = heapq.heappop(free)
+                heapq.heappush(free, t + (tokens + UNIT_OVERHEAD_TOKENS if tokens > 0 else 0))
+    return max(free)
+
+
 def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
     """Choose the KV chunk length of each request for split-KV decode.
 
     Returns (chunk [B], splits [B]) with splits_b = ceil(len_b / chunk_b)
-    (at least 1) and every chunk a multiple of page_size.
+    (at least 1) and every chunk a multiple of page_size (one chunk shared by
+    all requests).
 
-    Reading of the pages ([Lecture 4] sections 4.2 and 0.5, exercise 6):
-    one work unit is (request, KV head, segment); in the lecture's simple
-    GPU model each unit's time is proportional to the tokens it reads and
-    ``slots`` units run at once, so a plan costs
-    waves * (tokens of the largest unit), waves = ceil(units / slots).
-    * If the batch already has B * Hkv >= slots units, no request is split
-      ("when the batch is large there are enough work units; splitting only
-      adds merge overhead").
-    * Otherwise the candidate segment counts are the exercise's
-      S = 1, 2, 4, ..., 64; S gives the chunk
-      C = ceil(ceil(max_len / S) / page_size) * page_size, and request b
-      gets ceil(len_b / C) segments.  The cheapest plan wins; on a tie the
-      smaller S (fewer segments, less merging) wins.  This picks 8 segments
-      for 2 requests x 16384 tokens x 8 KV heads on 132 SMs, the
-      exercise's answer, and 16 segments (16x faster) for 1 x 32K.
-    * num_splits > 0 forces at most that many segments per request, with
-      one chunk for all requests:
+    Reading of the pages ([Lecture 4] sections 4.2 and 5.6, exercise 6):
+    * If the batch already has B * Hkv >= slots work units, no request is
+      split ("when the batch is large there are enough work units; splitting
+      only adds merge overhead").
+    * Otherwise the candidate segment counts are powers of two, as in the
+      exercise (1, 2, 4, ...), up to the largest S with B * Hkv * S <= 16 *
+      slots (more waves than that add merging without better balance).  S
+      gives the chunk C = ceil(ceil(max_len / S) / page_size) * page_size.
+      Each plan is timed with plan_makespan; the fastest wins and a tie goes
+      to the smaller S.  This picks 8 segments for 2 requests x 16384 tokens
+      x 8 KV heads on 132 SMs (the exercise's answer) and 16 segments (16x
+      faster) for 1 x 32K.
+    * num_splits > 0 forces at most that many segments per request:
       C = ceil(ceil(max_len / num_splits) / page_size) * page_size.
     """
     lens = [int(x) for x in seq_lens]
@@ -416,14 +442,14 @@ def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
     if num_splits > 0:
         c = max(page_size, _cdiv(_cdiv(longest, num_splits), page_size) * page_size)
         return [c] * bsz, [max(1, _cdiv(n, c)) for n in lens]
-    best_c, best_cost = max(page_size, _cdiv(longest, page_size) * page_size), None
+    best_c = max(page_size, _cdiv(longest, page_size) * page_size)
     if bsz * num_kv_heads < slots:
+        best_t = None
         s = 1
-        while s <= 64:
+        while bsz * num_kv_heads * s <= 16 * slots:
             c = max(page_size, _cdiv(_cdiv(longest, s), page_size) * page_size)
-            units = num_kv_heads * sum(max(1, _cdiv(n, c)) for n in lens)
-            cost = _cdiv(units, slots) * c
-            if best_cost is None or cost < best_cost:
-                best_c, best_cost = c, cost
+            t = plan_makespan(lens, num_kv_heads, slots, c)
+            if best_t is None or t < best_t:
+                best_c, best_t = c, t
             s *= 2
     return [best_c] * bsz, [max(1, _cdiv(n, best_c)) for n in lens]
