@@ -100,9 +100,9 @@ def source_sha(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"prefill": ["prefill_sm103.cu", "common.cuh"],
+KERNEL_SOURCES = {"prefill": ["prefill_sm103.cu", "sm103_ptx.cuh", "common.cuh"],
                   "prefill_f32": ["prefill_f32.cu", "common.cuh"],
-                  "decode": ["decode_paged.cu", "common.cuh"]}
+                  "decode": ["decode_paged.cu", "sm103_ptx.cuh", "tma_host.h", "common.cuh"]}
 
 
 def traffic_for(workload, kind):
@@ -189,6 +189,12 @@ def reduce_max(value, backend_ready):
     t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(world, work_per_step, steps, max_total_s, unit_scale):
+    """Whole-job throughput: every rank processes the same per-step work
+    (replicas, weak scaling), timed by the slowest rank."""
+    return world * work_per_step * steps / max_total_s / unit_scale
 
 
 def barrier(backend_ready):
@@ -412,7 +418,7 @@ def run_gpu(args):
     total_s = reduce_max(total_s, dist_ready)
     unit = res["unit"]
     scale = 1e12 if unit == "TFLOP/s" else 1e9
-    value = world * work * args.steps / total_s / scale
+    value = whole_job_value(world, work, args.steps, total_s, scale)
 
     secondary = []
     if not args.main_only and world == 1:

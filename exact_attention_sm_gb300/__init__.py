@@ -34,6 +34,7 @@ SIGNATURES = {
                                        _I, _F, _I, _P]),
     "attn_merge_states": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P]),
     "attn_get_device_status": (_I, [_P]),
+    "attn_selftest_wait_timeout": (_I, [_I, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_version": (_I, []),
 }
@@ -180,3 +181,9 @@ def attn_merge_states(o_parts, lse_parts, out_dtype=torch.bfloat16, out=None, ls
 def attn_get_device_status(stream=None):
     """Reads and clears the device status word; returns the status name."""
     return STATUS.get(lib().attn_get_device_status(_stream(stream)), "?")
+
+
+def attn_selftest_wait_timeout(limit_ms=200, stream=None):
+    """Runs the bounded-wait self-test kernel (see include/attn.h)."""
+    _check(lib().attn_selftest_wait_timeout(int(limit_ms), _stream(stream)),
+           "attn_selftest_wait_timeout")

@@ -52,9 +52,10 @@ int64_t plan_makespan(const int32_t* lens, int B, int Hkv, int slots, int64_t ch
     for (int k = 0; k < Hkv; ++k)
       for (int64_t s = 0; s < smax; ++s) {
         const int64_t tokens = std::max<int64_t>(0, std::min<int64_t>(lens[b], (s + 1) * chunk) - s * chunk);
+        if (tokens == 0) break;  // this and the later segments of the request are empty (cost 0)
         const int64_t t = free_at.top();
         free_at.pop();
-        free_at.push(t + (tokens > 0 ? tokens + kUnitOverheadTokens : 0));
+        free_at.push(t + tokens + kUnitOverheadTokens);
       }
   int64_t last = 0;
   while (!free_at.empty()) {
@@ -89,6 +90,34 @@ void plan(const int32_t* lens, int B, int Hkv, int page, int num_splits, int slo
   for (int b = 0; b < B; ++b) smax = std::max<int64_t>(smax, cdiv(lens[b], best_c));
   *chunk = static_cast<int32_t>(best_c);
   *max_splits = static_cast<int32_t>(smax);
+}
+
+// The last plan of this thread, reused when the next call has the same
+// lengths and parameters (every layer of one decode step does).
+struct PlanCache {
+  std::vector<int32_t> lens;
+  int Hkv = -1, page = -1, num_splits = -1, slots = -1;
+  int32_t chunk = 0, max_splits = 0;
+};
+
+void plan_cached(const int32_t* lens, int B, int Hkv, int page, int num_splits, int slots,
+                 int32_t* chunk, int32_t* max_splits) {
+  thread_local PlanCache cache;
+  if (cache.Hkv == Hkv && cache.page == page && cache.num_splits == num_splits &&
+      cache.slots == slots && cache.lens.size() == static_cast<size_t>(B) &&
+      std::equal(cache.lens.begin(), cache.lens.end(), lens)) {
+    *chunk = cache.chunk;
+    *max_splits = cache.max_splits;
+    return;
+  }
+  plan(lens, B, Hkv, page, num_splits, slots, chunk, max_splits);
+  cache.lens.assign(lens, lens + B);
+  cache.Hkv = Hkv;
+  cache.page = page;
+  cache.num_splits = num_splits;
+  cache.slots = slots;
+  cache.chunk = *chunk;
+  cache.max_splits = *max_splits;
 }
 
 }  // namespace
@@ -142,7 +171,7 @@ attn_status_t attn_decode_plan(const int32_t* seq_lens_host, int B, int Hkv, int
     if (sms <= 0) return ATTN_ERR_CUDA;
     slots = sms * attn_host::decode_ctas_per_sm();
   }
-  plan(seq_lens_host, B, Hkv, page_size, num_splits, slots, chunk_out, max_splits_out);
+  plan_cached(seq_lens_host, B, Hkv, page_size, num_splits, slots, chunk_out, max_splits_out);
   return ATTN_OK;
 }
 
@@ -191,7 +220,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
       if (sms <= 0) return ATTN_ERR_CUDA;
       slots = sms * attn_host::decode_ctas_per_sm();
     }
-    plan(lens, B, Hkv, page_size, num_splits, slots, &chunk, &smax);
+    plan_cached(lens, B, Hkv, page_size, num_splits, slots, &chunk, &smax);
   }
   if (smax > 65535) return ATTN_ERR_UNSUPPORTED;
   float* part_o = nullptr;

@@ -228,6 +228,18 @@ attn_status_t attn_merge_states(const float* o_parts, const float* lse_parts, in
  */
 attn_status_t attn_get_device_status(attn_stream_t stream);
 
+/*
+ * attn_selftest_wait_timeout - failure-detection self-test (no counterpart in
+ * the pages).  Launches one thread that waits on an mbarrier nothing will
+ * ever arrive at, using the same bounded wait as the pipelined attention
+ * kernels, with a limit of `limit_ms` milliseconds (1..10000).  The wait
+ * runs out, the kernel records ATTN_ERR_DEVICE_TIMEOUT in the device status
+ * word and returns normally: nothing faults or hangs and the context stays
+ * usable.  Read (and clear) the result with attn_get_device_status(); until
+ * it is cleared, prefill CTAs skip their work.
+ */
+attn_status_t attn_selftest_wait_timeout(int limit_ms, attn_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* attn_status_string(attn_status_t status);
 

@@ -118,3 +118,8 @@ def test_planner_config5_lengths_fill_the_gpu():
     chunk, smax = ea.attn_decode_plan(lens, 8, 16, 0, 152 * 3)
     units = 8 * sum(max(1, -(-n // chunk)) for n in lens)
     assert units >= 152 and chunk % 16 == 0
+
+
+def test_selftest_rejects_bad_limits_on_host():
+    assert ea.lib().attn_selftest_wait_timeout(0, None) == 1
+    assert ea.lib().attn_selftest_wait_timeout(20000, None) == 1
