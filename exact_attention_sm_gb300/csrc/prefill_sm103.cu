@@ -303,29 +303,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
 
       // S_x = Q_x K^T for the K tile in ring slot st.
+      // Descriptors are built once; a K step or a ring slot only moves the
+      // start-address field (bits 0-13, address >> 4), so each MMA costs one
+      // 64-bit add of a constant.  Shared addresses stay below 256 KB, so the
+      // field never carries into the neighbouring bits.
+      const uint64_t q_desc0 = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + C::OFF_V, C::BLOCK_BYTES, 1024);
+      constexpr uint64_t kTileStep = C::TILE_BYTES >> 4;
       auto issue_qk = [&](int x, int st, bool last) {
-        const uint32_t q_addr = sbase + C::OFF_Q + x * C::TILE_BYTES;
-        const uint32_t k_addr = sbase + C::OFF_K + st * C::TILE_BYTES;
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>(x) * kTileStep;
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>(st) * kTileStep;
+        const uint32_t d_tmem = tmem + x * BN;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::BLOCK_BYTES + (k & 3) * 32;
-          mma_bf16_ss(tmem + x * BN, smem_desc_sw128(q_addr + off, 16, 1024),
-                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          constexpr uint32_t kBlk = C::BLOCK_BYTES >> 4;
+          const uint64_t off = (k >> 2) * kBlk + (k & 3) * 2;  // (k>>2) blocks + (k&3)*32 bytes
+          mma_bf16_ss(d_tmem, qd + off, kd + off, idesc_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[x]);
         if (last) mma_commit(&q_empty[x]);  // Q_x may be refilled for the next item
       };
       // O_x (+)= P_x V for the V tile in ring slot st; P_x sits in S_x's columns.
+      // B = V, MN-major: 16 keys = two 8-row groups of 128 bytes (2048 bytes
+      // per K step); LBO steps to the next 64-column block of d.
       auto issue_pv = [&](int x, int st, bool accumulate) {
-        const uint32_t v_addr = sbase + C::OFF_V + st * C::TILE_BYTES;
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>(st) * kTileStep;
+        const uint32_t d_tmem = tmem + C::O_COL + x * D;
+        const uint32_t a_tmem = tmem + x * BN;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          // B = V, MN-major: 16 keys = two 8-row groups of 128 bytes; LBO steps
-          // to the next 64-column block of d.
-          mma_bf16_ts(tmem + C::O_COL + x * D, tmem + x * BN + k * 8,
-                      smem_desc_sw128(v_addr + k * 16 * 128, C::BLOCK_BYTES, 1024), idesc_pv,
+        for (int k = 0; k < BN / 16; ++k)
+          mma_bf16_ts(d_tmem, a_tmem + k * 8, vd + static_cast<uint64_t>(k) * 128, idesc_pv,
                       (accumulate || k > 0) ? 1u : 0u);
-        }
       };
 
       for (int it = sched.first; ok && it < sched.last; it += sched.step) {
@@ -342,6 +351,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int j = 0; ok && j < nmax; ++j) {
           const int st = (g + j) % NS, ph = ((g + j) / NS) & 1;
           const int st1 = (g + j + 1) % NS, ph1 = ((g + j + 1) / NS) & 1;
+          bool v_ready = false, k_ready = false;  // each K/V tile is waited for once
           for (int x = 0; x < 2; ++x) {
             if (j >= w.n[x]) continue;
             if (!mbar_wait(&p_full[x], np[x] & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
@@ -351,11 +361,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ok = false;
               break;
             }
-            if (!mbar_wait(&v_full[st], ph, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            if (!v_ready && !mbar_wait(&v_full[st], ph, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            v_ready = true;
             tc_fence_after();
             issue_pv(x, st, j > 0);
             if (j + 1 < w.n[x]) {
-              if (!mbar_wait(&k_full[st1], ph1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+              if (!k_ready && !mbar_wait(&k_full[st1], ph1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+              k_ready = true;
               tc_fence_after();
               issue_qk(x, st1, j + 2 == w.n[x]);
             } else {
