@@ -41,7 +41,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // state) and `slots` workers take the units in launch order (segment
 // fastest, then KV head, then request), each as soon as it is free.  Returns
 // when the last worker finishes.
-constexpr int64_t kUnitOverheadTokens = 64;
+constexpr int64_t kUnitOverheadTokens = 512;
 
 int64_t plan_makespan(const int32_t* lens, int B, int Hkv, int slots, int64_t chunk) {
   int64_t smax = 1;

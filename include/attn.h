@@ -92,7 +92,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * request; request b is cut into max(1, ceil(len_b / C)) segments.
  * Reading of [Lecture 4] section 4.2, section 5.6 and exercise 6: a work
  * unit is (request, KV head, segment) and costs its token count plus a
- * fixed 64 tokens (launch and merge overhead; the pages give no figure);
+ * fixed 512 tokens (launch and merge overhead; the pages give no figure);
  * `slots` workers take the units in launch order (segment fastest), each
  * as soon as it is free, and a plan costs the time the last one finishes.  If
  * B * Hkv >= slots nothing is split.  Otherwise S = 1, 2, 4, ... segments

@@ -385,7 +385,7 @@ def _cdiv(a, b):
     return -(-a // b)
 
 
-UNIT_OVERHEAD_TOKENS = 64
+UNIT_OVERHEAD_TOKENS = 512
 
 
 def plan_makespan(seq_lens, num_kv_heads, slots, chunk):
@@ -395,7 +395,8 @@ def plan_makespan(seq_lens, num_kv_heads, slots, chunk):
     takes time proportional to the tokens it reads, plus a fixed
     UNIT_OVERHEAD_TOKENS for launching it and merging its partial state (the
     lecture: splitting "only adds merge overhead" once there is enough work;
-    the pages give no number, 64 tokens is this reading's).  ``slots``
+    the pages give no number: 512 tokens is this reading's, about the startup
+    cost of one decode CTA measured against its streaming rate).  ``slots``
     workers take the units in launch order (segment fastest, then KV head,
     then request), each worker taking the next unit as soon as it is free;
     the plan costs the time the last worker finishes.  With equal units this
