@@ -10,7 +10,9 @@
 // and finally O = O~ / l, LSE = m + ln l.  S and P never leave the SM.
 //
 // GB300 mapping (the pages' FlashAttention-4 notes, 10.3.6, name the
-// primitives; this arrangement is ours):
+// primitives; this arrangement is ours).  Two kernels share the method:
+// prefill_bf16_kernel (d = 128, below) and prefill_bf16_d64_kernel (d = 64,
+// further down: two CTAs per SM, one Q tile each).  For d = 128:
 //   * One persistent CTA per SM walks a static list of work items; an item is
 //     a pair of consecutive Q tiles (A = rows 256i.., B = rows 256i+128..) of
 //     one (batch, head), heaviest items first.  Both tiles consume the same
@@ -528,6 +530,489 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 64: two CTAs per SM, each streaming K/V for ONE 128-row Q tile.
+//
+// A d = 64 tile step is short on the tensor core (QK^T 4 MMAs, PV 8), so a
+// CTA that interleaves two Q tiles spends most of a step on barrier tests
+// and on one tile waiting for the other.  Here each CTA owns 256 TMEM
+// columns and runs one independent pipeline; the two CTAs on an SM fill each
+// other's gaps on the tensor core and on the MUFU.
+//   TMEM columns (per CTA): S 0..127, P 128..191 (bf16 pairs), O 192..255.
+// P has its own columns, so S(t+1) is written while the softmax still works
+// on P(t).  Each MMA group waits on ONE barrier that already combines what it
+// needs:
+//   qk_ready[slot of tile t]: K(t) arrived and the softmax has read S(t-1);
+//   pv_ready[slot of tile t]: V(t) arrived and the softmax wrote P(t).
+// A forwarder warp turns the TMA completions (k_full, v_full) into one
+// arrival each; each softmax warp adds one.  pv_done[slot] (one commit per
+// PV) releases the K/V slot to the producer and tells the softmax that P and
+// O may be rewritten.  Work items are single Q tiles.
+struct Cfg64 {
+  static constexpr int D = 64;
+  static constexpr int THREADS = 256;            // 8 warps; two CTAs per SM
+  static constexpr int TILE_BYTES = BM * D * 2;  // 16 KB: one 128 x 128-byte swizzled block
+  static constexpr int NS = 2;                   // K/V pipeline stages
+  static constexpr int NQ = 2;                   // Q buffers
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = NQ * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  static constexpr uint32_t COLS = 256;
+  static constexpr uint32_t P_COL = BN;
+  static constexpr uint32_t O_COL = BN + BN / 2;
+  static constexpr uint32_t kSoftmaxWarps = 4;
+};
+
+struct Item1 {
+  int bh, qt, n;
+};
+
+__device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int num_qt, int n_kv,
+                                              int causal) {
+  Item1 w;
+  if (grouped) {
+    w.bh = it / num_qt;
+    w.qt = num_qt - 1 - it % num_qt;
+  } else {
+    w.qt = num_qt - 1 - it / BH;
+    w.bh = it % BH;
+  }
+  w.n = causal ? min(n_kv, w.qt + 1) : n_kv;
+  return w;
+}
+
+__global__ void __launch_bounds__(Cfg64::THREADS, 2)
+    prefill_bf16_d64_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int BH, int Hq,
+                            int Hkv, int Lq, int Lk, int causal, float scale_log2, int* status) {
+  using C = Cfg64;
+  constexpr int D = C::D, NS = C::NS, NQ = C::NQ;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;                 // [NQ]
+  uint64_t* q_empty = q_full + NQ;         // [NQ]
+  uint64_t* k_full = q_empty + NQ;         // [NS] TMA only
+  uint64_t* v_full = k_full + NS;          // [NS] TMA only
+  uint64_t* qk_ready = v_full + NS;        // [NS]
+  uint64_t* pv_ready = qk_ready + NS;      // [NS]
+  uint64_t* pv_done = pv_ready + NS;       // [NS] PV of the slot's tile done (V slot free)
+  uint64_t* k_done = pv_done + NS;         // [NS] QK^T of the slot's tile done (K slot free)
+  uint64_t* s_full = k_done + NS;
+  uint64_t* o_done = s_full + 1;
+  uint64_t* o_free = o_done + 1;
+  uint64_t* drain = o_free + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_qt = (Lq + BM - 1) / BM;
+  const int num_items = BH * num_qt;
+  const int n_kv = (Lk + BN - 1) / BN;
+  const int group = Hq / Hkv;
+  // Short rows (or no mask): each CTA takes a contiguous run of items, head
+  // by head, so a head's K/V is re-read from L2.  Long causal rows: items
+  // heaviest first, dealt round-robin.
+  Schedule sched;
+  sched.grouped = !causal || num_qt <= 2 * kGroupedMaxPairs;
+  if (sched.grouped) {
+    sched.first = static_cast<int>(static_cast<long long>(num_items) * blockIdx.x / gridDim.x);
+    sched.last = static_cast<int>(static_cast<long long>(num_items) * (blockIdx.x + 1) / gridDim.x);
+    sched.step = 1;
+  } else {
+    sched.first = blockIdx.x;
+    sched.last = num_items;
+    sched.step = gridDim.x;
+  }
+  auto item_at = [&](int it) { return decode_item1(it, sched.grouped, BH, num_qt, n_kv, causal); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&qk_ready[s], C::kSoftmaxWarps + 1);
+      mbar_init(&pv_ready[s], C::kSoftmaxWarps + 1);
+      mbar_init(&pv_done[s], 1);
+      mbar_init(&k_done[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(o_done, 1);
+    mbar_init(o_free, 128);
+    mbar_init(drain, 1);
+    *abort_flag = (status != nullptr &&
+                   *reinterpret_cast<volatile int*>(status) == ATTN_ERR_DEVICE_TIMEOUT) ? 2 : 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (*abort_flag == 2) return;
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wait = [&](uint64_t* bar, int parity) {
+    return mbar_wait(bar, static_cast<uint32_t>(parity) & 1u, abort_flag, kWaitLimitNs);
+  };
+
+  if (warp < 4) {
+    // 128 x 64 + 128 x 192 registers = the 256 x 128 the CTA launched with.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
+      // K runs one tile ahead of V: a K slot frees when its QK^T is done
+      // (k_done), a V slot when its PV is done (pv_done).
+      // Issue order K(0), K(1), V(0), K(2), V(1), ...
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      struct Cur {
+        int it, j, n, bh_kv;
+      };
+      auto start = [&](Cur& c) {
+        c.it = sched.first;
+        c.j = 0;
+        c.n = 0;
+        if (c.it < sched.last) {
+          const Item1 w = item_at(c.it);
+          c.n = w.n;
+          c.bh_kv = (w.bh / Hq) * Hkv + (w.bh % Hq) / group;
+        }
+      };
+      auto next = [&](Cur& c) {
+        if (++c.j < c.n) return;
+        c.j = 0;
+        c.it += sched.step;
+        if (c.it < sched.last) {
+          const Item1 w = item_at(c.it);
+          c.n = w.n;
+          c.bh_kv = (w.bh / Hq) * Hkv + (w.bh % Hq) / group;
+        }
+      };
+      Cur ck, cv;
+      start(ck);
+      start(cv);
+      int tk = 0, tv = 0;  // K / V tiles issued
+      bool ok = true;
+      auto load_k = [&]() -> bool {
+        const int st = tk % NS;
+        if (tk >= NS && !wait(&k_done[st], (tk / NS) + 1)) return false;
+        mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
+        tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k, &k_full[st], 0, ck.j * BN, ck.bh_kv);
+        ++tk;
+        next(ck);
+        return true;
+      };
+      auto load_v = [&]() -> bool {
+        const int st = tv % NS;
+        if (tv >= NS && !wait(&pv_done[st], (tv / NS) + 1)) return false;
+        mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
+        tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v, &v_full[st], 0, cv.j * BN, cv.bh_kv);
+        ++tv;
+        next(cv);
+        return true;
+      };
+      if (ck.it < sched.last) ok = load_k();
+      while (ok && cv.it < sched.last) {
+        if (ck.it < sched.last) ok = load_k();
+        if (ok) ok = load_v();
+      }
+      if (!ok) {
+        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // Drain: every issued copy has landed before the CTA may exit (k_full
+      // and v_full count TMA bytes only; copies always complete).
+      int no_abort = 0;
+      for (int u = tk > NS ? tk - NS : 0; u < tk; ++u)
+        mbar_wait(&k_full[u % NS], (u / NS) & 1, &no_abort, kWaitLimitNs);
+      for (int u = tv > NS ? tv - NS : 0; u < tv; ++u)
+        mbar_wait(&v_full[u % NS], (u / NS) & 1, &no_abort, kWaitLimitNs);
+    } else if (warp == 3 && lane == 0) {
+      // ---------------------------------------------------------- Q producer
+      // Q tiles go out as soon as their buffer frees (the item NQ back has
+      // issued its last S), about an item ahead of the K/V stream.
+      prefetch_tmap(&tm_q);
+      int nq = 0;
+      bool ok = true;
+      for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+        const Item1 w = item_at(it);
+        const int qs = nq % NQ;
+        if (nq >= NQ && !wait(&q_empty[qs], (nq / NQ) - 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&q_full[qs], C::TILE_BYTES);
+        tma_load_3d(smem + C::OFF_Q + qs * C::TILE_BYTES, &tm_q, &q_full[qs], 0, w.qt * BM, w.bh);
+        ++nq;
+      }
+      if (!ok) {
+        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      int no_abort = 0;
+      for (int i = nq > NQ ? nq - NQ : 0; i < nq; ++i)
+        mbar_wait(&q_full[i % NQ], (i / NQ) & 1, &no_abort, kWaitLimitNs);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------------------------------------------------- forwarder
+      int total = 0;
+      for (int it = sched.first; it < sched.last; it += sched.step) total += item_at(it).n;
+      // Same order as the loads: K one tile ahead of V.
+      bool ok = total == 0 || wait(&k_full[0], 0);
+      if (ok && total > 0) mbar_arrive(&qk_ready[0]);
+      for (int t = 0; ok && t < total; ++t) {
+        if (t + 1 < total) {
+          ok = wait(&k_full[(t + 1) % NS], (t + 1) / NS);
+          if (!ok) break;
+          mbar_arrive(&qk_ready[(t + 1) % NS]);
+        }
+        ok = wait(&v_full[t % NS], t / NS);
+        if (!ok) break;
+        mbar_arrive(&pv_ready[t % NS]);
+      }
+      if (!ok) {
+        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+      // Descriptors are built once; a K step or a ring slot only moves the
+      // start-address field (address >> 4), which never carries (shared
+      // addresses stay below 256 KB).
+      const uint64_t q_desc0 = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + C::OFF_V, C::TILE_BYTES, 1024);
+      constexpr uint64_t kTileStep = C::TILE_BYTES >> 4;
+      int nq = 0;      // Q tiles done with (last S issued)
+      int nitem = 0;   // items whose first PV was issued
+      bool ok = true;
+      // S = Q K(t)^T; j is the step within an item of n steps.
+      auto qk = [&](int j, int n, int t) {
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>(nq % NQ) * kTileStep;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16_ss(tmem, qd + k * 2, kd + k * 2, idesc_qk, k > 0 ? 1u : 0u);
+        mma_commit(s_full);
+        mma_commit(&k_done[t % NS]);
+        if (j + 1 == n) {
+          mma_commit(&q_empty[nq % NQ]);  // that Q slot may be refilled
+          ++nq;
+        }
+      };
+      int t = 0;  // global step of the current item's K/V tile 0
+      if (sched.first < sched.last) {
+        const Item1 w0 = item_at(sched.first);
+        ok = wait(&qk_ready[0], 0) && wait(&q_full[0], 0);
+        if (ok) {
+          tc_fence_after();
+          qk(0, w0.n, 0);
+        }
+      }
+      for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+        const Item1 w = item_at(it);
+        for (int j = 0; ok && j < w.n; ++j) {
+          const int tt = t + j;
+          // S for step tt + 1: the next K/V tile of this item or the first
+          // of the next item.
+          if (j + 1 < w.n) {
+            if (!wait(&qk_ready[(tt + 1) % NS], (tt + 1) / NS)) { ok = false; break; }
+            tc_fence_after();
+            qk(j + 1, w.n, tt + 1);
+          } else if (it + sched.step < sched.last) {
+            const Item1 w2 = item_at(it + sched.step);
+            if (!wait(&qk_ready[(tt + 1) % NS], (tt + 1) / NS) ||
+                !wait(&q_full[nq % NQ], nq / NQ)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            qk(0, w2.n, tt + 1);
+          }
+          // O (+)= P V for step tt.
+          if (!wait(&pv_ready[tt % NS], tt / NS) ||
+              (j == 0 && nitem > 0 && !wait(o_free, nitem - 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>(tt % NS) * kTileStep;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            mma_bf16_ts(tmem + C::O_COL, tmem + C::P_COL + k * 8, vd + static_cast<uint64_t>(k) * 128,
+                        idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&pv_done[tt % NS]);
+          if (j == 0) ++nitem;
+          if (j + 1 == w.n) mma_commit(o_done);
+        }
+        t += w.n;
+      }
+      if (!ok) {
+        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      int no_abort = 0;
+      mma_commit(drain);
+      mbar_wait(drain, 0, &no_abort, kWaitLimitNs);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    // ------------------------------------------------------------ softmax warps
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;  // row within the Q tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off;
+    const uint32_t p_addr = tmem + lane_off + C::P_COL;
+    const uint32_t o_addr = tmem + lane_off + C::O_COL;
+    // Nothing was read before the first S: this warp's share of qk_ready(0).
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qk_ready[0]);
+    int t = 0;       // global step of the current item's K/V tile 0
+    int nitem = 0;
+    bool ok = true;
+    for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+      const Item1 w = item_at(it);
+      const int n = w.n;
+      const int grow = w.qt * BM + row;
+      float m_s = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        const int tt = t + j;
+        ok = __all_sync(FULL, wait(s_full, tt));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+        tmem_ld_wait();
+        float* s = reinterpret_cast<float*>(&sr[0][0]);
+        // S is in registers: S(tt + 1) may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qk_ready[(tt + 1) % NS]);
+
+        const bool need_mask = (j == n - 1) && (causal || (Lk % BN) != 0);
+        if (need_mask) {
+          const int kmax = causal ? min(Lk - 1, grow) : Lk - 1;  // last visible key
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (j * BN + c > kmax) s[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+        for (int c = 16; c < BN; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7]));
+        const float mt_s = mt * scale_log2;
+        float alpha = 1.f;
+        if (mt_s > m_s + kRescaleThreshold) {
+          alpha = ex2(m_s - mt_s);  // 0 on the first tile (m_s = -inf)
+          m_s = mt_s;
+        }
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m_s, -m_s);
+        float2 rs[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          float2 e = ffma2(make_float2(s[c], s[c + 1]), sc2, nm2);
+          e.x = ex2(e.x);
+          e.y = ex2(e.y);
+          rs[(c >> 1) & 3] = fadd2(rs[(c >> 1) & 3], e);
+          pk[c >> 6][(c >> 1) & 31] = attn::pack_bf16x2(e.x, e.y);
+        }
+        const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+        const float2 r = fadd2(r01, r23);
+        l = l * alpha + (r.x + r.y);
+        // PV of the previous step has read P and updated O.
+        if (tt > 0) {
+          ok = __all_sync(FULL, wait(&pv_done[(tt - 1) % NS], (tt - 1) / NS));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o32[32];
+            tmem_ld32(o_addr + c * 32, o32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+            tmem_st32(o_addr + c * 32, o32);
+          }
+        }
+        tmem_st32(p_addr, pk[0]);
+        tmem_st32(p_addr + 32, pk[1]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pv_ready[tt % NS]);
+      }
+      if (ok) ok = __all_sync(FULL, wait(o_done, nitem));
+      if (!ok) break;
+      tc_fence_after();
+      // O to registers, then release O at once: the next item's first PV may
+      // overwrite it while this thread normalises and stores.
+      uint32_t r[2][32];
+      tmem_ld32(o_addr, r[0]);
+      tmem_ld32(o_addr + 32, r[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(o_free);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (grow < Lq) {
+        __nv_bfloat16* orow = o + (static_cast<size_t>(w.bh) * Lq + grow) * D;
+#pragma unroll
+        for (int v8 = 0; v8 < 8; ++v8) {
+          const uint32_t* rv = &r[v8 >> 2][(v8 & 3) * 8];
+          uint4 q4;
+          q4.x = attn::pack_bf16x2(__uint_as_float(rv[0]) * inv, __uint_as_float(rv[1]) * inv);
+          q4.y = attn::pack_bf16x2(__uint_as_float(rv[2]) * inv, __uint_as_float(rv[3]) * inv);
+          q4.z = attn::pack_bf16x2(__uint_as_float(rv[4]) * inv, __uint_as_float(rv[5]) * inv);
+          q4.w = attn::pack_bf16x2(__uint_as_float(rv[6]) * inv, __uint_as_float(rv[7]) * inv);
+          *reinterpret_cast<uint4*>(orow + v8 * 8) = q4;
+        }
+        if (lse != nullptr)
+          lse[static_cast<size_t>(w.bh) * Lq + grow] =
+              l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
+      }
+      ++nitem;
+      t += n;
+    }
+    if (!ok) {
+      if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::COLS);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -565,11 +1050,21 @@ bool make_map(CUtensorMap* m, const void* base, int D, int L, int BH) {
 template <int D>
 attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                      int Hkv, int Lq, int Lk, int causal, float scale, cudaStream_t stream) {
-  using C = Cfg<D>;
+  // d = 64 runs the two-CTAs-per-SM kernel on single Q tiles, d = 128 the
+  // Q-tile-pair ping-pong kernel.
+  constexpr bool kD64 = D == 64;
+  constexpr int smem_bytes = kD64 ? Cfg64::SMEM_BYTES : Cfg<D>::SMEM_BYTES;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(prefill_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+    const void* fn;
+    if constexpr (kD64)
+      fn = reinterpret_cast<const void*>(prefill_bf16_d64_kernel);
+    else
+      fn = reinterpret_cast<const void*>(prefill_bf16_kernel<D>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+            cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_set = true;
   }
@@ -578,14 +1073,22 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
       !make_map(&mv, v, D, Lk, B * Hkv))
     return ATTN_ERR_CUDA;
   const int num_qt = (Lq + BM - 1) / BM;
-  const long long items = static_cast<long long>(B) * Hq * ((num_qt + 1) / 2);
+  const long long items = static_cast<long long>(B) * Hq * (kD64 ? num_qt : (num_qt + 1) / 2);
   if (items > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
   const int sms = attn_host::num_sms();
   if (sms <= 0) return ATTN_ERR_CUDA;
-  const int grid = static_cast<int>(items < sms ? items : sms);
-  prefill_bf16_kernel<D><<<grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, Lq, Lk, causal,
-      scale * attn::kLog2e, attn_host::device_status_ptr());
+  const long long slots = static_cast<long long>(sms) * (kD64 ? 2 : 1);
+  const int grid = static_cast<int>(items < slots ? items : slots);
+  const float scale_log2 = scale * attn::kLog2e;
+  if constexpr (kD64) {
+    prefill_bf16_d64_kernel<<<grid, Cfg64::THREADS, smem_bytes, stream>>>(
+        mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, Lq, Lk, causal,
+        scale_log2, attn_host::device_status_ptr());
+  } else {
+    prefill_bf16_kernel<D><<<grid, NUM_THREADS, smem_bytes, stream>>>(
+        mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, Lq, Lk, causal,
+        scale_log2, attn_host::device_status_ptr());
+  }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
