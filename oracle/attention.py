@@ -378,6 +378,62 @@ def decode_split_states(q_row, keys, values, scale, chunk):
 
 
 # --------------------------------------------------------------------------
+# Cascade (shared-prefix) decode
+# --------------------------------------------------------------------------
+
+def cascade_kv_tokens(prefix_len, unique_lens):
+    """KV tokens read by plain decode and by cascade decode.
+
+    [Lecture 4] section 4.4 and exercise 7: with n requests sharing a prefix,
+    plain decode reads the prefix once per request, n * prefix + sum(unique);
+    cascade reads it once, prefix + sum(unique).  The same count in blocks
+    gives section 5.3's block totals.  Returns (plain, cascade, saving) with
+    saving = 1 - cascade / plain.
+    """
+    unique = [int(u) for u in unique_lens]
+    plain = len(unique) * int(prefix_len) + sum(unique)
+    cascade = int(prefix_len) + sum(unique)
+    return plain, cascade, 1.0 - cascade / plain
+
+
+def decode_cascade(q, prefix_k, prefix_v, k_pages, v_pages, block_table, suffix_lens, scale):
+    """Decode over a shared prefix plus per-request suffixes, the cascade way.
+
+    [Lecture 4] section 4.4 (cascade attention) and 5.3 (composable formats):
+      1. prefix part: for each KV head, the query rows of that head from all n
+         requests are stacked into one (n * g) x d matrix and attend once to
+         the shared prefix K/V: one dense problem, the prefix read once;
+      2. unique part: each request's rows attend to its own suffix, read from
+         the paged cache (paged_gather);
+      3. the two attention states of each row are merged with the LSE
+         operator (merge_states).
+
+    q: [B, Hq, d]; prefix_k, prefix_v: [Hkv, P, d] (the shared prefix, stored
+    once); k_pages, v_pages, block_table, suffix_lens: the suffixes, as in
+    decode_paged.  A request with no suffix tokens keeps the prefix state.
+    Returns O [B, Hq, d] and LSE [B, Hq].
+    """
+    q = _f64(q)
+    b_, hq, d = q.shape
+    hkv = prefix_k.shape[0]
+    o = np.zeros(q.shape)
+    lse = np.zeros((b_, hq))
+    for kh in range(hkv):
+        heads = [h for h in range(hq) if kv_head_of(h, hq, hkv) == kh]
+        rows = [(b, h) for b in range(b_) for h in heads]
+        stacked = np.stack([q[b, h] for b, h in rows])
+        o_pre, lse_pre, _, _ = attention_dense(stacked, prefix_k[kh], prefix_v[kh], scale, False)
+        for i, (b, h) in enumerate(rows):
+            n = int(suffix_lens[b])
+            kk = paged_gather(k_pages, block_table[b], n, kh)
+            vv = paged_gather(v_pages, block_table[b], n, kh)
+            o_suf, lse_suf, _, _ = attention_dense(q[b, h][None, :], kk, vv, scale, False)
+            o[b, h], lse[b, h] = merge_states(np.stack([o_pre[i], o_suf[0]]),
+                                              np.array([lse_pre[i], lse_suf[0]]))
+    return o, lse
+
+
+# --------------------------------------------------------------------------
 # Split planning (host integer logic)
 # --------------------------------------------------------------------------
 

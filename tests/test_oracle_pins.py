@@ -360,3 +360,71 @@ def test_plan_invariants():
                     assert s <= forced
     # enough units already: nothing is split
     assert orc.plan_splits([1024] * 256, 8, 152, 16)[1] == [1] * 256
+
+
+# ---------------------------------------------------------------- cascade decode
+
+def test_cascade_tokens_lecture_exercise_7():
+    g = GOLD["lecture_exercise_7_cascade_tokens"]
+    plain, cascade, saving = orc.cascade_kv_tokens(g["prefix"], [g["unique"]] * g["n_requests"])
+    assert (plain, cascade) == (g["plain"], g["cascade"])
+    assert round(100 * saving) == g["saving_percent"]
+
+
+def test_cascade_blocks_lecture_5_3():
+    """Section 5.3 prints only the totals; the unique blocks are whatever the
+    plain count leaves after n x shared (76 - 4 x 15 = 16), in any split."""
+    g = GOLD["lecture_5_3_composable_blocks"]
+    unique_total = g["plain_blocks"] - g["n_requests"] * g["shared_blocks"]
+    for split in ([4, 4, 4, 4], [1, 2, 6, 7], [16, 0, 0, 0]):
+        assert sum(split) == unique_total
+        plain, cascade, _ = orc.cascade_kv_tokens(g["shared_blocks"], split)
+        assert (plain, cascade) == (g["plain_blocks"], g["cascade_blocks"])
+
+
+def test_cascade_saving_lecture_summary():
+    g = GOLD["lecture_cascade_64_requests"]
+    _, _, saving = orc.cascade_kv_tokens(g["prefix"], [g["unique"]] * g["n_requests"])
+    assert round(100 * saving) == g["saving_percent"]
+
+
+def _cascade_case(rng, prefix_len, suffix_lens, hkv=2, hq=6, d=16, page=4):
+    pk = rng.standard_normal((hkv, prefix_len, d))
+    pv = rng.standard_normal((hkv, prefix_len, d))
+    suf_k = [rng.standard_normal((hkv, n, d)) for n in suffix_lens]
+    suf_v = [rng.standard_normal((hkv, n, d)) for n in suffix_lens]
+    npages = sum(-(-n // page) for n in suffix_lens) + 1
+    perm = rng.permutation(npages)
+    kp = np.zeros((npages, page, hkv, d)); vp = np.zeros_like(kp)
+    maxp = max(1, max(-(-n // page) for n in suffix_lens))
+    table = -np.ones((len(suffix_lens), maxp), dtype=np.int64)
+    off = 0
+    for b, n in enumerate(suffix_lens):
+        for i in range(-(-n // page)):
+            table[b, i] = perm[off]; off += 1
+            for s in range(page):
+                t = i * page + s
+                if t < n:
+                    kp[table[b, i], s] = suf_k[b][:, t]
+                    vp[table[b, i], s] = suf_v[b][:, t]
+    q = rng.standard_normal((len(suffix_lens), hq, d))
+    return q, pk, pv, suf_k, suf_v, kp, vp, table
+
+
+@pytest.mark.parametrize("prefix_len,suffix_lens", [(7, [0, 1, 5, 13]), (33, [9, 0]), (1, [4])])
+def test_cascade_equals_attention_over_whole_sequence(prefix_len, suffix_lens):
+    """[Lecture 4] 4.4: the cascade result equals attending to prefix + suffix
+    as one sequence; checked against torch's float64 math attention on the
+    concatenated keys (an independent routine)."""
+    rng = np.random.default_rng(prefix_len * 100 + len(suffix_lens))
+    q, pk, pv, suf_k, suf_v, kp, vp, table = _cascade_case(rng, prefix_len, suffix_lens)
+    o, lse = orc.decode_cascade(q, pk, pv, kp, vp, table, suffix_lens, 0.3)
+    hq, hkv = q.shape[1], pk.shape[0]
+    for b, n in enumerate(suffix_lens):
+        kk = np.concatenate([pk, suf_k[b]], axis=1)   # [hkv, P + n, d]
+        vv = np.concatenate([pv, suf_v[b]], axis=1)
+        rep = hq // hkv
+        o_ref, lse_ref = _sdpa64(q[b][:, None, :], np.repeat(kk, rep, axis=0),
+                                 np.repeat(vv, rep, axis=0), 0.3, False)
+        assert np.abs(o[b] - o_ref[:, 0]).max() < 1e-12
+        assert np.abs(lse[b] - lse_ref[:, 0]).max() < 1e-12
