@@ -48,6 +48,10 @@ WORKLOADS = {
                                   dtype="bf16"),
     "decode-b256-ctx1024": dict(kind="decode", B=256, Hq=32, Hkv=8, d=128, lens="1024x256"),
     "decode-b4-long-splitkv": dict(kind="decode", B=4, Hq=32, Hkv=8, d=128, lens="uniform"),
+    # Lecture 4, section 4.4 demo 4: a 4096-token prefix shared by 64 requests,
+    # 256 unique tokens each.
+    "decode-cascade-b64-prefix4096": dict(kind="cascade", B=64, Hq=32, Hkv=8, d=128, prefix=4096,
+                                          suffix=256),
 }
 MAIN = "gpt2-medium-prefill"
 
@@ -57,6 +61,9 @@ def describe(name):
     if w["kind"] == "prefill":
         return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} L={w['L']} d={w['d']} "
                 f"{'causal' if w['causal'] else 'non-causal'} {w['dtype']} + LSE")
+    if w["kind"] == "cascade":
+        return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, shared prefix "
+                f"{w['prefix']} + {w['suffix']} unique tokens per request (16-token shuffled pages)")
     lens = "ctx 1024 each" if w["lens"] == "1024x256" else "ctx U[4096,131072] seed 2"
     return f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, {lens}, 16-token shuffled pages"
 
@@ -219,6 +226,8 @@ def make_step(name, torch, ea, inputs):
         def step():
             ea.attn_fwd(q, k, v, causal=w["causal"], scale=scale, out=o, lse=lse)
         return step, 1, prefill_flops(w), "flops", None
+    if w["kind"] == "cascade":
+        return make_cascade_step(w, torch, ea, inputs)
     lens = decode_lens(w)
     q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0,
                                                 device="cuda")
@@ -232,6 +241,80 @@ def make_step(name, torch, ea, inputs):
         ea.attn_decode_paged(q, kp, vp, table, sl, seq_lens_host=lens, out=o, lse=lse,
                              workspace=ws)
     return step, (1 if smax == 1 else 2), decode_bytes(w, lens), "bytes", (lens, chunk, smax)
+
+
+def make_cascade_step(w, torch, ea, inputs):
+    """Shared-prefix decode.  work = the KV bytes the cascade must read (the
+    prefix once, every suffix once); the extra entry also times plain paged
+    decode over the same whole sequences (prefix copied into each request's
+    pages), the read-the-prefix-n-times baseline of Lecture 4, section 4.4."""
+    B, P, n = w["B"], w["prefix"], w["suffix"]
+    lens = [n] * B
+    q, pk, pv, kp, vp, table, sl = inputs.cascade_inputs(P, lens, w["Hq"], w["Hkv"], w["d"], seed=0,
+                                                         device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, w["Hq"], dtype=torch.float32, device="cuda")
+    pc, _, ss = ea.attn_cascade_plan(B, w["Hq"], w["Hkv"], P, lens)
+    ws = torch.empty(ea.attn_cascade_workspace_bytes(B, w["Hq"], w["d"], pc, ss), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        ea.attn_decode_cascade(q, pk, pv, kp, vp, table, sl, seq_lens_host=lens, out=o, lse=lse,
+                               workspace=ws)
+    step = graphed(torch, call)
+    token_bytes = w["Hkv"] * w["d"] * 2 * 2
+    work = float(P + sum(lens)) * token_bytes
+    return step, 4, work, "bytes", {"prefix_chunks": pc, "suffix_splits": ss,
+                                    "plain_bytes": float(B * P + sum(lens)) * token_bytes,
+                                    "whole": (q, pk, pv, kp, vp, table, lens)}
+
+
+def plain_decode_over_whole_sequences(torch, ea, whole, steps, warmup, flush):
+    """Plain paged decode of the same requests over prefix + suffix pages."""
+    q, pk, pv, kp, vp, table, lens = whole
+    P = pk.shape[1]
+    Hkv, d = pk.shape[0], pk.shape[2]
+    full = [P + n for n in lens]
+    pages = [-(-x // 16) for x in full]
+    kp2 = torch.empty(sum(pages), 16, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    vp2 = torch.empty_like(kp2)
+    tab = torch.arange(sum(pages), dtype=torch.int32, device="cuda").view(len(lens), -1)
+    pre_k = pk.permute(1, 0, 2).reshape(P // 16, 16, Hkv, d)
+    pre_v = pv.permute(1, 0, 2).reshape(P // 16, 16, Hkv, d)
+    per = pages[0]
+    for b in range(len(lens)):
+        kp2[b * per: b * per + P // 16] = pre_k
+        vp2[b * per: b * per + P // 16] = pre_v
+        own = table[b, : -(-lens[b] // 16)].long()
+        kp2[b * per + P // 16: (b + 1) * per] = kp[own]
+        vp2[b * per + P // 16: (b + 1) * per] = vp[own]
+    sl = torch.tensor(full, dtype=torch.int32, device="cuda")
+    chunk, smax = ea.attn_decode_plan(full, Hkv, 16, 0)
+    ws = torch.empty(max(1, ea.attn_decode_workspace_bytes(len(lens), q.shape[1], d, smax)),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+
+    def call():
+        ea.attn_decode_paged(q, kp2, vp2, tab, sl, seq_lens_host=full, out=o, workspace=ws)
+    ms = time_steps(torch, graphed(torch, call), steps, warmup, flush)
+    return sum(ms) / len(ms)
+
+
+def graphed(torch, call):
+    """The step captured once as a CUDA graph (the library's launches go to
+    the capturing stream; the cascade's side stream forks from it and joins
+    back), replayed per step: a multi-launch step of tens of microseconds is
+    otherwise bounded by host launch latency."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    return g.replay
 
 
 def time_steps(torch, step, steps, warmup, flush):
@@ -277,7 +360,15 @@ def measure(name, torch, ea, inputs, steps, warmup, flush, peaks, peak_src):
     out = {"workload": describe(name), "value": value, "unit": unit, "ms_per_step": mean_ms,
            "ms_min": min(ms), "launches_per_step": launches, "roofline": roof,
            "algorithmic_" + kind: work}
-    if extra is not None:
+    if w["kind"] == "cascade":
+        plain_ms = plain_decode_over_whole_sequences(torch, ea, extra["whole"], steps, warmup, flush)
+        out["cascade"] = {"cuda_graph": True, "prefix_chunks": extra["prefix_chunks"],
+                          "suffix_splits": extra["suffix_splits"],
+                          "kv_bytes_plain_decode": extra["plain_bytes"],
+                          "effective_gbs": extra["plain_bytes"] / (mean_ms * 1e-3) / 1e9,
+                          "plain_decode_ms": plain_ms,
+                          "speedup_vs_plain_decode": plain_ms / mean_ms}
+    elif extra is not None:
         out["split_plan"] = {"chunk": extra[1], "max_splits": extra[2]}
     return out, step, launches, work
 

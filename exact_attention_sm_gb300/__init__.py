@@ -33,6 +33,10 @@ SIGNATURES = {
     "attn_decode_paged_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I,
                                        _I, _F, _I, _P]),
     "attn_merge_states": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P]),
+    "attn_cascade_plan": (_I, [_I, _I, _I, _I, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "attn_cascade_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "attn_decode_cascade": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I,
+                                 _I, _I, _I, _F, _P, _SZ, _I, _P]),
     "attn_get_device_status": (_I, [_P]),
     "attn_selftest_wait_timeout": (_I, [_I, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
@@ -159,6 +163,59 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, seq_lens_host=
         int(num_splits), _ptr(out), _ptr(lse), B, Hq, Hkv, d, block_table.shape[1], num_pages,
         float(scale), _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
     _check(st, "attn_decode_paged")
+    return out, lse
+
+
+def attn_cascade_plan(B, Hq, Hkv, prefix_len, suffix_lens_host, page_size=16, num_splits=0,
+                      prefix_slots=0, suffix_slots=0):
+    """Cascade plan: (prefix_chunks, suffix_chunk, suffix_splits); slots <= 0 query the device."""
+    arr = (ctypes.c_int32 * B)(*[int(x) for x in suffix_lens_host])
+    pc, sc, ss = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = lib().attn_cascade_plan(B, Hq, Hkv, int(prefix_len), ctypes.cast(arr, ctypes.c_void_p),
+                                 page_size, int(num_splits), int(prefix_slots), int(suffix_slots),
+                                 ctypes.byref(pc), ctypes.byref(sc), ctypes.byref(ss))
+    _check(st, "attn_cascade_plan")
+    return pc.value, sc.value, ss.value
+
+
+def attn_cascade_workspace_bytes(B, Hq, d, prefix_chunks, suffix_splits):
+    return lib().attn_cascade_workspace_bytes(B, Hq, d, prefix_chunks, suffix_splits)
+
+
+def attn_decode_cascade(q, prefix_k, prefix_v, k_pages, v_pages, block_table, seq_lens,
+                        seq_lens_host=None, num_splits=0, scale=None, out=None, lse=None,
+                        workspace=None, want_lse=True, stream=None):
+    """Shared-prefix decode. q [B,Hq,d]; prefix_k/v [Hkv,P,d]; the suffixes in the paged cache
+    (seq_lens = suffix lengths). Allocates the workspace when none is given.
+    Returns (o [B,Hq,d], lse [B,Hq])."""
+    for t, n in ((q, "q"), (prefix_k, "prefix_k"), (prefix_v, "prefix_v"), (k_pages, "k_pages"),
+                 (v_pages, "v_pages"), (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _need(t, n)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    prefix_len = prefix_k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if seq_lens_host is None:
+        seq_lens_host = seq_lens.cpu().tolist()
+    if workspace is None:
+        pc, _, ss = attn_cascade_plan(B, Hq, Hkv, prefix_len, seq_lens_host, page_size, num_splits)
+        workspace = torch.empty(attn_cascade_workspace_bytes(B, Hq, d, pc, ss), dtype=torch.uint8,
+                                device=q.device)
+    host_arr = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens_host])
+    st = lib().attn_decode_cascade(
+        _ptr(q), _ptr(prefix_k), _ptr(prefix_v), prefix_len, _ptr(k_pages), _ptr(v_pages),
+        _ptr(block_table), _ptr(seq_lens), ctypes.cast(host_arr, ctypes.c_void_p), page_size,
+        int(num_splits), _ptr(out), _ptr(lse), B, Hq, Hkv, d, block_table.shape[1], num_pages,
+        float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _dtype_code(q), _stream(stream))
+    _check(st, "attn_decode_cascade")
     return out, lse
 
 

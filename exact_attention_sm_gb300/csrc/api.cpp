@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <functional>
+#include <mutex>
 #include <queue>
 #include <vector>
 
@@ -19,12 +20,15 @@ int decode_ctas_per_sm();
 attn_status_t launch_prefill_f32(const float*, const float*, const float*, float*, float*, int, int,
                                  int, int, int, int, int, float, cudaStream_t);
 attn_status_t launch_prefill_bf16(const void*, const void*, const void*, void*, float*, int, int,
-                                  int, int, int, int, int, float, cudaStream_t);
+                                  int, int, int, int, int, float, int, cudaStream_t);
 attn_status_t launch_decode_bf16(const void*, const void*, const void*, const int32_t*,
                                  const int32_t*, int, int, int, void*, float*, float*, float*, int,
                                  int, int, int, int, int, float, cudaStream_t);
 attn_status_t launch_merge(const float*, const float*, int, int, int, void*, float*, attn_dtype_t,
                            cudaStream_t);
+attn_status_t launch_cascade_gather_q(const void*, void*, int, int, int, int, cudaStream_t);
+attn_status_t launch_cascade_merge(const void*, const float*, int, const float*, const float*, int,
+                                   int, int, int, int, void*, float*, cudaStream_t);
 }  // namespace attn_host
 
 namespace {
@@ -156,7 +160,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                                          static_cast<const float*>(v), static_cast<float*>(o), lse,
                                          B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0, scale, st);
   return attn_host::launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0,
-                                        scale, st);
+                                        scale, 1, st);
 }
 
 attn_status_t attn_decode_plan(const int32_t* seq_lens_host, int B, int Hkv, int page_size,
@@ -255,3 +259,181 @@ attn_status_t attn_merge_states(const float* o_parts, const float* lse_parts, in
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- cascade decode
+
+namespace {
+
+// Prefix chunks for the cascade prefix pass ("Lecture 4", section 4.4: the
+// stacked query rows attend to the prefix once; splitting the prefix into
+// chunks merged by the LSE operator only adds parallelism).  The prefill
+// kernel at d = 128 runs one item (two 128-row Q tiles of one head, one
+// chunk) per SM at a time, so a plan costs
+//   waves x (kItemOverheadTiles + K/V tiles per chunk),
+// waves = ceil(Hkv x tile pairs x chunks / slots).  Chunks are divisors of
+// the prefix of at least 128 tokens (one chunk if the prefix is shorter);
+// the cheapest plan wins, ties to fewer chunks.
+constexpr int64_t kItemOverheadTiles = 2;
+
+int cascade_prefix_chunks(int prefix_len, int rows_per_kvh, int Hkv, int slots) {
+  const int64_t pairs = cdiv(rows_per_kvh, 256);
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int c = 1; c == 1 || (int64_t)c * 128 <= prefix_len; ++c) {
+    if (prefix_len % c != 0) continue;
+    const int64_t waves = cdiv((int64_t)Hkv * pairs * c, slots);
+    const int64_t cost = waves * (kItemOverheadTiles + cdiv(prefix_len / c, 128));
+    if (best_cost < 0 || cost < best_cost) {
+      best = c;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// One side stream and its fork / join events per device, created on first
+// use and kept for the process.  Concurrent callers share them: the side
+// stream then runs their suffix passes one after another, and a join event
+// re-recorded by another call only makes a caller wait longer, never less.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+  static std::mutex mu;
+  static SideStream per_device[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& s = per_device[dev];
+  if (s.stream == nullptr) {
+    if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+      s.stream = nullptr;
+      return nullptr;
+    }
+  }
+  return &s;
+}
+
+struct CascadeLayout {
+  size_t q_stack, o_pre, lse_pre, o_suf, lse_suf, total;
+};
+
+CascadeLayout cascade_layout(int B, int Hq, int d, int prefix_chunks, int suffix_splits) {
+  CascadeLayout L;
+  const size_t rows = (size_t)B * Hq;
+  size_t off = 0;
+  L.q_stack = off;
+  off += round_up(rows * d * 2, kAlign);
+  L.o_pre = off;
+  off += round_up(rows * prefix_chunks * d * 2, kAlign);
+  L.lse_pre = off;
+  off += round_up(rows * prefix_chunks * sizeof(float), kAlign);
+  L.o_suf = off;
+  off += round_up(rows * suffix_splits * d * sizeof(float), kAlign);
+  L.lse_suf = off;
+  off += round_up(rows * suffix_splits * sizeof(float), kAlign);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+attn_status_t attn_cascade_plan(int B, int Hq, int Hkv, int prefix_len,
+                                const int32_t* suffix_lens_host, int page_size, int num_splits,
+                                int prefix_slots, int suffix_slots, int32_t* prefix_chunks_out,
+                                int32_t* suffix_chunk_out, int32_t* suffix_splits_out) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || prefix_len <= 0 || page_size <= 0 ||
+      num_splits < 0 || suffix_lens_host == nullptr || prefix_chunks_out == nullptr ||
+      suffix_chunk_out == nullptr || suffix_splits_out == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (prefix_slots <= 0) {
+    prefix_slots = attn_host::num_sms();
+    if (prefix_slots <= 0) return ATTN_ERR_CUDA;
+  }
+  *prefix_chunks_out = cascade_prefix_chunks(prefix_len, B * (Hq / Hkv), Hkv, prefix_slots);
+  return attn_decode_plan(suffix_lens_host, B, Hkv, page_size, num_splits, suffix_slots,
+                          suffix_chunk_out, suffix_splits_out);
+}
+
+size_t attn_cascade_workspace_bytes(int B, int Hq, int d, int prefix_chunks, int suffix_splits) {
+  if (B <= 0 || Hq <= 0 || d <= 0 || prefix_chunks <= 0 || suffix_splits <= 0) return 0;
+  return cascade_layout(B, Hq, d, prefix_chunks, suffix_splits).total;
+}
+
+attn_status_t attn_decode_cascade(const void* q, const void* prefix_k, const void* prefix_v,
+                                  int prefix_len, const void* k_pages, const void* v_pages,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  const int32_t* seq_lens_host, int page_size, int num_splits,
+                                  void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                  int max_pages_per_seq, int num_pages, float scale,
+                                  void* workspace, size_t workspace_bytes, attn_dtype_t dtype,
+                                  attn_stream_t stream) {
+  if (!q || !prefix_k || !prefix_v || !k_pages || !v_pages || !block_table || !seq_lens || !o ||
+      !seq_lens_host)
+    return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || prefix_len <= 0 ||
+      max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128 || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || Hq > 65535 || (int64_t)B * Hq > (1 << 24)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(prefix_k) || !aligned16(prefix_v) || !aligned16(k_pages) ||
+      !aligned16(v_pages) || !aligned16(o))
+    return ATTN_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens_host[b] < 0 || (int64_t)seq_lens_host[b] > (int64_t)max_pages_per_seq * page_size)
+      return ATTN_ERR_INVALID_ARG;
+  const int sms = attn_host::num_sms();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const int prefix_chunks = cascade_prefix_chunks(prefix_len, B * (Hq / Hkv), Hkv, sms);
+  int32_t chunk = max_pages_per_seq * page_size, smax = 1;
+  if (num_splits != 1)
+    plan_cached(seq_lens_host, B, Hkv, page_size, num_splits,
+                num_splits == 0 ? sms * attn_host::decode_ctas_per_sm() : 1, &chunk, &smax);
+  if (smax > 65535) return ATTN_ERR_UNSUPPORTED;
+  const CascadeLayout L = cascade_layout(B, Hq, d, prefix_chunks, smax);
+  if (workspace == nullptr || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return ATTN_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  void* q_stack = ws + L.q_stack;
+  void* o_pre = ws + L.o_pre;
+  float* lse_pre = reinterpret_cast<float*>(ws + L.lse_pre);
+  float* o_suf = reinterpret_cast<float*>(ws + L.o_suf);
+  float* lse_suf = reinterpret_cast<float*>(ws + L.lse_suf);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // The suffix decode does not depend on the prefix pass: it runs on a side
+  // stream forked from (and joined back into) the caller's stream, so its
+  // CTAs fill the SMs the prefix prefill leaves free.
+  SideStream* side = side_stream();
+  if (side == nullptr) return ATTN_ERR_CUDA;
+  if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  // 3. (side stream) each request's own suffix, as partial states;
+  attn_status_t s = attn_host::launch_decode_bf16(q, k_pages, v_pages, block_table, seq_lens,
+                                                  page_size, chunk, smax, o, lse, o_suf, lse_suf,
+                                                  B, Hq, Hkv, d, max_pages_per_seq, num_pages,
+                                                  scale, side->stream);
+  if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return ATTN_ERR_CUDA;
+
+  // 1. the query rows of each KV head, stacked over the requests;
+  if (s == ATTN_OK) s = attn_host::launch_cascade_gather_q(q, q_stack, B, Hq, Hkv, d, st);
+  // 2. those rows against the prefix, once, in prefix_chunks chunks: the
+  //    prefix [Hkv, P, d] is the same memory as [Hkv * chunks, P / chunks, d],
+  //    and output head h * chunks + c reads the Q rows of KV head h;
+  if (s == ATTN_OK)
+    s = attn_host::launch_prefill_bf16(q_stack, prefix_k, prefix_v, o_pre, lse_pre, 1,
+                                       Hkv * prefix_chunks, Hkv * prefix_chunks, B * (Hq / Hkv),
+                                       prefix_len / prefix_chunks, d, 0, scale, prefix_chunks, st);
+  // 4. prefix and suffix states merged per row, once the side stream is done.
+  if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (s == ATTN_OK)
+    s = attn_host::launch_cascade_merge(o_pre, lse_pre, prefix_chunks, o_suf, lse_suf, smax, B, Hq,
+                                        Hkv, d, o, lse, st);
+  return s;
+}

@@ -48,9 +48,11 @@ int decode_ctas_per_sm();  // resident decode CTAs per SM for the decode kernel
 attn_status_t launch_prefill_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                                  int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                                  float scale, cudaStream_t stream);
+// q_div > 1: output head h reads the Q rows of head h / q_div (several K/V
+// ranges share one set of queries).
 attn_status_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
-                                  float scale, cudaStream_t stream);
+                                  float scale, int q_div, cudaStream_t stream);
 attn_status_t launch_decode_bf16(const void* q, const void* k_pages, const void* v_pages,
                                  const int32_t* block_table, const int32_t* seq_lens, int page_size,
                                  int chunk, int max_splits, void* o, float* lse, float* part_o,
@@ -58,4 +60,9 @@ attn_status_t launch_decode_bf16(const void* q, const void* k_pages, const void*
                                  int num_pages, float scale, cudaStream_t stream);
 attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int rows, int S, int d,
                            void* o_out, float* lse_out, attn_dtype_t out_dtype, cudaStream_t stream);
+attn_status_t launch_cascade_gather_q(const void* q, void* q_stack, int B, int Hq, int Hkv, int d,
+                                      cudaStream_t stream);
+attn_status_t launch_cascade_merge(const void* o_pre, const float* lse_pre, int S_pre,
+                                   const float* o_suf, const float* lse_suf, int S_suf, int B,
+                                   int Hq, int Hkv, int d, void* o, float* lse, cudaStream_t stream);
 }  // namespace attn_host

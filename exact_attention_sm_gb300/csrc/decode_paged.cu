@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
       const float out = empty_row ? 0.f : ow / lw;
       const float row_lse = empty_row ? -INFINITY : (big + log2f(lw)) * attn::kLn2;
       const size_t r = static_cast<size_t>(b) * Hq + h0 + h;
-      if (max_splits == 1) {
+      if (part_o == nullptr) {  // one split: the final output
         o[r * D + t] = __float2bfloat16_rn(out);
         if (t == 0 && lse != nullptr) lse[r] = row_lse;
       } else {

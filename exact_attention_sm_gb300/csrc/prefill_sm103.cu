@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
                         float* __restrict__ lse, int BH, int Hq, int Hkv, int Lq, int Lk,
-                        int causal, float scale_log2, int* status) {
+                        int causal, float scale_log2, int q_div, int* status) {
   using C = Cfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q,
-                        &q_full[x], kb * 64, w.qt[x] * BM, w.bh);
+                        &q_full[x], kb * 64, w.qt[x] * BM, w.bh / q_div);
           ++nq[x];
         }
         for (int j = 1; ok && j < nmax; ++j) ok = issue_kv(j);
@@ -588,7 +588,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int BH, int Hq,
-                            int Hkv, int Lq, int Lk, int causal, float scale_log2, int* status) {
+                            int Hkv, int Lq, int Lk, int causal, float scale_log2, int q_div,
+                            int* status) {
   using C = Cfg64;
   constexpr int D = C::D, NS = C::NS, NQ = C::NQ;
   extern __shared__ uint8_t smem_raw[];
@@ -755,7 +756,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           break;
         }
         mbar_arrive_expect_tx(&q_full[qs], C::TILE_BYTES);
-        tma_load_3d(smem + C::OFF_Q + qs * C::TILE_BYTES, &tm_q, &q_full[qs], 0, w.qt * BM, w.bh);
+        tma_load_3d(smem + C::OFF_Q + qs * C::TILE_BYTES, &tm_q, &q_full[qs], 0, w.qt * BM,
+                    w.bh / q_div);
         ++nq;
       }
       if (!ok) {
@@ -1049,7 +1051,8 @@ bool make_map(CUtensorMap* m, const void* base, int D, int L, int BH) {
 
 template <int D>
 attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                     int Hkv, int Lq, int Lk, int causal, float scale, cudaStream_t stream) {
+                     int Hkv, int Lq, int Lk, int causal, float scale, int q_div,
+                     cudaStream_t stream) {
   // d = 64 runs the two-CTAs-per-SM kernel on single Q tiles, d = 128 the
   // Q-tile-pair ping-pong kernel.
   constexpr bool kD64 = D == 64;
@@ -1069,7 +1072,8 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
     attr_set = true;
   }
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, D, Lq, B * Hq) || !make_map(&mk, k, D, Lk, B * Hkv) ||
+  if (q_div < 1 || (B * Hq) % q_div != 0) return ATTN_ERR_INVALID_ARG;
+  if (!make_map(&mq, q, D, Lq, B * Hq / q_div) || !make_map(&mk, k, D, Lk, B * Hkv) ||
       !make_map(&mv, v, D, Lk, B * Hkv))
     return ATTN_ERR_CUDA;
   const int num_qt = (Lq + BM - 1) / BM;
@@ -1083,11 +1087,11 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   if constexpr (kD64) {
     prefill_bf16_d64_kernel<<<grid, Cfg64::THREADS, smem_bytes, stream>>>(
         mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, Lq, Lk, causal,
-        scale_log2, attn_host::device_status_ptr());
+        scale_log2, q_div, attn_host::device_status_ptr());
   } else {
     prefill_bf16_kernel<D><<<grid, NUM_THREADS, smem_bytes, stream>>>(
         mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, Lq, Lk, causal,
-        scale_log2, attn_host::device_status_ptr());
+        scale_log2, q_div, attn_host::device_status_ptr());
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -1098,9 +1102,9 @@ namespace attn_host {
 
 attn_status_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
-                                  float scale, cudaStream_t stream) {
-  if (d == 64) return launch<64>(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, causal, scale, stream);
-  if (d == 128) return launch<128>(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, causal, scale, stream);
+                                  float scale, int q_div, cudaStream_t stream) {
+  if (d == 64) return launch<64>(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, causal, scale, q_div, stream);
+  if (d == 128) return launch<128>(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, causal, scale, q_div, stream);
   return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -100,3 +100,17 @@ def merge_inputs(rows, S, d, seed=0, empty_frac=0.0):
         lse[drop] = float("-inf")
         lse[0, :] = float("-inf")
     return o, lse
+
+
+def cascade_inputs(prefix_len, suffix_lens, Hq, Hkv, d, seed=0, device="cpu"):
+    """Shared-prefix decode inputs: the suffixes exactly as decode_inputs
+    (q, paged cache, shuffled table) with ``seed``, then the prefix K and V
+    [Hkv, prefix_len, d] bf16 ~ N(0,1) drawn from ``seed + 100``.  Returns
+    (q, prefix_k, prefix_v, k_pages, v_pages, block_table, suffix_lens)."""
+    q, kp, vp, table, sl = decode_inputs(suffix_lens, Hq, Hkv, d, seed=seed, perm_seed=seed + 1,
+                                         device=device)
+    g = _gen(seed + 100, device)
+    pk = torch.randn(Hkv, prefix_len, d, generator=g, device=device).to(torch.bfloat16)
+    pv = torch.randn(Hkv, prefix_len, d, generator=g, device=device).to(torch.bfloat16)
+    return q, pk, pv, kp, vp, table, sl
+

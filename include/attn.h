@@ -200,6 +200,56 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_pages, cons
                                         float scale, attn_dtype_t dtype, attn_stream_t stream);
 
 /*
+ * Cascade (shared-prefix) decode ([Lecture 4] 4.4 "cascade attention" and
+ * 5.3 "composable formats").  B requests share one prefix of prefix_len
+ * tokens, stored once as prefix_k / prefix_v [Hkv, prefix_len, d] bf16
+ * (the dense (n, B_c) block of 5.3), and each has its own suffix in the
+ * paged cache (k_pages, v_pages, block_table, seq_lens as in
+ * attn_decode_paged; seq_lens holds the SUFFIX lengths, 0 allowed).  The
+ * result equals decode over prefix + suffix as one sequence:
+ *   1. the query rows of each KV head, from all B requests, are stacked into
+ *      one (B * g) x d matrix (g = Hq / Hkv) and attend to the prefix ONCE,
+ *      on the tensor cores (the prefill kernel; the prefix is cut into
+ *      prefix_chunks chunks, each a divisor of prefix_len, for parallelism);
+ *   2. each request attends to its own suffix (the paged decode kernel);
+ *   3. the prefix-chunk and suffix states of every row are merged with the
+ *      LSE operator in a fixed order (prefix chunks, then suffix segments).
+ * The prefix is read once instead of B times ([Lecture 4] exercise 7).
+ *
+ * attn_cascade_plan: prefix_chunks = the chunk count c (a divisor of
+ *   prefix_len with chunks of >= 128 tokens, or 1) minimising
+ *   ceil(Hkv x ceil(B*g/256) x c / prefix_slots) x (2 + ceil(prefix_len/c/128)),
+ *   the waves of prefill items times their K/V tiles plus a 2-tile per-item
+ *   overhead; ties go to fewer chunks.  The suffix split plan is
+ *   attn_decode_plan with suffix_slots.  prefix_slots <= 0 / suffix_slots <= 0 query the
+ *   current device (SMs / resident decode CTAs), as attn_decode_cascade does.
+ * attn_cascade_workspace_bytes: bytes attn_decode_cascade needs for the plan
+ *   (stacked queries, prefix-chunk states, suffix states), 256-byte aligned.
+ * attn_decode_cascade: q [B, Hq, d], o [B, Hq, d] bf16, lse [B, Hq] fp32 or
+ *   NULL.  d = 128, page_size = 16, bf16 only.  seq_lens_host (host copy of
+ *   the suffix lengths) is required: it fixes the plan.  prefix_len >= 1.
+ *   Pointers: device, 16-byte aligned (workspace 256-byte aligned), owned
+ *   by the caller.  Errors: ATTN_ERR_INVALID_ARG for bad sizes, NULLs,
+ *   misalignment or a suffix length outside [0, max_pages_per_seq * 16];
+ *   ATTN_ERR_WORKSPACE if the workspace is missing, short or misaligned;
+ *   ATTN_ERR_UNSUPPORTED for d != 128, page_size != 16 or non-bf16; device
+ *   errors as attn_fwd / attn_decode_paged (status word).
+ */
+attn_status_t attn_cascade_plan(int B, int Hq, int Hkv, int prefix_len,
+                                const int32_t* suffix_lens_host, int page_size, int num_splits,
+                                int prefix_slots, int suffix_slots, int32_t* prefix_chunks_out,
+                                int32_t* suffix_chunk_out, int32_t* suffix_splits_out);
+size_t attn_cascade_workspace_bytes(int B, int Hq, int d, int prefix_chunks, int suffix_splits);
+attn_status_t attn_decode_cascade(const void* q, const void* prefix_k, const void* prefix_v,
+                                  int prefix_len, const void* k_pages, const void* v_pages,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  const int32_t* seq_lens_host, int page_size, int num_splits,
+                                  void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                  int max_pages_per_seq, int num_pages, float scale,
+                                  void* workspace, size_t workspace_bytes, attn_dtype_t dtype,
+                                  attn_stream_t stream);
+
+/*
  * attn_merge_states - the LSE merge operator over S partial states per row.
  *
  * For each row r: M = max_s LSE[r,s] over non-empty states, w_s =

@@ -123,3 +123,56 @@ def test_planner_config5_lengths_fill_the_gpu():
 def test_selftest_rejects_bad_limits_on_host():
     assert ea.lib().attn_selftest_wait_timeout(0, None) == 1
     assert ea.lib().attn_selftest_wait_timeout(20000, None) == 1
+
+
+def casc(**kw):
+    lens = (ctypes.c_int32 * 2)(100, 0)
+    args = dict(q=FAKE, pk=FAKE, pv=FAKE, P=300, k=FAKE, v=FAKE, table=FAKE, lens=FAKE,
+                lens_host=ctypes.cast(lens, ctypes.c_void_p), page=16, splits=0, o=FAKE, lse=None,
+                B=2, Hq=8, Hkv=2, d=128, max_pages=7, num_pages=14, scale=0.1, ws=None, ws_bytes=0,
+                dtype=ea.ATTN_BF16)
+    args.update(kw)
+    a = args
+    return ea.lib().attn_decode_cascade(a["q"], a["pk"], a["pv"], a["P"], a["k"], a["v"], a["table"],
+                                        a["lens"], a["lens_host"], a["page"], a["splits"], a["o"],
+                                        a["lse"], a["B"], a["Hq"], a["Hkv"], a["d"], a["max_pages"],
+                                        a["num_pages"], a["scale"], a["ws"], a["ws_bytes"],
+                                        a["dtype"], None)
+
+
+def test_cascade_rejects_on_host():
+    assert casc(q=None) == 1
+    assert casc(pk=None) == 1
+    assert casc(lens_host=None) == 1          # the host lengths fix the plan
+    assert casc(P=0) == 1
+    assert casc(Hkv=3) == 1
+    assert casc(splits=-1) == 1
+    assert casc(d=64) == 2
+    assert casc(page=32) == 2
+    assert casc(dtype=ea.ATTN_F32) == 2
+    assert casc(pk=MISALIGNED) == 1
+    assert casc(max_pages=6) == 1             # suffix length 100 > 6 * 16
+
+
+def prefix_chunks_rule(P, rows, Hkv, slots):
+    """The documented rule: among divisors c of P with chunks of >= 128
+    tokens (or c = 1), minimise waves x (2 + tiles per chunk); ties to fewer."""
+    pairs = -(-rows // 256)
+    ok = [c for c in range(1, max(1, P // 128) + 1) if P % c == 0]
+    cost = lambda c: -(-Hkv * pairs * c // slots) * (2 + -(-(P // c) // 128))
+    return min(ok, key=lambda c: (cost(c), c))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,P,slots", [(64, 32, 8, 4096, 152), (4, 32, 8, 300, 152),
+                                              (2, 8, 2, 100, 152), (256, 32, 8, 1000, 16),
+                                              (1, 4, 1, 131072, 152), (7, 6, 3, 2560, 152)])
+def test_cascade_plan(B, Hq, Hkv, P, slots):
+    lens = [0, 5, 300, 16][:B] + [17] * max(0, B - 4)
+    pc, sc, ss = ea.attn_cascade_plan(B, Hq, Hkv, P, lens, 16, 0, slots, 456)
+    assert pc == prefix_chunks_rule(P, B * (Hq // Hkv), Hkv, slots)
+    assert P % pc == 0
+    assert (sc, ss) == ea.attn_decode_plan(lens, Hkv, 16, 0, 456)
+    rows = B * Hq
+    r = lambda x: -(-x // 256) * 256
+    want = r(rows * 128 * 2) + r(rows * pc * 128 * 2) + r(rows * pc * 4) + r(rows * ss * 128 * 4) + r(rows * ss * 4)
+    assert ea.attn_cascade_workspace_bytes(B, Hq, 128, pc, ss) == want
