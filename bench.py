@@ -34,6 +34,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "prefill attn TFLOPS & paged-decode KV GB/s on 1 GB300, % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's published per-GPU GB300 figures (dense bf16 tensor throughput;
+# HBM3e bandwidth), reported beside the measured roofs as a second reference.
+DATASHEET = {"TFLOP/s": 2250.0, "GB/s": 8000.0}
 
 WORKLOADS = {
     "gpt2-medium-prefill": dict(kind="prefill", B=64, Hq=16, Hkv=16, L=1024, d=64, causal=True,
@@ -356,6 +359,9 @@ def measure(name, torch, ea, inputs, steps, warmup, flush, peaks, peak_src):
                 "peak_source": f"hbm_gbs of {peak_src}"}
         tkind = "decode"
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if roof["bound"] in ("tensor", "hbm"):
+        roof["datasheet"] = {"peak": DATASHEET[roof["unit"]],
+                             "frac": roof["achieved"] / DATASHEET[roof["unit"]]}
     roof["traffic"] = traffic_for(name, tkind)
     out = {"workload": describe(name), "value": value, "unit": unit, "ms_per_step": mean_ms,
            "ms_min": min(ms), "launches_per_step": launches, "roofline": roof,
