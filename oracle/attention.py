@@ -119,7 +119,7 @@ def block_state(scores, values):
 # Dense attention: the definition the fused kernel must reproduce
 # --------------------------------------------------------------------------
 
-def attention_dense(q, k, v, scale, causal=False):
+def attention_dense(q, k, v, scale, causal=False, causal_offset=0):
     """Standard (materialising) attention for one head, in float64.
 
     [Tiling blog] section 01: S = Q K^T * scale, P = softmax(S), O = P V,
@@ -127,6 +127,9 @@ def attention_dense(q, k, v, scale, causal=False):
     follows [Tiling blog] section 06: query i sees key j only if j <= i, and
     masked scores are -inf before the max and the sum.  The per-row
     log-sum-exp is LSE = m + ln l ([LLM book] 10.3.2, "LSE").
+
+    causal_offset shifts the rule to key j <= i + causal_offset (0: the
+    square rule above; Lk - Lq: the bottom-right alignment of prefill_varlen).
 
     A row with no visible key (all -inf) has l = 0; its output is O = 0 and
     LSE = -inf rather than NaN ([CUDA book] split-K merge exercise: skip
@@ -142,7 +145,7 @@ def attention_dense(q, k, v, scale, causal=False):
     if causal:
         i = np.arange(lq)[:, None]
         j = np.arange(lk)[None, :]
-        s = np.where(j > i, NEG_INF, s)
+        s = np.where(j > i + int(causal_offset), NEG_INF, s)
     if lk == 0:
         m = np.full(lq, NEG_INF)
     else:
@@ -310,6 +313,42 @@ def prefill_rows(q, k, v, scale, causal, rows):
             out_o[n] = orow
             out_lse[n] = lrow
     return out_o, out_lse
+
+
+# --------------------------------------------------------------------------
+# Variable-length (packed) prefill
+# --------------------------------------------------------------------------
+
+def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale, causal):
+    """Prefill over sequences packed end to end.
+
+    [LLM book] 10.3.8 (variable-length batching): the sequences of a batch
+    are concatenated into [total_tokens, heads, d], and cu_seqlens_q /
+    cu_seqlens_k of shape [B + 1] hold the cumulative lengths (lengths 3, 5,
+    2 give [0, 3, 8, 10]); sequence b owns rows cu[b] .. cu[b+1]-1 and no
+    sequence sees another.  GQA as in prefill.
+
+    Causal with Lq != Lk is not defined on the pages; the reading here aligns
+    it bottom-right: query i of a sequence with Lq queries and Lk keys sees
+    key j <= i + (Lk - Lq), the queries being the last Lq tokens of that
+    sequence (chunked prefill).  With Lq = Lk this is the square rule.
+
+    q [total_q, Hq, d]; k, v [total_k, Hkv, d].  Returns O [total_q, Hq, d]
+    and LSE [total_q, Hq].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    hq, hkv = q.shape[1], k.shape[1]
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:2])
+    for b in range(len(cu_seqlens_q) - 1):
+        q0, q1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        k0, k1 = int(cu_seqlens_k[b]), int(cu_seqlens_k[b + 1])
+        for h in range(hq):
+            kh = kv_head_of(h, hq, hkv)
+            oo, ll, _, _ = attention_dense(q[q0:q1, h], k[k0:k1, kh], v[k0:k1, kh], scale, causal,
+                                           (k1 - k0) - (q1 - q0))
+            o[q0:q1, h], lse[q0:q1, h] = oo, ll
+    return o, lse
 
 
 # --------------------------------------------------------------------------

@@ -428,3 +428,66 @@ def test_cascade_equals_attention_over_whole_sequence(prefix_len, suffix_lens):
                                  np.repeat(vv, rep, axis=0), 0.3, False)
         assert np.abs(o[b] - o_ref[:, 0]).max() < 1e-12
         assert np.abs(lse[b] - lse_ref[:, 0]).max() < 1e-12
+
+
+# ---------------------------------------------------------------- varlen prefill
+
+def test_varlen_cu_seqlens_llm_book_10_3_8():
+    """The page's packing example, and sequences that never see each other:
+    each packed sequence equals its own dense attention."""
+    g = GOLD["llm_book_varlen_cu_seqlens"]
+    cu = np.concatenate([[0], np.cumsum(g["lengths"])]).tolist()
+    assert cu == g["cu_seqlens"]
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((cu[-1], 4, 8))
+    k = rng.standard_normal((cu[-1], 2, 8))
+    v = rng.standard_normal((cu[-1], 2, 8))
+    for causal in (False, True):
+        o, lse = orc.prefill_varlen(q, k, v, cu, cu, 0.4, causal)
+        for b in range(len(g["lengths"])):
+            sl = slice(cu[b], cu[b + 1])
+            o_ref, lse_ref = _sdpa64(q[sl].transpose(1, 0, 2), k[sl].transpose(1, 0, 2),
+                                     v[sl].transpose(1, 0, 2), 0.4, causal)
+            assert np.abs(o[sl] - o_ref.transpose(1, 0, 2)).max() < 1e-12
+            assert np.abs(lse[sl] - lse_ref.T).max() < 1e-12
+
+
+def _sdpa64_mask(q, k, v, scale, mask):
+    """torch float64 math attention with an explicit boolean mask (True = visible)."""
+    q, k, v = (torch.as_tensor(np.asarray(x, np.float64)) for x in (q, k, v))
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    m = torch.as_tensor(mask)
+    with sdpa_kernel(SDPBackend.MATH):
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m, scale=scale)
+    s = ((q @ k.transpose(-1, -2)) * scale).masked_fill(~m, -math.inf)
+    return o.numpy(), torch.logsumexp(s, dim=-1).numpy()
+
+
+@pytest.mark.parametrize("lq,lk", [(5, 12), (12, 12), (1, 9), (130, 300)])
+def test_varlen_bottom_right_causal_matches_masked_sdpa(lq, lk):
+    """Bottom-right causal (query i sees key j <= i + lk - lq) against torch's
+    attention with the same explicit mask; GQA 4 query heads on 2 KV heads."""
+    rng = np.random.default_rng(lq * 1000 + lk)
+    q = rng.standard_normal((lq, 4, 16))
+    k = rng.standard_normal((lk, 2, 16))
+    v = rng.standard_normal((lk, 2, 16))
+    o, lse = orc.prefill_varlen(q, k, v, [0, lq], [0, lk], 0.25, True)
+    mask = np.arange(lk)[None, :] <= np.arange(lq)[:, None] + (lk - lq)
+    o_ref, lse_ref = _sdpa64_mask(q.transpose(1, 0, 2), np.repeat(k, 2, 1).transpose(1, 0, 2),
+                                  np.repeat(v, 2, 1).transpose(1, 0, 2), 0.25, mask)
+    assert np.abs(o - o_ref.transpose(1, 0, 2)).max() < 1e-12
+    assert np.abs(lse - lse_ref.T).max() < 1e-12
+
+
+def test_varlen_rows_with_no_visible_key():
+    """More queries than keys under bottom-right causal: the first lq - lk
+    rows see nothing and give O = 0, LSE = -inf (never NaN)."""
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((6, 1, 8))
+    k = rng.standard_normal((2, 1, 8))
+    v = rng.standard_normal((2, 1, 8))
+    o, lse = orc.prefill_varlen(q, k, v, [0, 6], [0, 2], 0.3, True)
+    assert (o[:4] == 0).all() and np.isneginf(lse[:4]).all()
+    # rows 4 and 5 see keys j <= row + (2 - 6), i.e. the square rule on the last two rows
+    o_last, lse_last, _, _ = orc.attention_dense(q[4:, 0], k[:, 0], v[:, 0], 0.3, True, 0)
+    assert np.isfinite(lse[4:]).all() and np.abs(o[4:, 0] - o_last).max() == 0
