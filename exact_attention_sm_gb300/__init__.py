@@ -26,6 +26,8 @@ STATUS = {
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                             _I, _P]),
     "attn_decode_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F,
@@ -109,6 +111,36 @@ def attn_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, want_lse=Tru
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Lq, Lk, d,
                         int(bool(causal)), float(scale), _dtype_code(q), _stream(stream))
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=None, max_seqlen_k=None,
+                    causal=False, scale=None, out=None, lse=None, want_lse=True, stream=None):
+    """Packed prefill. q [total_q,Hq,d], k/v [total_k,Hkv,d] bf16; cu_seqlens_q/k int32 [B+1] on
+    the device. Causal is aligned bottom-right. Returns (o [total_q,Hq,d], lse [total_q,Hq])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cu_seqlens_q, "cu_seqlens_q"),
+                 (cu_seqlens_k, "cu_seqlens_k")):
+        _need(t, n)
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    if max_seqlen_q is None or max_seqlen_k is None:
+        cq, ck = cu_seqlens_q.cpu(), cu_seqlens_k.cpu()
+        max_seqlen_q = int((cq[1:] - cq[:-1]).max()) if max_seqlen_q is None else max_seqlen_q
+        max_seqlen_k = int((ck[1:] - ck[:-1]).max()) if max_seqlen_k is None else max_seqlen_k
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(total_q, Hq, dtype=torch.float32, device=q.device)
+    st = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                               _ptr(cu_seqlens_k), B, max(1, int(max_seqlen_q)),
+                               max(1, int(max_seqlen_k)), total_q, total_k, Hq, Hkv, d,
+                               1 if causal else 0, float(scale), _dtype_code(q), _stream(stream))
+    _check(st, "attn_fwd_varlen")
     return out, lse
 
 

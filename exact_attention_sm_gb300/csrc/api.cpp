@@ -21,6 +21,9 @@ attn_status_t launch_prefill_f32(const float*, const float*, const float*, float
                                  int, int, int, int, int, float, cudaStream_t);
 attn_status_t launch_prefill_bf16(const void*, const void*, const void*, void*, float*, int, int,
                                   int, int, int, int, int, float, int, cudaStream_t);
+attn_status_t launch_prefill_bf16_varlen(const void*, const void*, const void*, void*, float*,
+                                         const int*, const int*, int, int, int, int, int, int, int,
+                                         int, int, float, cudaStream_t);
 attn_status_t launch_decode_bf16(const void*, const void*, const void*, const int32_t*,
                                  const int32_t*, int, int, int, void*, float*, float*, float*, int,
                                  int, int, int, int, int, float, cudaStream_t);
@@ -161,6 +164,39 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                                          B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0, scale, st);
   return attn_host::launch_prefill_bf16(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0,
                                         scale, 1, st);
+}
+
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B,
+                              int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                              int Hkv, int d, int causal, float scale, attn_dtype_t dtype,
+                              attn_stream_t stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 ||
+      total_q < 0 || total_k < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (total_q == 0) return ATTN_OK;  // no query rows: nothing to write
+  if (!q || !o || !cu_seqlens_q || !cu_seqlens_k || (total_k > 0 && (!k || !v)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hq > (1 << 24) || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (total_k == 0) {
+    // No sequence has keys, so every row sees none (O = 0, LSE = -inf) and
+    // no K/V tile is ever loaded; q stands in for the unread K/V buffers so
+    // that their tensor maps are still encodable.
+    k = v = q;  // Hkv <= Hq rows of q are a valid stand-in
+    total_k = 1;
+    max_seqlen_k = 1;
+  }
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  return attn_host::launch_prefill_bf16_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B,
+                                               max_seqlen_q, max_seqlen_k, total_q, total_k, Hq,
+                                               Hkv, d, causal ? 1 : 0, scale,
+                                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_decode_plan(const int32_t* seq_lens_host, int B, int Hkv, int page_size,

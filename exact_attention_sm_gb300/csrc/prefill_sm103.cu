@@ -113,8 +113,60 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
+// Row geometry.  Dense: every (batch, head) has Lq query rows and Lk keys,
+// stored head by head ([B * H, L, d]).  Packed ("10.3 FlashAttention",
+// 10.3.8, variable-length batching): sequence b owns rows cu_q[b] ..
+// cu_q[b+1]-1 of q [total_q, Hq, d] and keys cu_k[b] .. of k, v
+// [total_k, Hkv, d]; Lq and Lk are then bounds on the lengths.
+struct Geo {
+  const int* cu_q;  // nullptr: dense
+  const int* cu_k;
+  int Lq, Lk, total_q, total_k;
+};
+
+struct Seq {
+  int q_off, lq, k_off, lk;
+};
+
+// One sequence's rows; a packed entry outside its bounds is reported and the
+// sequence treated as empty (nothing is read or written for it).
+template <bool kPacked>
+__device__ __forceinline__ Seq seq_of(const Geo& g, int b, int* status) {
+  if constexpr (!kPacked) return Seq{0, g.Lq, 0, g.Lk};
+  const int q0 = g.cu_q[b], q1 = g.cu_q[b + 1], k0 = g.cu_k[b], k1 = g.cu_k[b + 1];
+  if (q0 < 0 || q1 < q0 || q1 > g.total_q || q1 - q0 > g.Lq || k0 < 0 || k1 < k0 ||
+      k1 > g.total_k || k1 - k0 > g.Lk) {
+    attn::record_status(status, ATTN_ERR_BAD_INDEX);
+    return Seq{0, 0, 0, 0};
+  }
+  return Seq{q0, q1 - q0, k0, k1 - k0};
+}
+
+// K/V tiles a 128-row Q tile reads: -1 if the tile has no rows, 0 if its rows
+// see no key.  Causal is aligned bottom-right: row r of a sequence sees keys
+// j <= r + (lk - lq) (the square rule when lq == lk); tiles past the last
+// visible key of the tile's last row are skipped.
+__device__ __forceinline__ int kv_tiles(const Seq& sq, int qt, int causal) {
+  if (qt * BM >= sq.lq) return -1;
+  if (!causal) return (sq.lk + BN - 1) / BN;
+  const int last_row = min(sq.lq, (qt + 1) * BM) - 1;
+  const int kmax = min(sq.lk - 1, last_row + sq.lk - sq.lq);
+  return kmax < 0 ? 0 : kmax / BN + 1;
+}
+
+// Last visible key of a row (grow = row within its sequence), and whether K/V
+// tile j needs the element-wise mask for any row of Q tile qt.
+__device__ __forceinline__ int row_kmax(const Seq& sq, int grow, int causal) {
+  return causal ? min(sq.lk - 1, grow + sq.lk - sq.lq) : sq.lk - 1;
+}
+__device__ __forceinline__ bool tile_needs_mask(const Seq& sq, int qt, int j, int causal) {
+  return j * BN + BN - 1 > row_kmax(sq, qt * BM, causal);
+}
+
 struct Item {
-  int bh, qt[2], n[2];  // n[1] == 0: tile B is absent
+  int bh, qt[2], n[2];  // n[x] == 0: tile x has no K/V work
+  bool zero[2];         // tile x has rows that see no key: O = 0, LSE = -inf
+  Seq sq;
 };
 
 // Work-item order and assignment.
@@ -147,8 +199,9 @@ __device__ __forceinline__ Schedule make_schedule(int num_items, int num_pairs, 
   return sc;
 }
 
-__device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int num_pairs, int num_qt,
-                                            int n_kv, int causal) {
+template <bool kPacked>
+__device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int Hq, int num_pairs,
+                                            const Geo& geo, int causal, int* status) {
   Item w;
   int pair;
   if (grouped) {
@@ -158,19 +211,23 @@ __device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int nu
     pair = num_pairs - 1 - it / BH;
     w.bh = it % BH;
   }
-  w.qt[0] = 2 * pair;
-  w.qt[1] = 2 * pair + 1;
-  w.n[0] = causal ? min(n_kv, w.qt[0] + 1) : n_kv;
-  w.n[1] = w.qt[1] < num_qt ? (causal ? min(n_kv, w.qt[1] + 1) : n_kv) : 0;
+  w.sq = seq_of<kPacked>(geo, w.bh / Hq, status);
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    w.qt[x] = 2 * pair + x;
+    const int kv = kv_tiles(w.sq, w.qt[x], causal);
+    w.n[x] = kv > 0 ? kv : 0;
+    w.zero[x] = kv == 0;
+  }
   return w;
 }
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
-                        float* __restrict__ lse, int BH, int Hq, int Hkv, int Lq, int Lk,
+                        float* __restrict__ lse, int BH, int Hq, int Hkv, const Geo geo,
                         int causal, float scale_log2, int q_div, int* status) {
   using C = Cfg<D>;
   constexpr int NS = C::NS;
@@ -194,10 +251,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_qt = (Lq + BM - 1) / BM;
+  const int num_qt = (geo.Lq + BM - 1) / BM;
   const int num_pairs = (num_qt + 1) / 2;
   const int num_items = BH * num_pairs;
-  const int n_kv = (Lk + BN - 1) / BN;
+  constexpr bool packed = kPacked;
   const int group = Hq / Hkv;
   const Schedule sched = make_schedule(num_items, num_pairs, causal);
 
@@ -243,9 +300,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int nq[2] = {0, 0};       // Q tiles issued per slot
       bool ok = true;
       for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-        const Item w = decode_item(it, sched.grouped, BH, num_pairs, num_qt, n_kv, causal);
-        const int bh_kv = (w.bh / Hq) * Hkv + (w.bh % Hq) / group;
+        const Item w = decode_item<kPacked>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
         const int nmax = max(w.n[0], w.n[1]);
+        if (nmax == 0) continue;
+        const int h = w.bh % Hq;
+        // TMA coordinates (rows, heads): dense tensors are [heads, rows],
+        // packed ones [rows, heads].
+        const int kv_c1 = packed ? h / group : 0;
+        const int kv_c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
         // K/V tile j of this item into the next ring slot.
         auto issue_kv = [&](int j) -> bool {
           const int st = g % NS;
@@ -255,10 +317,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
           mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &k_full[st], kb * 64, j * BN, bh_kv);
+            tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &k_full[st], kb * 64,
+                        packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
           mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &v_full[st], kb * 64, j * BN, bh_kv);
+            tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &v_full[st], kb * 64,
+                        packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
           ++g;
           return true;
         };
@@ -275,7 +339,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q,
-                        &q_full[x], kb * 64, w.qt[x] * BM, w.bh / q_div);
+                        &q_full[x], kb * 64, packed ? h : w.qt[x] * BM,
+                        packed ? w.sq.q_off + w.qt[x] * BM : w.bh / q_div);
           ++nq[x];
         }
         for (int j = 1; ok && j < nmax; ++j) ok = issue_kv(j);
@@ -340,8 +405,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
 
       for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-        const Item w = decode_item(it, sched.grouped, BH, num_pairs, num_qt, n_kv, causal);
+        const Item w = decode_item<kPacked>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
         const int nmax = max(w.n[0], w.n[1]);
+        if (nmax == 0) continue;
         // First QK^T of each present tile.
         if (!mbar_wait(&k_full[g % NS], (g / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
         for (int x = 0; x < 2 && ok; ++x) {
@@ -404,10 +470,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int ns = 0, nitem = 0;
     bool ok = true;
     for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-      const Item w = decode_item(it, sched.grouped, BH, num_pairs, num_qt, n_kv, causal);
+      const Item w = decode_item<kPacked>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
       const int n = w.n[x];
-      if (n == 0) continue;
       const int grow = w.qt[x] * BM + row;
+      const int h = w.bh % Hq;
+      // Output row: dense [heads, rows], packed [rows, heads].
+      const size_t orow_index = packed ? static_cast<size_t>(w.sq.q_off + grow) * Hq + h
+                                       : static_cast<size_t>(w.bh) * geo.Lq + grow;
+      if (n == 0) {
+        if constexpr (kPacked) {
+          if (w.zero[x] && grow < w.sq.lq) {  // rows that see no key
+            uint4* op = reinterpret_cast<uint4*>(o + orow_index * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) op[c] = make_uint4(0u, 0u, 0u, 0u);
+            if (lse != nullptr) lse[orow_index] = -INFINITY;
+          }
+        }
+        continue;
+      }
       float m_s = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         ok = __all_sync(FULL, mbar_wait(&s_full[x], ns & 1, abort_flag, kWaitLimitNs));
@@ -420,9 +500,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld_wait();
         float* s = reinterpret_cast<float*>(&sr[0][0]);
 
-        const bool need_mask = (j == n - 1) && (causal || (Lk % BN) != 0);
+        const bool need_mask = kPacked ? tile_needs_mask(w.sq, w.qt[x], j, causal)
+                                       : (j == n - 1) && (causal || (geo.Lk % BN) != 0);
         if (need_mask) {
-          const int kmax = causal ? min(Lk - 1, grow) : Lk - 1;  // last visible key
+          const int kmax = row_kmax(w.sq, grow, causal);  // last visible key
 #pragma unroll
           for (int c = 0; c < BN; ++c)
             if (j * BN + c > kmax) s[c] = -INFINITY;
@@ -447,8 +528,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // into 4 independent row-sum chains; P goes to TMEM in 16-column
         // chunks (8 bf16x2 words) over S's own columns as soon as a chunk is
         // packed, which keeps few registers live next to S.
+        // A row that sees no key yet (every score -inf, possible when causal
+        // is aligned bottom-right with lq > lk) keeps m = -inf: subtract 0
+        // instead so that its p are exp(-inf) = 0, not NaN.
+        const float m_sub = kPacked && m_s == -INFINITY ? 0.f : m_s;
         const float2 sc2 = make_float2(scale_log2, scale_log2);
-        const float2 nm2 = make_float2(-m_s, -m_s);
+        const float2 nm2 = make_float2(-m_sub, -m_sub);
         float2 rs[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
@@ -489,8 +574,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool live = grow < Lq;
-      __nv_bfloat16* orow = o + (static_cast<size_t>(w.bh) * Lq + (live ? grow : 0)) * D;
+      const bool live = grow < w.sq.lq;
+      __nv_bfloat16* orow = o + (live ? orow_index : 0) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -509,7 +594,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (live && lse != nullptr)
-        lse[static_cast<size_t>(w.bh) * Lq + grow] =
+        lse[orow_index] =
             l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&o_free[x]);
@@ -566,11 +651,14 @@ struct Cfg64 {
 };
 
 struct Item1 {
-  int bh, qt, n;
+  int bh, qt, n;  // n == 0: no K/V work
+  bool zero;      // rows that see no key: O = 0, LSE = -inf
+  Seq sq;
 };
 
-__device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int num_qt, int n_kv,
-                                              int causal) {
+template <bool kPacked>
+__device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int Hq, int num_qt,
+                                              const Geo& geo, int causal, int* status) {
   Item1 w;
   if (grouped) {
     w.bh = it / num_qt;
@@ -579,16 +667,20 @@ __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int 
     w.qt = num_qt - 1 - it / BH;
     w.bh = it % BH;
   }
-  w.n = causal ? min(n_kv, w.qt + 1) : n_kv;
+  w.sq = seq_of<kPacked>(geo, w.bh / Hq, status);
+  const int kv = kv_tiles(w.sq, w.qt, causal);
+  w.n = kv > 0 ? kv : 0;
+  w.zero = kv == 0;
   return w;
 }
 
+template <bool kPacked>
 __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     prefill_bf16_d64_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
                             __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int BH, int Hq,
-                            int Hkv, int Lq, int Lk, int causal, float scale_log2, int q_div,
+                            int Hkv, const Geo geo, int causal, float scale_log2, int q_div,
                             int* status) {
   using C = Cfg64;
   constexpr int D = C::D, NS = C::NS, NQ = C::NQ;
@@ -614,9 +706,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_qt = (Lq + BM - 1) / BM;
+  const int num_qt = (geo.Lq + BM - 1) / BM;
   const int num_items = BH * num_qt;
-  const int n_kv = (Lk + BN - 1) / BN;
+  constexpr bool packed = kPacked;
   const int group = Hq / Hkv;
   // Short rows (or no mask): each CTA takes a contiguous run of items, head
   // by head, so a head's K/V is re-read from L2.  Long causal rows: items
@@ -632,7 +724,18 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     sched.last = num_items;
     sched.step = gridDim.x;
   }
-  auto item_at = [&](int it) { return decode_item1(it, sched.grouped, BH, num_qt, n_kv, causal); };
+  auto item_at = [&](int it) {
+    return decode_item1<kPacked>(it, sched.grouped, BH, Hq, num_qt, geo, causal, status);
+  };
+  // The first item at or after `it` (in this CTA's order) with K/V work;
+  // items without any (no rows, or rows that see no key) only make the
+  // softmax warps write their rows.
+  auto next_active = [&](int it) {
+    if constexpr (kPacked) {
+      while (it < sched.last && item_at(it).n == 0) it += sched.step;
+    }
+    return it;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NQ; ++i) {
@@ -680,27 +783,27 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       struct Cur {
-        int it, j, n, bh_kv;
+        int it, j, n, c1, c2;  // tile j of n; TMA coordinates (rows, heads) of tile 0
       };
-      auto start = [&](Cur& c) {
-        c.it = sched.first;
+      auto enter = [&](Cur& c) {
         c.j = 0;
         c.n = 0;
         if (c.it < sched.last) {
           const Item1 w = item_at(c.it);
+          const int h = w.bh % Hq;
           c.n = w.n;
-          c.bh_kv = (w.bh / Hq) * Hkv + (w.bh % Hq) / group;
+          c.c1 = packed ? h / group : 0;
+          c.c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
         }
+      };
+      auto start = [&](Cur& c) {
+        c.it = next_active(sched.first);
+        enter(c);
       };
       auto next = [&](Cur& c) {
         if (++c.j < c.n) return;
-        c.j = 0;
-        c.it += sched.step;
-        if (c.it < sched.last) {
-          const Item1 w = item_at(c.it);
-          c.n = w.n;
-          c.bh_kv = (w.bh / Hq) * Hkv + (w.bh % Hq) / group;
-        }
+        c.it = next_active(c.it + sched.step);
+        enter(c);
       };
       Cur ck, cv;
       start(ck);
@@ -711,7 +814,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         const int st = tk % NS;
         if (tk >= NS && !wait(&k_done[st], (tk / NS) + 1)) return false;
         mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
-        tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k, &k_full[st], 0, ck.j * BN, ck.bh_kv);
+        tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k, &k_full[st], 0,
+                    packed ? ck.c1 : ck.j * BN, packed ? ck.c2 + ck.j * BN : ck.c2);
         ++tk;
         next(ck);
         return true;
@@ -720,7 +824,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         const int st = tv % NS;
         if (tv >= NS && !wait(&pv_done[st], (tv / NS) + 1)) return false;
         mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
-        tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v, &v_full[st], 0, cv.j * BN, cv.bh_kv);
+        tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v, &v_full[st], 0,
+                    packed ? cv.c1 : cv.j * BN, packed ? cv.c2 + cv.j * BN : cv.c2);
         ++tv;
         next(cv);
         return true;
@@ -748,7 +853,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       prefetch_tmap(&tm_q);
       int nq = 0;
       bool ok = true;
-      for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+      for (int it = next_active(sched.first); ok && it < sched.last;
+           it = next_active(it + sched.step)) {
         const Item1 w = item_at(it);
         const int qs = nq % NQ;
         if (nq >= NQ && !wait(&q_empty[qs], (nq / NQ) - 1)) {
@@ -756,8 +862,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           break;
         }
         mbar_arrive_expect_tx(&q_full[qs], C::TILE_BYTES);
-        tma_load_3d(smem + C::OFF_Q + qs * C::TILE_BYTES, &tm_q, &q_full[qs], 0, w.qt * BM,
-                    w.bh / q_div);
+        tma_load_3d(smem + C::OFF_Q + qs * C::TILE_BYTES, &tm_q, &q_full[qs], 0,
+                    packed ? w.bh % Hq : w.qt * BM,
+                    packed ? w.sq.q_off + w.qt * BM : w.bh / q_div);
         ++nq;
       }
       if (!ok) {
@@ -817,16 +924,18 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         }
       };
       int t = 0;  // global step of the current item's K/V tile 0
-      if (sched.first < sched.last) {
-        const Item1 w0 = item_at(sched.first);
+      const int it0 = next_active(sched.first);
+      if (it0 < sched.last) {
+        const Item1 w0 = item_at(it0);
         ok = wait(&qk_ready[0], 0) && wait(&q_full[0], 0);
         if (ok) {
           tc_fence_after();
           qk(0, w0.n, 0);
         }
       }
-      for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+      for (int it = it0; ok && it < sched.last;) {
         const Item1 w = item_at(it);
+        const int it2 = next_active(it + sched.step);
         for (int j = 0; ok && j < w.n; ++j) {
           const int tt = t + j;
           // S for step tt + 1: the next K/V tile of this item or the first
@@ -835,8 +944,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
             if (!wait(&qk_ready[(tt + 1) % NS], (tt + 1) / NS)) { ok = false; break; }
             tc_fence_after();
             qk(j + 1, w.n, tt + 1);
-          } else if (it + sched.step < sched.last) {
-            const Item1 w2 = item_at(it + sched.step);
+          } else if (it2 < sched.last) {
+            const Item1 w2 = item_at(it2);
             if (!wait(&qk_ready[(tt + 1) % NS], (tt + 1) / NS) ||
                 !wait(&q_full[nq % NQ], nq / NQ)) {
               ok = false;
@@ -862,6 +971,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           if (j + 1 == w.n) mma_commit(o_done);
         }
         t += w.n;
+        it = it2;
       }
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
@@ -890,6 +1000,21 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       const Item1 w = item_at(it);
       const int n = w.n;
       const int grow = w.qt * BM + row;
+      const int h = w.bh % Hq;
+      // Output row: dense [heads, rows], packed [rows, heads].
+      const size_t orow_index = packed ? static_cast<size_t>(w.sq.q_off + grow) * Hq + h
+                                       : static_cast<size_t>(w.bh) * geo.Lq + grow;
+      if (n == 0) {
+        if constexpr (kPacked) {
+          if (w.zero && grow < w.sq.lq) {  // rows that see no key
+            uint4* op = reinterpret_cast<uint4*>(o + orow_index * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) op[c] = make_uint4(0u, 0u, 0u, 0u);
+            if (lse != nullptr) lse[orow_index] = -INFINITY;
+          }
+        }
+        continue;
+      }
       float m_s = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         const int tt = t + j;
@@ -906,9 +1031,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(&qk_ready[(tt + 1) % NS]);
 
-        const bool need_mask = (j == n - 1) && (causal || (Lk % BN) != 0);
+        const bool need_mask = kPacked ? tile_needs_mask(w.sq, w.qt, j, causal)
+                                       : (j == n - 1) && (causal || (geo.Lk % BN) != 0);
         if (need_mask) {
-          const int kmax = causal ? min(Lk - 1, grow) : Lk - 1;  // last visible key
+          const int kmax = row_kmax(w.sq, grow, causal);  // last visible key
 #pragma unroll
           for (int c = 0; c < BN; ++c)
             if (j * BN + c > kmax) s[c] = -INFINITY;
@@ -928,8 +1054,12 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           alpha = ex2(m_s - mt_s);  // 0 on the first tile (m_s = -inf)
           m_s = mt_s;
         }
+        // A row that sees no key yet (every score -inf, possible when causal
+        // is aligned bottom-right with lq > lk) keeps m = -inf: subtract 0
+        // instead so that its p are exp(-inf) = 0, not NaN.
+        const float m_sub = kPacked && m_s == -INFINITY ? 0.f : m_s;
         const float2 sc2 = make_float2(scale_log2, scale_log2);
-        const float2 nm2 = make_float2(-m_s, -m_s);
+        const float2 nm2 = make_float2(-m_sub, -m_sub);
         float2 rs[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
@@ -981,8 +1111,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       tc_fence_before();
       mbar_arrive(o_free);
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (grow < Lq) {
-        __nv_bfloat16* orow = o + (static_cast<size_t>(w.bh) * Lq + grow) * D;
+      if (grow < w.sq.lq) {
+        __nv_bfloat16* orow = o + orow_index * D;
 #pragma unroll
         for (int v8 = 0; v8 < 8; ++v8) {
           const uint32_t* rv = &r[v8 >> 2][(v8 & 3) * 8];
@@ -994,8 +1124,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           *reinterpret_cast<uint4*>(orow + v8 * 8) = q4;
         }
         if (lse != nullptr)
-          lse[static_cast<size_t>(w.bh) * Lq + grow] =
-              l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
+          lse[orow_index] = l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
       }
       ++nitem;
       t += n;
@@ -1033,6 +1162,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Packed rows: [total rows, H heads] x d bf16 viewed as {d, H, total}; box
+// {64, 1, 128} (128 rows of one head, the same shared-memory tile as the
+// dense box).  Rows past total read as zeros.
+bool make_map_packed(CUtensorMap* m, const void* base, int D, int H, int total) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(total)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(H) * D * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [BH heads, L rows] x d bf16 viewed as a 3-D tensor {d, L, BH}; box
 // {64, 128, 1} with 128-byte swizzle.  Rows past L read as zeros.
 bool make_map(CUtensorMap* m, const void* base, int D, int L, int BH) {
@@ -1049,9 +1195,9 @@ bool make_map(CUtensorMap* m, const void* base, int D, int L, int BH) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kPacked>
 attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                     int Hkv, int Lq, int Lk, int causal, float scale, int q_div,
+                     int Hkv, const Geo& geo, int causal, float scale, int q_div,
                      cudaStream_t stream) {
   // d = 64 runs the two-CTAs-per-SM kernel on single Q tiles, d = 128 the
   // Q-tile-pair ping-pong kernel.
@@ -1061,9 +1207,9 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   if (!attr_set) {
     const void* fn;
     if constexpr (kD64)
-      fn = reinterpret_cast<const void*>(prefill_bf16_d64_kernel);
+      fn = reinterpret_cast<const void*>(prefill_bf16_d64_kernel<kPacked>);
     else
-      fn = reinterpret_cast<const void*>(prefill_bf16_kernel<D>);
+      fn = reinterpret_cast<const void*>(prefill_bf16_kernel<D, kPacked>);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
             cudaSuccess ||
         cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
@@ -1073,10 +1219,14 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   }
   CUtensorMap mq, mk, mv;
   if (q_div < 1 || (B * Hq) % q_div != 0) return ATTN_ERR_INVALID_ARG;
-  if (!make_map(&mq, q, D, Lq, B * Hq / q_div) || !make_map(&mk, k, D, Lk, B * Hkv) ||
-      !make_map(&mv, v, D, Lk, B * Hkv))
-    return ATTN_ERR_CUDA;
-  const int num_qt = (Lq + BM - 1) / BM;
+  const bool maps_ok =
+      kPacked
+          ? make_map_packed(&mq, q, D, Hq, geo.total_q) && make_map_packed(&mk, k, D, Hkv, geo.total_k) &&
+                make_map_packed(&mv, v, D, Hkv, geo.total_k)
+          : make_map(&mq, q, D, geo.Lq, B * Hq / q_div) && make_map(&mk, k, D, geo.Lk, B * Hkv) &&
+                make_map(&mv, v, D, geo.Lk, B * Hkv);
+  if (!maps_ok) return ATTN_ERR_CUDA;
+  const int num_qt = (geo.Lq + BM - 1) / BM;
   const long long items = static_cast<long long>(B) * Hq * (kD64 ? num_qt : (num_qt + 1) / 2);
   if (items > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
   const int sms = attn_host::num_sms();
@@ -1085,12 +1235,12 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   const int grid = static_cast<int>(items < slots ? items : slots);
   const float scale_log2 = scale * attn::kLog2e;
   if constexpr (kD64) {
-    prefill_bf16_d64_kernel<<<grid, Cfg64::THREADS, smem_bytes, stream>>>(
-        mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, Lq, Lk, causal,
+    prefill_bf16_d64_kernel<kPacked><<<grid, Cfg64::THREADS, smem_bytes, stream>>>(
+        mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, geo, causal,
         scale_log2, q_div, attn_host::device_status_ptr());
   } else {
-    prefill_bf16_kernel<D><<<grid, NUM_THREADS, smem_bytes, stream>>>(
-        mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, Lq, Lk, causal,
+    prefill_bf16_kernel<D, kPacked><<<grid, NUM_THREADS, smem_bytes, stream>>>(
+        mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, geo, causal,
         scale_log2, q_div, attn_host::device_status_ptr());
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -1103,8 +1253,21 @@ namespace attn_host {
 attn_status_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                                   float scale, int q_div, cudaStream_t stream) {
-  if (d == 64) return launch<64>(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, causal, scale, q_div, stream);
-  if (d == 128) return launch<128>(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, causal, scale, q_div, stream);
+  const Geo geo{nullptr, nullptr, Lq, Lk, 0, 0};
+  if (d == 64) return launch<64, false>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
+  if (d == 128)
+    return launch<128, false>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+attn_status_t launch_prefill_bf16_varlen(const void* q, const void* k, const void* v, void* o,
+                                         float* lse, const int* cu_q, const int* cu_k, int B,
+                                         int max_q, int max_k, int total_q, int total_k, int Hq,
+                                         int Hkv, int d, int causal, float scale,
+                                         cudaStream_t stream) {
+  const Geo geo{cu_q, cu_k, max_q, max_k, total_q, total_k};
+  if (d == 64) return launch<64, true>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, 1, stream);
+  if (d == 128) return launch<128, true>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, 1, stream);
   return ATTN_ERR_UNSUPPORTED;
 }
 

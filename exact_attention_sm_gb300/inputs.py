@@ -114,3 +114,17 @@ def cascade_inputs(prefix_len, suffix_lens, Hq, Hkv, d, seed=0, device="cpu"):
     pv = torch.randn(Hkv, prefix_len, d, generator=g, device=device).to(torch.bfloat16)
     return q, pk, pv, kp, vp, table, sl
 
+
+
+def varlen_inputs(lens_q, lens_k, Hq, Hkv, d, seed=0, device="cpu"):
+    """Packed (variable-length) prefill inputs: q [sum lens_q, Hq, d], k and v
+    [sum lens_k, Hkv, d], bf16 ~ N(0,1) drawn in the order q, k, v, plus the
+    int32 cumulative lengths cu_seqlens_q / cu_seqlens_k [B + 1]."""
+    g = _gen(seed, device)
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    q = torch.randn(max(tq, 1), Hq, d, generator=g, device=device)[:tq].to(torch.bfloat16)
+    k = torch.randn(max(tk, 1), Hkv, d, generator=g, device=device)[:tk].to(torch.bfloat16)
+    v = torch.randn(max(tk, 1), Hkv, d, generator=g, device=device)[:tk].to(torch.bfloat16)
+    cu = lambda lens: torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()),
+                                   dtype=torch.int32, device=device)
+    return q.contiguous(), k.contiguous(), v.contiguous(), cu(lens_q), cu(lens_k)

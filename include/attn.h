@@ -200,6 +200,40 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_pages, cons
                                         float scale, attn_dtype_t dtype, attn_stream_t stream);
 
 /*
+ * attn_fwd_varlen - prefill over sequences packed end to end ("10.3
+ * FlashAttention", 10.3.8 variable-length batching).
+ *
+ *   q  [total_q, Hq, d]  k, v [total_k, Hkv, d]  bf16, row-major, 16-byte
+ *   aligned; o [total_q, Hq, d] bf16; lse [total_q, Hq] fp32 or NULL.
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B + 1], cumulative lengths
+ *   (lengths 3, 5, 2 -> [0, 3, 8, 10]); sequence b owns q rows
+ *   cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and k/v rows cu_seqlens_k[b] ..,
+ *   and sees nothing of the other sequences.  max_seqlen_q / max_seqlen_k
+ *   bound every length (they size the work list); total_q / total_k are the
+ *   row counts of q and k.  GQA: query head h reads KV head h / (Hq / Hkv).
+ *
+ * Causal is aligned bottom-right (the pages define only the square case):
+ * query i of a sequence with Lq queries and Lk keys sees key j <= i + Lk - Lq,
+ * i.e. the queries are the last Lq tokens of the sequence (chunked prefill).
+ * Rows that see no key (Lq > Lk) get O = 0, LSE = -inf.  Lengths may be 0;
+ * total_q = 0 returns ATTN_OK without any launch (every pointer may be
+ * NULL), and total_k = 0 (k, v may be NULL) gives every row O = 0,
+ * LSE = -inf.
+ *
+ * d in {64, 128}, bf16 only.  Errors: ATTN_ERR_INVALID_ARG for NULLs, bad
+ * sizes or misalignment; ATTN_ERR_UNSUPPORTED for other d or dtypes.  A
+ * cu_seqlens entry that breaks its bounds (decreasing, past total, longer
+ * than max_seqlen) is reported as ATTN_ERR_BAD_INDEX in the device status
+ * word and that sequence is left unwritten; nothing outside the tensors is
+ * touched.
+ */
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B,
+                              int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq,
+                              int Hkv, int d, int causal, float scale, attn_dtype_t dtype,
+                              attn_stream_t stream);
+
+/*
  * Cascade (shared-prefix) decode ([Lecture 4] 4.4 "cascade attention" and
  * 5.3 "composable formats").  B requests share one prefix of prefix_len
  * tokens, stored once as prefix_k / prefix_v [Hkv, prefix_len, d] bf16

@@ -176,3 +176,35 @@ def test_cascade_plan(B, Hq, Hkv, P, slots):
     r = lambda x: -(-x // 256) * 256
     want = r(rows * 128 * 2) + r(rows * pc * 128 * 2) + r(rows * pc * 4) + r(rows * ss * 128 * 4) + r(rows * ss * 4)
     assert ea.attn_cascade_workspace_bytes(B, Hq, 128, pc, ss) == want
+
+
+def varlen(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cq=FAKE, ck=FAKE, B=3, mq=5, mk=5, tq=10,
+                tk=10, Hq=4, Hkv=2, d=64, causal=1, scale=0.125, dtype=ea.ATTN_BF16)
+    args.update(kw)
+    a = args
+    return ea.lib().attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"],
+                                    a["B"], a["mq"], a["mk"], a["tq"], a["tk"], a["Hq"], a["Hkv"],
+                                    a["d"], a["causal"], a["scale"], a["dtype"], None)
+
+
+def test_varlen_rejects_on_host():
+    assert varlen(q=None) == 1
+    assert varlen(o=None) == 1
+    assert varlen(cq=None) == 1
+    assert varlen(k=None) == 1                # keys present but no k
+    assert varlen(B=0) == 1
+    assert varlen(Hkv=3) == 1
+    assert varlen(mq=0) == 1
+    assert varlen(tq=-1) == 1
+    assert varlen(scale=0.0) == 1
+    assert varlen(scale=float("nan")) == 1
+    assert varlen(q=MISALIGNED) == 1
+    assert varlen(cq=ctypes.c_void_p(0x10002)) == 1   # cu_seqlens must be 4-byte aligned
+    assert varlen(d=96) == 2
+    assert varlen(dtype=ea.ATTN_F32) == 2
+
+
+def test_varlen_without_queries_is_a_no_op():
+    """total_q = 0 (every sequence empty) succeeds without a launch, NULLs allowed."""
+    assert varlen(q=None, k=None, v=None, o=None, cq=None, ck=None, tq=0, tk=0) == 0
