@@ -656,9 +656,17 @@ struct Item1 {
   Seq sq;
 };
 
+// The last sequence a thread looked up: consecutive items mostly belong to
+// the same sequence, so its cu_seqlens entries are read from memory once.
+struct SeqCache {
+  int b = -1;
+  Seq sq;
+};
+
 template <bool kPacked>
 __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int Hq, int num_qt,
-                                              const Geo& geo, int causal, int* status) {
+                                              const Geo& geo, int causal, int* status,
+                                              SeqCache& cache) {
   Item1 w;
   if (grouped) {
     w.bh = it / num_qt;
@@ -667,7 +675,16 @@ __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int 
     w.qt = num_qt - 1 - it / BH;
     w.bh = it % BH;
   }
-  w.sq = seq_of<kPacked>(geo, w.bh / Hq, status);
+  if constexpr (kPacked) {
+    const int b = w.bh / Hq;
+    if (b != cache.b) {
+      cache.sq = seq_of<true>(geo, b, status);
+      cache.b = b;
+    }
+    w.sq = cache.sq;
+  } else {
+    w.sq = seq_of<false>(geo, w.bh / Hq, status);
+  }
   const int kv = kv_tiles(w.sq, w.qt, causal);
   w.n = kv > 0 ? kv : 0;
   w.zero = kv == 0;
@@ -724,15 +741,19 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     sched.last = num_items;
     sched.step = gridDim.x;
   }
+  SeqCache seq_cache;
   auto item_at = [&](int it) {
-    return decode_item1<kPacked>(it, sched.grouped, BH, Hq, num_qt, geo, causal, status);
+    return decode_item1<kPacked>(it, sched.grouped, BH, Hq, num_qt, geo, causal, status,
+                                 seq_cache);
   };
-  // The first item at or after `it` (in this CTA's order) with K/V work;
-  // items without any (no rows, or rows that see no key) only make the
-  // softmax warps write their rows.
-  auto next_active = [&](int it) {
-    if constexpr (kPacked) {
-      while (it < sched.last && item_at(it).n == 0) it += sched.step;
+  // The first item at or after `it` (in this CTA's order) with K/V work,
+  // described in w (set only when the result is < sched.last).  Items
+  // without any (no rows, or rows that see no key; packed layout only) just
+  // make the softmax warps write their rows.  Each role decodes an item once.
+  auto next_active = [&](int it, Item1& w) {
+    for (; it < sched.last; it += sched.step) {
+      w = item_at(it);
+      if (!kPacked || w.n > 0) break;
     }
     return it;
   };
@@ -785,29 +806,25 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       struct Cur {
         int it, j, n, c1, c2;  // tile j of n; TMA coordinates (rows, heads) of tile 0
       };
-      auto enter = [&](Cur& c) {
+      auto enter = [&](Cur& c, int it) {
+        Item1 w;
+        c.it = next_active(it, w);
         c.j = 0;
         c.n = 0;
         if (c.it < sched.last) {
-          const Item1 w = item_at(c.it);
           const int h = w.bh % Hq;
           c.n = w.n;
           c.c1 = packed ? h / group : 0;
           c.c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
         }
       };
-      auto start = [&](Cur& c) {
-        c.it = next_active(sched.first);
-        enter(c);
-      };
       auto next = [&](Cur& c) {
         if (++c.j < c.n) return;
-        c.it = next_active(c.it + sched.step);
-        enter(c);
+        enter(c, c.it + sched.step);
       };
       Cur ck, cv;
-      start(ck);
-      start(cv);
+      enter(ck, sched.first);
+      enter(cv, sched.first);
       int tk = 0, tv = 0;  // K / V tiles issued
       bool ok = true;
       auto load_k = [&]() -> bool {
@@ -853,9 +870,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       prefetch_tmap(&tm_q);
       int nq = 0;
       bool ok = true;
-      for (int it = next_active(sched.first); ok && it < sched.last;
-           it = next_active(it + sched.step)) {
-        const Item1 w = item_at(it);
+      Item1 w;
+      for (int it = next_active(sched.first, w); ok && it < sched.last;
+           it = next_active(it + sched.step, w)) {
         const int qs = nq % NQ;
         if (nq >= NQ && !wait(&q_empty[qs], (nq / NQ) - 1)) {
           ok = false;
@@ -924,18 +941,17 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         }
       };
       int t = 0;  // global step of the current item's K/V tile 0
-      const int it0 = next_active(sched.first);
-      if (it0 < sched.last) {
-        const Item1 w0 = item_at(it0);
+      Item1 w, w2{};
+      int it = next_active(sched.first, w);
+      if (it < sched.last) {
         ok = wait(&qk_ready[0], 0) && wait(&q_full[0], 0);
         if (ok) {
           tc_fence_after();
-          qk(0, w0.n, 0);
+          qk(0, w.n, 0);
         }
       }
-      for (int it = it0; ok && it < sched.last;) {
-        const Item1 w = item_at(it);
-        const int it2 = next_active(it + sched.step);
+      while (ok && it < sched.last) {
+        const int it2 = next_active(it + sched.step, w2);
         for (int j = 0; ok && j < w.n; ++j) {
           const int tt = t + j;
           // S for step tt + 1: the next K/V tile of this item or the first
@@ -945,7 +961,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
             tc_fence_after();
             qk(j + 1, w.n, tt + 1);
           } else if (it2 < sched.last) {
-            const Item1 w2 = item_at(it2);
             if (!wait(&qk_ready[(tt + 1) % NS], (tt + 1) / NS) ||
                 !wait(&q_full[nq % NQ], nq / NQ)) {
               ok = false;
@@ -972,6 +987,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         }
         t += w.n;
         it = it2;
+        w = w2;
       }
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
