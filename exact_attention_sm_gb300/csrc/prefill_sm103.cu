@@ -170,9 +170,10 @@ struct Item {
 };
 
 // Work-item order and assignment.
-//  * Long causal rows (more than kGroupedMaxPairs pairs per head): items are
-//    listed heaviest pair first across all heads and dealt round-robin to the
-//    persistent CTAs, which keeps them balanced.
+//  * Long causal rows (more than kGroupedMaxPairs pairs per head) and every
+//    packed (variable-length) batch: items are listed heaviest pair first
+//    across all heads and dealt round-robin to the persistent CTAs, which
+//    keeps them balanced when the work per item varies.
 //  * Short rows or non-causal: items are listed head by head and every CTA
 //    takes one contiguous run of them, so the pairs of a head run back to back
 //    on the same SM and re-read that head's K/V from L2; each run spans whole
@@ -184,9 +185,10 @@ struct Schedule {
   int first, last, step;  // items first, first+step, ... < last
 };
 
-__device__ __forceinline__ Schedule make_schedule(int num_items, int num_pairs, int causal) {
+__device__ __forceinline__ Schedule make_schedule(int num_items, int num_pairs, int causal,
+                                                  bool packed) {
   Schedule sc;
-  sc.grouped = !causal || num_pairs <= kGroupedMaxPairs;
+  sc.grouped = !packed && (!causal || num_pairs <= kGroupedMaxPairs);
   if (sc.grouped) {
     sc.first = static_cast<int>(static_cast<long long>(num_items) * blockIdx.x / gridDim.x);
     sc.last = static_cast<int>(static_cast<long long>(num_items) * (blockIdx.x + 1) / gridDim.x);
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_items = BH * num_pairs;
   constexpr bool packed = kPacked;
   const int group = Hq / Hkv;
-  const Schedule sched = make_schedule(num_items, num_pairs, causal);
+  const Schedule sched = make_schedule(num_items, num_pairs, causal, kPacked);
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -727,11 +729,13 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   const int num_items = BH * num_qt;
   constexpr bool packed = kPacked;
   const int group = Hq / Hkv;
-  // Short rows (or no mask): each CTA takes a contiguous run of items, head
-  // by head, so a head's K/V is re-read from L2.  Long causal rows: items
-  // heaviest first, dealt round-robin.
+  // Dense short rows (or no mask): each CTA takes a contiguous run of items,
+  // head by head, so a head's K/V is re-read from L2.  Long causal rows and
+  // every packed batch: items heaviest first (Q tile index descending over
+  // all heads), dealt round-robin, which balances the CTAs when the work per
+  // item varies (causal, or sequences of mixed lengths).
   Schedule sched;
-  sched.grouped = !causal || num_qt <= 2 * kGroupedMaxPairs;
+  sched.grouped = !kPacked && (!causal || num_qt <= 2 * kGroupedMaxPairs);
   if (sched.grouped) {
     sched.first = static_cast<int>(static_cast<long long>(num_items) * blockIdx.x / gridDim.x);
     sched.last = static_cast<int>(static_cast<long long>(num_items) * (blockIdx.x + 1) / gridDim.x);
