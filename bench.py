@@ -51,6 +51,12 @@ WORKLOADS = {
                                   dtype="bf16"),
     "decode-b256-ctx1024": dict(kind="decode", B=256, Hq=32, Hkv=8, d=128, lens="1024x256"),
     "decode-b4-long-splitkv": dict(kind="decode", B=4, Hq=32, Hkv=8, d=128, lens="uniform"),
+    # LLM book 10.3.8: sequences of mixed lengths packed end to end
+    # (cu_seqlens), lengths uniform in [1, max_len] with seed 3.
+    "prefill-varlen-gpt2-mixed": dict(kind="varlen", B=64, Hq=16, Hkv=16, max_len=2048, d=64,
+                                      causal=True, dtype="bf16"),
+    "prefill-varlen-llama-mixed": dict(kind="varlen", B=32, Hq=32, Hkv=8, max_len=4096, d=128,
+                                       causal=True, dtype="bf16"),
     # Lecture 4, section 4.4 demo 4: a 4096-token prefix shared by 64 requests,
     # 256 unique tokens each.
     "decode-cascade-b64-prefix4096": dict(kind="cascade", B=64, Hq=32, Hkv=8, d=128, prefix=4096,
@@ -64,6 +70,9 @@ def describe(name):
     if w["kind"] == "prefill":
         return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} L={w['L']} d={w['d']} "
                 f"{'causal' if w['causal'] else 'non-causal'} {w['dtype']} + LSE")
+    if w["kind"] == "varlen":
+        return (f"{name}: {w['B']} packed sequences, lengths U[1,{w['max_len']}] seed 3, "
+                f"Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} causal (bottom-right) bf16 + LSE")
     if w["kind"] == "cascade":
         return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, shared prefix "
                 f"{w['prefix']} + {w['suffix']} unique tokens per request (16-token shuffled pages)")
@@ -86,6 +95,16 @@ def prefill_flops(w, rows=None):
         per_head = L * L * (0.5 if w["causal"] else 1.0)
         return 4.0 * d * w["B"] * w["Hq"] * per_head
     return float(sum(4.0 * d * ((i + 1) if w["causal"] else L) for (_, _, i) in rows))
+
+
+def varlen_lens(w):
+    from exact_attention_sm_gb300 import inputs
+    return inputs.decode_lengths_uniform(w["B"], 1, w["max_len"], seed=3)
+
+
+def varlen_flops(w, lens):
+    """prefill_flops summed over the packed sequences (L_b^2 / 2 pairs each)."""
+    return float(sum(4.0 * w["d"] * w["Hq"] * L * L * 0.5 for L in lens))
 
 
 def decode_bytes(w, lens):
@@ -231,6 +250,17 @@ def make_step(name, torch, ea, inputs):
         return step, 1, prefill_flops(w), "flops", None
     if w["kind"] == "cascade":
         return make_cascade_step(w, torch, ea, inputs)
+    if w["kind"] == "varlen":
+        lens = varlen_lens(w)
+        q, k, v, cq, ck = inputs.varlen_inputs(lens, lens, w["Hq"], w["Hkv"], w["d"], seed=0,
+                                               device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[0], w["Hq"], dtype=torch.float32, device="cuda")
+        mx = max(lens)
+
+        def step():
+            ea.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True, out=o, lse=lse)
+        return step, 1, varlen_flops(w, lens), "flops", None
     lens = decode_lens(w)
     q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0,
                                                 device="cuda")

@@ -8,7 +8,6 @@
 #include <cstdint>
 #include <functional>
 #include <mutex>
-#include <queue>
 #include <vector>
 
 #include "attn.h"
@@ -26,7 +25,7 @@ attn_status_t launch_prefill_bf16_varlen(const void*, const void*, const void*, 
                                          int, int, float, cudaStream_t);
 attn_status_t launch_decode_bf16(const void*, const void*, const void*, const int32_t*,
                                  const int32_t*, int, int, int, void*, float*, float*, float*, int,
-                                 int, int, int, int, int, float, cudaStream_t);
+                                 int, int, int, int, int, float, const int32_t*, cudaStream_t);
 attn_status_t launch_merge(const float*, const float*, int, int, int, void*, float*, attn_dtype_t,
                            cudaStream_t);
 attn_status_t launch_cascade_gather_q(const void*, void*, int, int, int, int, cudaStream_t);
@@ -42,56 +41,35 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Time of a split plan in the lecture's simple model ("Lecture 4", sections
-// 0.5 and 4.2): a non-empty unit (request, KV head, segment) costs its token
-// count plus kUnitOverheadTokens (launching it and merging its partial
-// state) and `slots` workers take the units in launch order (segment
-// fastest, then KV head, then request), each as soon as it is free.  Returns
-// when the last worker finishes.
-constexpr int64_t kUnitOverheadTokens = 512;
-
-int64_t plan_makespan(const int32_t* lens, int B, int Hkv, int slots, int64_t chunk) {
-  int64_t smax = 1;
-  for (int b = 0; b < B; ++b) smax = std::max<int64_t>(smax, cdiv(lens[b], chunk));
-  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> free_at;
-  for (int i = 0; i < slots; ++i) free_at.push(0);
-  for (int b = 0; b < B; ++b)
-    for (int k = 0; k < Hkv; ++k)
-      for (int64_t s = 0; s < smax; ++s) {
-        const int64_t tokens = std::max<int64_t>(0, std::min<int64_t>(lens[b], (s + 1) * chunk) - s * chunk);
-        if (tokens == 0) break;  // this and the later segments of the request are empty (cost 0)
-        const int64_t t = free_at.top();
-        free_at.pop();
-        free_at.push(t + tokens + kUnitOverheadTokens);
-      }
-  int64_t last = 0;
-  while (!free_at.empty()) {
-    last = std::max(last, free_at.top());
-    free_at.pop();
-  }
-  return last;
+// Non-empty work units (request, KV head, segment) for chunk length C.
+int64_t plan_units(const int32_t* lens, int B, int Hkv, int64_t chunk) {
+  int64_t n = 0;
+  for (int b = 0; b < B; ++b) n += cdiv(std::max<int32_t>(lens[b], 0), chunk);
+  return n * Hkv;
 }
 
-// Split planner ("Lecture 4" sections 4.2 / 5.6 and exercise 6; the reading
-// is spelled out in attn.h): returns the shared chunk length C and the largest
-// per-request segment count.
+// Split planner ("Lecture 4" section 4.2 and exercise 6; the reading is
+// spelled out in attn.h): the shortest page-multiple chunk C whose units fit
+// in one round of `slots` workers, or no split when even whole requests do
+// not fit.  Returns C and the largest per-request segment count.
 void plan(const int32_t* lens, int B, int Hkv, int page, int num_splits, int slots, int32_t* chunk,
           int32_t* max_splits) {
   int64_t longest = 1;
   for (int b = 0; b < B; ++b) longest = std::max<int64_t>(longest, lens[b]);
-  int64_t best_c = std::max<int64_t>(page, cdiv(longest, page) * page);
+  const int64_t full = std::max<int64_t>(page, cdiv(longest, page) * page);
+  int64_t best_c = full;
   if (num_splits > 0) {
     best_c = std::max<int64_t>(page, cdiv(cdiv(longest, num_splits), page) * page);
-  } else if ((int64_t)B * Hkv < slots) {
-    int64_t best_t = -1;
-    for (int64_t s = 1; (int64_t)B * Hkv * s <= 16LL * slots; s *= 2) {
-      const int64_t c = std::max<int64_t>(page, cdiv(cdiv(longest, s), page) * page);
-      const int64_t t = plan_makespan(lens, B, Hkv, slots, c);
-      if (best_t < 0 || t < best_t) {
-        best_t = t;
-        best_c = c;
-      }
+  } else if (plan_units(lens, B, Hkv, full) <= slots) {
+    int64_t lo = 1, hi = full / page;  // in pages; hi fits
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) / 2;
+      if (plan_units(lens, B, Hkv, mid * page) <= slots)
+        hi = mid;
+      else
+        lo = mid + 1;
     }
+    best_c = hi * page;
   }
   int64_t smax = 1;
   for (int b = 0; b < B; ++b) smax = std::max<int64_t>(smax, cdiv(lens[b], best_c));
@@ -240,9 +218,9 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   int32_t chunk = max_pages_per_seq * page_size, smax = 1;
+  std::vector<int32_t> host_lens;
+  const int32_t* lens = seq_lens_host;
   if (num_splits != 1) {
-    std::vector<int32_t> host_lens;
-    const int32_t* lens = seq_lens_host;
     if (lens == nullptr) {
       host_lens.resize(B);
       if (cudaMemcpyAsync(host_lens.data(), seq_lens, sizeof(int32_t) * B, cudaMemcpyDeviceToHost,
@@ -276,7 +254,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
   attn_status_t s = attn_host::launch_decode_bf16(q, k_pages, v_pages, block_table, seq_lens,
                                                   page_size, chunk, smax, o, lse, part_o, part_lse,
                                                   B, Hq, Hkv, d, max_pages_per_seq, num_pages,
-                                                  scale, st);
+                                                  scale, lens, st);
   if (s != ATTN_OK || smax == 1) return s;
   return attn_host::launch_merge(part_o, part_lse, B * Hq, smax, d, o, lse, dtype, st);
 }
@@ -454,7 +432,7 @@ attn_status_t attn_decode_cascade(const void* q, const void* prefix_k, const voi
   attn_status_t s = attn_host::launch_decode_bf16(q, k_pages, v_pages, block_table, seq_lens,
                                                   page_size, chunk, smax, o, lse, o_suf, lse_suf,
                                                   B, Hq, Hkv, d, max_pages_per_seq, num_pages,
-                                                  scale, side->stream);
+                                                  scale, seq_lens_host, side->stream);
   if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return ATTN_ERR_CUDA;
 
   // 1. the query rows of each KV head, stacked over the requests;

@@ -34,6 +34,8 @@
 //     (one segment) or its normalised partial state for the merge kernel.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
@@ -92,6 +94,16 @@ __device__ __forceinline__ void fma_phi_v(uint32_t pw, uint32_t v, float& c0, fl
       : "r"(pw), "r"(v));
 }
 
+// Compact grid of a split plan: request b owns the off[b + 1] - off[b]
+// segment CTAs blockIdx.x = off[b] .. off[b + 1] - 1 (n = B), so requests
+// shorter than the longest launch no empty CTAs.  n = 0: the plain grid
+// (segment, KV head group, request).
+constexpr int kSegMapMax = 512;
+struct SegMap {
+  int n;
+  int off[kSegMapMax + 1];
+};
+
 __global__ void __launch_bounds__(NUM_THREADS, 3)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -99,7 +111,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
                        const int32_t* __restrict__ seq_lens, int chunk, int max_splits,
                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                        float* __restrict__ part_o, float* __restrict__ part_lse, int Hq, int Hkv,
-                       int max_pages, int num_pages, float scale_log2, int* status) {
+                       int max_pages, int num_pages, float scale_log2, int* status,
+                       const __grid_constant__ SegMap map) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -111,14 +124,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
 
-  const int s = blockIdx.x;
+  int s = blockIdx.x, b = blockIdx.z, n_segs = max_splits;
+  if (map.n > 0) {  // the request whose segment range holds blockIdx.x
+    int lo = 0, hi = map.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (map.off[mid] <= static_cast<int>(blockIdx.x)) lo = mid;
+      else hi = mid - 1;
+    }
+    b = lo;
+    s = blockIdx.x - map.off[b];
+    n_segs = map.off[b + 1] - map.off[b];
+  }
   const int group = Hq / Hkv;
   const int groups_per_kvh = (group + HG - 1) / HG;
   const int kvh = blockIdx.y / groups_per_kvh;
   const int gi = blockIdx.y % groups_per_kvh;
   const int h0 = kvh * group + gi * HG;
   const int nh = min(HG, group - gi * HG);  // real heads in this CTA (the rest is padding)
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // A length past the table's capacity is reported and clamped, so the
@@ -376,6 +399,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
       } else {
         part_o[(r * max_splits + s) * D + t] = out;
         if (t == 0) part_lse[r * max_splits + s] = row_lse;
+        // Compact grid: the request's last segment CTA also writes the empty
+        // states (O = 0, LSE = -inf) of the slots past its segment count, so
+        // the merge reads max_splits written states per row.
+        if (s == n_segs - 1)
+          for (int s2 = n_segs; s2 < max_splits; ++s2) {
+            part_o[(r * max_splits + s2) * D + t] = 0.f;
+            if (t == 0) part_lse[r * max_splits + s2] = -INFINITY;
+          }
       }
     }
   }
@@ -433,18 +464,34 @@ attn_status_t launch_decode_bf16(const void* q, const void* k_pages, const void*
                                  const int32_t* block_table, const int32_t* seq_lens, int page_size,
                                  int chunk, int max_splits, void* o, float* lse, float* part_o,
                                  float* part_lse, int B, int Hq, int Hkv, int d, int max_pages,
-                                 int num_pages, float scale, cudaStream_t stream) {
+                                 int num_pages, float scale, const int32_t* lens_host,
+                                 cudaStream_t stream) {
   if (d != D || page_size != PAGE) return ATTN_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
   if (!set_smem_attr()) return ATTN_ERR_CUDA;
   CUtensorMap mk, mv;
   if (!make_page_map(&mk, k_pages, Hkv, num_pages) || !make_page_map(&mv, v_pages, Hkv, num_pages))
     return ATTN_ERR_CUDA;
-  dim3 grid(max_splits, Hkv * ((group + HG - 1) / HG), B);
+  const int groups = Hkv * ((group + HG - 1) / HG);
+  dim3 grid(max_splits, groups, B);
+  SegMap map;
+  map.n = 0;
+  if (max_splits > 1 && lens_host != nullptr && B <= kSegMapMax) {
+    // One CTA per non-empty segment (at least one per request): a plan that
+    // fits the resident CTAs runs as one wave with no empty CTAs in it.
+    map.n = B;
+    map.off[0] = 0;
+    for (int i = 0; i < B; ++i) {
+      const int len = lens_host[i] < 0 ? 0 : lens_host[i];
+      const int n = std::min(max_splits, std::max(1, (len + chunk - 1) / chunk));
+      map.off[i + 1] = map.off[i] + n;
+    }
+    grid = dim3(map.off[B], groups, 1);
+  }
   decode_bf16_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
       mk, mv, static_cast<const __nv_bfloat16*>(q), block_table, seq_lens, chunk, max_splits,
       static_cast<__nv_bfloat16*>(o), lse, part_o, part_lse, Hq, Hkv, max_pages, num_pages,
-      scale * attn::kLog2e, device_status_ptr());
+      scale * attn::kLog2e, device_status_ptr(), map);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

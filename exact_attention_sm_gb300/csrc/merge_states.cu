@@ -8,19 +8,20 @@
 // problem size alone and with no atomics, so the result is bitwise
 // reproducible ("Lecture 4", sections 4.3 and 5.6).
 //
-// One CTA (4 warps) per row.  The states of the row are dealt to the warps
-// (warp w takes s = w, w + 4, ...), each warp keeps 4 states' loads in flight
-// and lane l owns dims 4l + 128c; the 4 warp partials are then added in warp
-// order.  The summation order is fixed by (S, d) alone, so results are
-// bitwise reproducible.
+// One CTA of NW warps per row, NW = 4, 8 or 16 from S (more warps when a
+// row has many states, so that few rows still keep many loads in flight).
+// The states of the row are dealt to the warps (warp w takes s = w, w + NW,
+// ...), each warp keeps 4 states' loads in flight (the O loads do not wait
+// for the weights) and lane l owns dims 4l + 128c; the NW warp partials are
+// then added in warp order.  The summation order is fixed by (S, d) alone,
+// so results are bitwise reproducible.
 #include "common.cuh"
 
 namespace {
 
-constexpr int NW = 4;
 constexpr int UNROLL = 4;
 
-template <int C, bool BF16_OUT>
+template <int NW, int C, bool BF16_OUT>
 __global__ void __launch_bounds__(NW * 32) merge_kernel(const float* __restrict__ o_parts,
                                                         const float* __restrict__ lse_parts,
                                                         int S, int d, void* __restrict__ o_out,
@@ -39,7 +40,9 @@ __global__ void __launch_bounds__(NW * 32) merge_kernel(const float* __restrict_
   for (int off = 16; off > 0; off >>= 1) big = fmaxf(big, __shfl_xor_sync(0xffffffffu, big, off));
   if (lane == 0) red[warp] = big;
   __syncthreads();
-  big = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  big = red[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) big = fmaxf(big, red[w]);
 
   float4 acc[C];
 #pragma unroll
@@ -53,15 +56,22 @@ __global__ void __launch_bounds__(NW * 32) merge_kernel(const float* __restrict_
       for (int u = 0; u < UNROLL; ++u) {
         const int s = s0 + u * NW;
         const float ls = s < S ? lp[s] : -INFINITY;
-        w[u] = ls == -INFINITY ? 0.f : expf(ls - big);  // empty segment: weight 0, O never read
+        w[u] = ls == -INFINITY ? 0.f : expf(ls - big);  // empty segment: weight 0
 #pragma unroll
         for (int c = 0; c < C; ++c) {
           const int j = 4 * lane + 128 * c;
-          x[u][c] = (w[u] > 0.f && j < d)
+          x[u][c] = (s < S && j < d)
                         ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(s) * d + j)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+      // An empty segment's O may hold anything (it is not read by value):
+      // its weight 0 selects zeros instead of multiplying.
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u)
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          if (!(w[u] > 0.f)) x[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
         wsum += w[u];
@@ -110,16 +120,30 @@ __global__ void __launch_bounds__(NW * 32) merge_kernel(const float* __restrict_
   if (lane == 0 && lse_out != nullptr) lse_out[row] = empty ? -INFINITY : big + logf(total);
 }
 
+template <int NW, bool BF16_OUT>
+void launch_nw(const float* o_parts, const float* lse_parts, int rows, int S, int d, void* o_out,
+               float* lse_out, cudaStream_t stream) {
+  const int c = (d + 127) / 128;
+  if (c == 1)
+    merge_kernel<NW, 1, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out,
+                                                               lse_out);
+  else if (c == 2)
+    merge_kernel<NW, 2, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out,
+                                                               lse_out);
+  else
+    merge_kernel<NW, 4, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out,
+                                                               lse_out);
+}
+
 template <bool BF16_OUT>
 void launch(const float* o_parts, const float* lse_parts, int rows, int S, int d, void* o_out,
             float* lse_out, cudaStream_t stream) {
-  const int c = (d + 127) / 128;
-  if (c == 1)
-    merge_kernel<1, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out, lse_out);
-  else if (c == 2)
-    merge_kernel<2, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out, lse_out);
+  if (S <= 16)
+    launch_nw<4, BF16_OUT>(o_parts, lse_parts, rows, S, d, o_out, lse_out, stream);
+  else if (S <= 32)
+    launch_nw<8, BF16_OUT>(o_parts, lse_parts, rows, S, d, o_out, lse_out, stream);
   else
-    merge_kernel<4, BF16_OUT><<<rows, NW * 32, 0, stream>>>(o_parts, lse_parts, S, d, o_out, lse_out);
+    launch_nw<16, BF16_OUT>(o_parts, lse_parts, rows, S, d, o_out, lse_out, stream);
 }
 
 }  // namespace

@@ -90,14 +90,12 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  *
  * Chooses one chunk length C (a multiple of page_size) shared by every
  * request; request b is cut into max(1, ceil(len_b / C)) segments.
- * Reading of [Lecture 4] section 4.2, section 5.6 and exercise 6: a work
- * unit is (request, KV head, segment) and costs its token count plus a
- * fixed 512 tokens (launch and merge overhead; the pages give no figure);
- * `slots` workers take the units in launch order (segment fastest), each
- * as soon as it is free, and a plan costs the time the last one finishes.  If
- * B * Hkv >= slots nothing is split.  Otherwise S = 1, 2, 4, ... segments
- * (of the longest request, while B * Hkv * S <= 16 * slots) are tried and
- * the cheapest wins, ties going to fewer segments.
+ * Reading of [Lecture 4] section 4.2 and exercise 6 (whose answer is the
+ * finest split that still fits in one round of the SMs): a work unit is
+ * (request, KV head, segment) and `slots` workers run one unit each at a
+ * time.  C is the shortest multiple of page_size for which the non-empty
+ * units Hkv * sum_b ceil(len_b / C) fit in `slots`; if even unsplit
+ * requests do not fit, nothing is split.
  * num_splits > 0 forces C = ceil(ceil(max_len / num_splits) / page_size) *
  * page_size instead.  slots <= 0 means "ask the current device": SM count x
  * resident decode CTAs per SM.

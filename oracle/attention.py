@@ -480,34 +480,10 @@ def _cdiv(a, b):
     return -(-a // b)
 
 
-UNIT_OVERHEAD_TOKENS = 512
-
-
-def plan_makespan(seq_lens, num_kv_heads, slots, chunk):
-    """Time of one split plan in the lecture's simple GPU model.
-
-    [Lecture 4] section 0.5 / 4.2: a work unit (request, KV head, segment)
-    takes time proportional to the tokens it reads, plus a fixed
-    UNIT_OVERHEAD_TOKENS for launching it and merging its partial state (the
-    lecture: splitting "only adds merge overhead" once there is enough work;
-    the pages give no number: 512 tokens is this reading's, about the startup
-    cost of one decode CTA measured against its streaming rate).  ``slots``
-    workers take the units in launch order (segment fastest, then KV head,
-    then request), each worker taking the next unit as soon as it is free;
-    the plan costs the time the last worker finishes.  With equal units this
-    is waves * unit length, the exercise's arithmetic.  Empty units cost 0.
-    """
-    import heapq
-    lens = [int(x) for x in seq_lens]
-    smax = max([1] + [_cdiv(n, chunk) for n in lens])
-    free = [0] * slots
-    for n in lens:
-        for _ in range(num_kv_heads):
-            for s in range(smax):
-                tokens = max(0, min(n, (s + 1) * chunk) - s * chunk)
-                t = heapq.heappop(free)
-                heapq.heappush(free, t + (tokens + UNIT_OVERHEAD_TOKENS if tokens > 0 else 0))
-    return max(free)
+def plan_units(seq_lens, num_kv_heads, chunk):
+    """Non-empty work units (request, KV head, segment) when every request is
+    cut into segments of `chunk` tokens: Hkv * sum_b ceil(len_b / chunk)."""
+    return num_kv_heads * sum(_cdiv(int(n), chunk) for n in seq_lens)
 
 
 def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
@@ -517,18 +493,22 @@ def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
     (at least 1) and every chunk a multiple of page_size (one chunk shared by
     all requests).
 
-    Reading of the pages ([Lecture 4] sections 4.2 and 5.6, exercise 6):
-    * If the batch already has B * Hkv >= slots work units, no request is
-      split ("when the batch is large there are enough work units; splitting
-      only adds merge overhead").
-    * Otherwise the candidate segment counts are powers of two, as in the
-      exercise (1, 2, 4, ...), up to the largest S with B * Hkv * S <= 16 *
-      slots (more waves than that add merging without better balance).  S
-      gives the chunk C = ceil(ceil(max_len / S) / page_size) * page_size.
-      Each plan is timed with plan_makespan; the fastest wins and a tie goes
-      to the smaller S.  This picks 8 segments for 2 requests x 16384 tokens
-      x 8 KV heads on 132 SMs (the exercise's answer) and 16 segments (16x
-      faster) for 1 x 32K.
+    Reading of the pages ([Lecture 4] section 4.2, exercise 6 and its answer):
+    a work unit is (request, KV head, segment) and `slots` workers run one
+    unit each at a time.  The answer to exercise 6 picks the finest split
+    whose units still fit in one round of the workers (2 x 8 x 8 = 128 <= 132
+    SMs; more segments need a second round with smaller units and only add
+    merging), and its rule of thumb asks for requests x KV heads x segments
+    just within the worker count.  With requests of different lengths the
+    same rule is taken on the chunk length itself:
+    * C = the shortest multiple of page_size for which the non-empty units
+      Hkv * sum_b ceil(len_b / C) fit in `slots`;
+    * if even C = the longest length (no split) gives more units than slots,
+      nothing is split ("when the batch is large there are enough work units;
+      splitting only adds merge overhead").
+    This gives 8 segments for 2 requests x 16384 tokens x 8 KV heads on 132
+    SMs (the exercise's answer) and 16 segments (16x faster) for 1 x 32K
+    (section 4.2).
     * num_splits > 0 forces at most that many segments per request:
       C = ceil(ceil(max_len / num_splits) / page_size) * page_size.
     """
@@ -538,14 +518,16 @@ def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
     if num_splits > 0:
         c = max(page_size, _cdiv(_cdiv(longest, num_splits), page_size) * page_size)
         return [c] * bsz, [max(1, _cdiv(n, c)) for n in lens]
-    best_c = max(page_size, _cdiv(longest, page_size) * page_size)
-    if bsz * num_kv_heads < slots:
-        best_t = None
-        s = 1
-        while bsz * num_kv_heads * s <= 16 * slots:
-            c = max(page_size, _cdiv(_cdiv(longest, s), page_size) * page_size)
-            t = plan_makespan(lens, num_kv_heads, slots, c)
-            if best_t is None or t < best_t:
-                best_c, best_t = c, t
-            s *= 2
+    full = max(page_size, _cdiv(longest, page_size) * page_size)
+    best_c = full
+    if plan_units(lens, num_kv_heads, full) <= slots:
+        # smallest page multiple that still fits: units(C) never grows with C
+        lo, hi = 1, full // page_size          # in pages; hi fits
+        while lo < hi:
+            mid = (lo + hi) // 2
+            if plan_units(lens, num_kv_heads, mid * page_size) <= slots:
+                hi = mid
+            else:
+                lo = mid + 1
+        best_c = hi * page_size
     return [best_c] * bsz, [max(1, _cdiv(n, best_c)) for n in lens]

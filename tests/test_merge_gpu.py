@@ -11,7 +11,7 @@ from tests.gpu_util import to_np
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("S", [1, 3, 64])
+@pytest.mark.parametrize("S", [1, 3, 24, 64, 200])
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("empty", [0.0, 0.3])
 def test_merge_matches_oracle(S, d, empty):
@@ -40,3 +40,18 @@ def test_merge_is_deterministic():
     torch.cuda.synchronize()
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+@pytest.mark.parametrize("S", [5, 24, 100])
+def test_empty_states_are_not_read_by_value(S):
+    """An empty state (LSE = -inf) may hold anything in O, NaN included: it
+    gets weight 0 and its O never reaches the sum."""
+    o_p, l_p = inputs.merge_inputs(64, S, 128, seed=S, empty_frac=0.4)
+    o_ref, l_ref = orc.merge_states_batched(o_p.numpy(), l_p.numpy())
+    o_bad = o_p.clone()
+    o_bad[torch.isneginf(l_p)] = float("nan")
+    o32, l32 = ea.attn_merge_states(o_bad.cuda(), l_p.cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    got = to_np(o32)
+    assert np.isfinite(got).all()
+    assert np.abs(got - o_ref).max() < 1e-5

@@ -362,6 +362,23 @@ def test_plan_invariants():
     assert orc.plan_splits([1024] * 256, 8, 152, 16)[1] == [1] * 256
 
 
+def test_plan_one_round():
+    """Exercise 6's answer: the finest split whose units still fit in one
+    round; one page less per chunk would need a second round."""
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        lens = rng.integers(0, 140000, size=int(rng.integers(1, 9))).tolist()
+        hkv = int(rng.choice([1, 2, 8]))
+        slots = int(rng.choice([132, 152, 456]))
+        c = orc.plan_splits(lens, hkv, slots, 16)[0][0]
+        units = hkv * sum(-(-n // c) for n in lens)
+        if hkv * sum(1 for n in lens if n > 0) <= slots:
+            assert units <= slots
+            assert c == 16 or hkv * sum(-(-n // (c - 16)) for n in lens) > slots
+        else:
+            assert c >= max(lens)      # not split
+
+
 # ---------------------------------------------------------------- cascade decode
 
 def test_cascade_tokens_lecture_exercise_7():
