@@ -396,6 +396,38 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, scale):
     return o, lse
 
 
+def prefill_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_k, scale, causal):
+    """Chunked prefill of packed queries against a paged KV cache.
+
+    [Lecture 4] section 5.2: prefill over KV kept in shuffled physical
+    blocks gives exactly the attention over the blocks gathered into
+    contiguous arrays; [LLM book] 10.3.7 "addressing by block table":
+    block_table [B, max_pages], k_cache [num_pages, page_size, Hkv, d].
+    Sequence b's queries are rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of
+    q [total_q, Hq, d] ([LLM book] 10.3.8 packing); its keys are tokens
+    0 .. seq_lens_k[b]-1 of its pages (paged_gather).  Causal is aligned
+    bottom-right as in prefill_varlen: the queries are the last Lq tokens of
+    the Lk-token sequence (their K/V already in the cache).
+
+    Returns O [total_q, Hq, d] and LSE [total_q, Hq].
+    """
+    q = _f64(q)
+    hq = q.shape[1]
+    hkv = k_pages.shape[2]
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:2])
+    for b in range(len(cu_seqlens_q) - 1):
+        q0, q1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        lk = int(seq_lens_k[b])
+        for h in range(hq):
+            kh = kv_head_of(h, hq, hkv)
+            kk = paged_gather(k_pages, block_table[b], lk, kh)
+            vv = paged_gather(v_pages, block_table[b], lk, kh)
+            oo, ll, _, _ = attention_dense(q[q0:q1, h], kk, vv, scale, causal, lk - (q1 - q0))
+            o[q0:q1, h], lse[q0:q1, h] = oo, ll
+    return o, lse
+
+
 def decode_split_states(q_row, keys, values, scale, chunk):
     """Split-KV partial states of one query row (Flash-Decoding).
 

@@ -508,3 +508,61 @@ def test_varlen_rows_with_no_visible_key():
     # rows 4 and 5 see keys j <= row + (2 - 6), i.e. the square rule on the last two rows
     o_last, lse_last, _, _ = orc.attention_dense(q[4:, 0], k[:, 0], v[:, 0], 0.3, True, 0)
     assert np.isfinite(lse[4:]).all() and np.abs(o[4:, 0] - o_last).max() == 0
+
+
+# ---------------------------------------------------------------- paged prefill
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_prefill_lecture_5_2_equals_contiguous(causal):
+    """[Lecture 4] section 5.2: prefill of the three requests (lengths 19,
+    10, 29; block size 4; the page's shuffled block tables) over the paged
+    cache equals attention over the same K/V laid out contiguously, here
+    computed by torch float64 with its own masking (independent code)."""
+    g = GOLD["lecture_bsr_page_tables"]
+    bs, lens, tables = g["block_size"], g["seq_lens"], g["tables"]
+    rng = np.random.default_rng(11)
+    num_pages, hq, hkv, d = 24, 4, 2, 8
+    kp = rng.standard_normal((num_pages, bs, hkv, d))
+    vp = rng.standard_normal((num_pages, bs, hkv, d))
+    table = np.full((3, 8), -1)
+    for b, t in enumerate(tables):
+        table[b, :len(t)] = t
+    lq = [5, 10, 29]                      # chunks: the last 5, all 10, all 29 tokens
+    cu = np.concatenate([[0], np.cumsum(lq)])
+    q = rng.standard_normal((int(cu[-1]), hq, d))
+    o, lse = orc.prefill_paged(q, kp, vp, table, cu, lens, 0.3, causal)
+    for b in range(3):
+        # contiguous K/V by direct indexing of the block table (no paged_gather)
+        pages = np.asarray(tables[b])
+        k = kp[pages].reshape(-1, hkv, d)[:lens[b]]
+        v = vp[pages].reshape(-1, hkv, d)[:lens[b]]
+        mask = np.ones((lq[b], lens[b]), bool)
+        if causal:
+            mask = np.arange(lens[b])[None, :] <= np.arange(lq[b])[:, None] + lens[b] - lq[b]
+        qq = q[cu[b]:cu[b + 1]].transpose(1, 0, 2)
+        kk = np.repeat(k, hq // hkv, 1).transpose(1, 0, 2)
+        vv = np.repeat(v, hq // hkv, 1).transpose(1, 0, 2)
+        o_ref, lse_ref = _sdpa64_mask(qq, kk, vv, 0.3, mask)
+        assert np.abs(o[cu[b]:cu[b + 1]] - o_ref.transpose(1, 0, 2)).max() < 1e-12
+        assert np.abs(lse[cu[b]:cu[b + 1]] - lse_ref.T).max() < 1e-12
+
+
+def test_paged_prefill_with_whole_sequence_matches_varlen():
+    """Queries covering the whole sequence: the paged prefill is the packed
+    prefill of the gathered keys (the page's 'max diff 0')."""
+    rng = np.random.default_rng(12)
+    bs, hkv, d = 16, 1, 8
+    lens = [37, 16, 1]
+    pages = [[3, 0, 5], [1], [4]]
+    kp = rng.standard_normal((6, bs, hkv, d))
+    vp = rng.standard_normal((6, bs, hkv, d))
+    table = np.full((3, 3), -1)
+    for b, t in enumerate(pages):
+        table[b, :len(t)] = t
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q = rng.standard_normal((int(cu[-1]), 2, d))
+    o, lse = orc.prefill_paged(q, kp, vp, table, cu, lens, 0.5, True)
+    kc = np.concatenate([kp[p].reshape(-1, hkv, d)[:n] for p, n in zip(pages, lens)])
+    vc = np.concatenate([vp[p].reshape(-1, hkv, d)[:n] for p, n in zip(pages, lens)])
+    o2, lse2 = orc.prefill_varlen(q, kc, vc, cu, cu, 0.5, True)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
