@@ -57,6 +57,10 @@ WORKLOADS = {
                                       causal=True, dtype="bf16"),
     "prefill-varlen-llama-mixed": dict(kind="varlen", B=32, Hq=32, Hkv=8, max_len=4096, d=128,
                                        causal=True, dtype="bf16"),
+    # Chunked prefill against the paged cache: each request's newest `chunk`
+    # tokens attend to its whole cached context (lengths U[1024, 8192], seed 4).
+    "prefill-paged-chunk512-llama": dict(kind="paged", B=16, Hq=32, Hkv=8, chunk=512, d=128,
+                                         lo=1024, hi=8192, causal=True, dtype="bf16"),
     # Lecture 4, section 4.4 demo 4: a 4096-token prefix shared by 64 requests,
     # 256 unique tokens each.
     "decode-cascade-b64-prefix4096": dict(kind="cascade", B=64, Hq=32, Hkv=8, d=128, prefix=4096,
@@ -73,6 +77,10 @@ def describe(name):
     if w["kind"] == "varlen":
         return (f"{name}: {w['B']} packed sequences, lengths U[1,{w['max_len']}] seed 3, "
                 f"Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} causal (bottom-right) bf16 + LSE")
+    if w["kind"] == "paged":
+        return (f"{name}: {w['B']} requests, cached context U[{w['lo']},{w['hi']}] seed 4, the last "
+                f"{w['chunk']} tokens of each as packed queries, Hq={w['Hq']} Hkv={w['Hkv']} "
+                f"d={w['d']} causal (bottom-right) bf16 + LSE, 16-token shuffled pages")
     if w["kind"] == "cascade":
         return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, shared prefix "
                 f"{w['prefix']} + {w['suffix']} unique tokens per request (16-token shuffled pages)")
@@ -105,6 +113,14 @@ def varlen_lens(w):
 def varlen_flops(w, lens):
     """prefill_flops summed over the packed sequences (L_b^2 / 2 pairs each)."""
     return float(sum(4.0 * w["d"] * w["Hq"] * L * L * 0.5 for L in lens))
+
+
+def paged_flops(w, lens_q, lens_k):
+    """Causal-aware FLOPs of chunks at the end of longer sequences: row i of
+    a chunk of lq sees lk - lq + i + 1 keys; the diagonal block counts
+    lq^2 / 2 pairs as in prefill_flops."""
+    return float(sum(4.0 * w["d"] * w["Hq"] * (lq * (lk - lq) + lq * lq * 0.5)
+                     for lq, lk in zip(lens_q, lens_k)))
 
 
 def decode_bytes(w, lens):
@@ -261,6 +277,20 @@ def make_step(name, torch, ea, inputs):
         def step():
             ea.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True, out=o, lse=lse)
         return step, 1, varlen_flops(w, lens), "flops", None
+    if w["kind"] == "paged":
+        lens_k = inputs.decode_lengths_uniform(w["B"], w["lo"], w["hi"], seed=4)
+        lens_q = [min(w["chunk"], n) for n in lens_k]
+        _, kp, vp, table, sl = inputs.decode_inputs(lens_k, w["Hq"], w["Hkv"], w["d"], seed=0,
+                                                    device="cuda")
+        q, _, _, cq, _ = inputs.varlen_inputs(lens_q, lens_q, w["Hq"], w["Hkv"], w["d"], seed=1,
+                                              device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[0], w["Hq"], dtype=torch.float32, device="cuda")
+        mq, mk = max(lens_q), max(lens_k)
+
+        def step():
+            ea.attn_prefill_paged(q, kp, vp, table, cq, sl, mq, mk, causal=True, out=o, lse=lse)
+        return step, 1, paged_flops(w, lens_q, lens_k), "flops", None
     lens = decode_lens(w)
     q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0,
                                                 device="cuda")

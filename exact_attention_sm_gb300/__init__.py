@@ -28,6 +28,8 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                              _I, _P]),
+    "attn_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                _I, _I, _I, _F, _I, _P]),
     "attn_decode_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F,
@@ -141,6 +143,42 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=None, max_
                                max(1, int(max_seqlen_k)), total_q, total_k, Hq, Hkv, d,
                                1 if causal else 0, float(scale), _dtype_code(q), _stream(stream))
     _check(st, "attn_fwd_varlen")
+    return out, lse
+
+
+def attn_prefill_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_k,
+                       max_seqlen_q=None, max_seqlen_k=None, causal=False, scale=None, out=None,
+                       lse=None, want_lse=True, stream=None):
+    """Chunked prefill against a paged cache. q [total_q,Hq,d] bf16 packed by cu_seqlens_q
+    (int32 [B+1], device); k_pages/v_pages [num_pages,16,Hkv,d] bf16; block_table int32
+    [B,max_pages]; seq_lens_k int32 [B] (device). Causal is aligned bottom-right.
+    Returns (o [total_q,Hq,d], lse [total_q,Hq])."""
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"), (block_table, "block_table"),
+                 (cu_seqlens_q, "cu_seqlens_q"), (seq_lens_k, "seq_lens_k")):
+        _need(t, n)
+    for t in (block_table, cu_seqlens_q, seq_lens_k):
+        if t.dtype != torch.int32:
+            raise TypeError("block_table, cu_seqlens_q and seq_lens_k must be int32")
+    total_q, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    B = cu_seqlens_q.numel() - 1
+    if max_seqlen_q is None:
+        cq = cu_seqlens_q.cpu()
+        max_seqlen_q = int((cq[1:] - cq[:-1]).max()) if B > 0 else 1
+    if max_seqlen_k is None:
+        max_seqlen_k = int(seq_lens_k.max()) if B > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(total_q, Hq, dtype=torch.float32, device=q.device)
+    st = lib().attn_prefill_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                  _ptr(cu_seqlens_q), _ptr(seq_lens_k), _ptr(out), _ptr(lse), B,
+                                  max(1, int(max_seqlen_q)), int(max_seqlen_k), total_q, Hq, Hkv, d,
+                                  page_size, block_table.shape[1], num_pages, 1 if causal else 0,
+                                  float(scale), _dtype_code(q), _stream(stream))
+    _check(st, "attn_prefill_paged")
     return out, lse
 
 

@@ -20,6 +20,9 @@ attn_status_t launch_prefill_f32(const float*, const float*, const float*, float
                                  int, int, int, int, int, float, cudaStream_t);
 attn_status_t launch_prefill_bf16(const void*, const void*, const void*, void*, float*, int, int,
                                   int, int, int, int, int, float, int, cudaStream_t);
+attn_status_t launch_prefill_bf16_paged(const void*, const void*, const void*, const int*,
+                                        const int*, const int*, void*, float*, int, int, int, int,
+                                        int, int, int, int, int, int, float, cudaStream_t);
 attn_status_t launch_prefill_bf16_varlen(const void*, const void*, const void*, void*, float*,
                                          const int*, const int*, int, int, int, int, int, int, int,
                                          int, int, float, cudaStream_t);
@@ -175,6 +178,37 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                                                max_seqlen_q, max_seqlen_k, total_q, total_k, Hq,
                                                Hkv, d, causal ? 1 : 0, scale,
                                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                 const int32_t* seq_lens_k, void* o, float* lse, int B,
+                                 int max_seqlen_q, int max_seqlen_k, int total_q, int Hq, int Hkv,
+                                 int d, int page_size, int max_pages_per_seq, int num_pages,
+                                 int causal, float scale, attn_dtype_t dtype, attn_stream_t stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seqlen_q <= 0 || max_seqlen_k < 0 ||
+      total_q < 0 || max_pages_per_seq <= 0 || num_pages <= 0 || page_size <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (total_q == 0) return ATTN_OK;  // no query rows: nothing to write
+  if (!q || !k_pages || !v_pages || !block_table || !cu_seqlens_q || !seq_lens_k || !o)
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)max_seqlen_k > (int64_t)max_pages_per_seq * page_size) return ATTN_ERR_INVALID_ARG;
+  if ((int64_t)B * max_pages_per_seq > 0x7fffffffLL || num_pages == 0x7fffffff)
+    return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hq > (1 << 24) || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(seq_lens_k) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  return attn_host::launch_prefill_bf16_paged(
+      q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_k, o, lse, B, max_seqlen_q,
+      std::max(max_seqlen_k, 1), total_q, Hq, Hkv, d, max_pages_per_seq, num_pages,
+      causal ? 1 : 0, scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_decode_plan(const int32_t* seq_lens_host, int B, int Hkv, int page_size,

@@ -118,11 +118,23 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 // 10.3.8, variable-length batching): sequence b owns rows cu_q[b] ..
 // cu_q[b+1]-1 of q [total_q, Hq, d] and keys cu_k[b] .. of k, v
 // [total_k, Hkv, d]; Lq and Lk are then bounds on the lengths.
+// Paged K/V ([LLM book] 10.3.7 block-table addressing; "Lecture 4" 5.2):
+// the queries are packed as above, sequence b's keys are tokens 0 ..
+// seq_k[b]-1 of the cache [num_pages, 16, Hkv, d], token t in page
+// table[b * max_pages + t / 16], slot t % 16.
 struct Geo {
   const int* cu_q;  // nullptr: dense
   const int* cu_k;
   int Lq, Lk, total_q, total_k;
+  const int* seq_k;  // paged layout only
+  const int* table;
+  int max_pages, num_pages;
 };
+
+// Tensor layouts of one launch: dense [B, H, L, d]; packed sequences
+// (cu_seqlens); packed queries with K/V in a paged cache.
+constexpr int kDenseLayout = 0, kPackedLayout = 1, kPagedLayout = 2;
+constexpr int kPage = 16;  // tokens per cache page
 
 struct Seq {
   int q_off, lq, k_off, lk;
@@ -130,16 +142,27 @@ struct Seq {
 
 // One sequence's rows; a packed entry outside its bounds is reported and the
 // sequence treated as empty (nothing is read or written for it).
-template <bool kPacked>
+template <int kLayout>
 __device__ __forceinline__ Seq seq_of(const Geo& g, int b, int* status) {
-  if constexpr (!kPacked) return Seq{0, g.Lq, 0, g.Lk};
-  const int q0 = g.cu_q[b], q1 = g.cu_q[b + 1], k0 = g.cu_k[b], k1 = g.cu_k[b + 1];
-  if (q0 < 0 || q1 < q0 || q1 > g.total_q || q1 - q0 > g.Lq || k0 < 0 || k1 < k0 ||
-      k1 > g.total_k || k1 - k0 > g.Lk) {
-    attn::record_status(status, ATTN_ERR_BAD_INDEX);
-    return Seq{0, 0, 0, 0};
+  if constexpr (kLayout == kDenseLayout) {
+    return Seq{0, g.Lq, 0, g.Lk};
+  } else if constexpr (kLayout == kPackedLayout) {
+    const int q0 = g.cu_q[b], q1 = g.cu_q[b + 1], k0 = g.cu_k[b], k1 = g.cu_k[b + 1];
+    if (q0 < 0 || q1 < q0 || q1 > g.total_q || q1 - q0 > g.Lq || k0 < 0 || k1 < k0 ||
+        k1 > g.total_k || k1 - k0 > g.Lk) {
+      attn::record_status(status, ATTN_ERR_BAD_INDEX);
+      return Seq{0, 0, 0, 0};
+    }
+    return Seq{q0, q1 - q0, k0, k1 - k0};
+  } else {
+    const int q0 = g.cu_q[b], q1 = g.cu_q[b + 1], lk = g.seq_k[b];
+    if (q0 < 0 || q1 < q0 || q1 > g.total_q || q1 - q0 > g.Lq || lk < 0 || lk > g.Lk ||
+        lk > g.max_pages * kPage) {
+      attn::record_status(status, ATTN_ERR_BAD_INDEX);
+      return Seq{0, 0, 0, 0};
+    }
+    return Seq{q0, q1 - q0, 0, lk};
   }
-  return Seq{q0, q1 - q0, k0, k1 - k0};
 }
 
 // K/V tiles a 128-row Q tile reads: -1 if the tile has no rows, 0 if its rows
@@ -161,6 +184,89 @@ __device__ __forceinline__ int row_kmax(const Seq& sq, int grow, int causal) {
 }
 __device__ __forceinline__ bool tile_needs_mask(const Seq& sq, int qt, int j, int causal) {
   return j * BN + BN - 1 > row_kmax(sq, qt * BM, causal);
+}
+
+// Physical pages of one sequence's K/V tiles, looked up one tile ahead: the
+// block-table entries of tile j + 1 are requested when tile j is taken, so
+// their latency overlaps the wait for a free ring slot.  Pages past the
+// sequence's length are not looked up; they, and entries outside
+// [0, num_pages) (reported as ATTN_ERR_BAD_INDEX), take the page coordinate
+// num_pages, which lies outside the tensor: TMA writes zeros there and reads
+// nothing, and the complete-tx count is the full tile either way.
+struct PageCursor {
+  static constexpr int NP = BN / kPage;  // pages per K/V tile
+  const int* row;                        // the sequence's block-table row
+  int lk, j;                             // length; tile whose entries `next` holds
+  int next[NP];
+
+  __device__ __forceinline__ void fetch(const Geo& g) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int p = j * NP + i;
+      next[i] = p * kPage < lk ? row[p] : g.num_pages;
+    }
+  }
+  __device__ __forceinline__ void begin(const Geo& g, int b, int len) {
+    row = g.table + static_cast<size_t>(b) * g.max_pages;
+    lk = len;
+    j = 0;
+    fetch(g);
+  }
+  // Pages of tile j (tiles are taken in order 0, 1, ...).
+  __device__ __forceinline__ void take(int (&pg)[NP], const Geo& g, int* status) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const bool needed = (j * NP + i) * kPage < lk;
+      pg[i] = next[i];
+      if (needed && (pg[i] < 0 || pg[i] >= g.num_pages)) {
+        attn::record_status(status, ATTN_ERR_BAD_INDEX);
+        pg[i] = g.num_pages;
+      }
+    }
+    ++j;
+    fetch(g);
+  }
+};
+
+// One K or V tile from the paged cache: a 4-D TMA copy {64 columns, KV head,
+// 16 slots, page} per page and 64-column block, into the same swizzled rows
+// a dense tile occupies (each page is 16 rows, 2 KB per block, so the
+// 1024-byte swizzle atoms line up).
+template <int KB, int BLOCK_BYTES>
+__device__ __forceinline__ void tma_load_pages(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                               const int (&pg)[PageCursor::NP], int kvh) {
+#pragma unroll
+  for (int i = 0; i < PageCursor::NP; ++i)
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb)
+      tma_load_4d(dst + kb * BLOCK_BYTES + i * kPage * 128, map, bar, kb * 64, kvh, 0, pg[i]);
+}
+
+// Paged cache: the slots of a sequence's last page past its length may hold
+// anything, and P = 0 times a NaN there would still reach O through the PV
+// MMA.  Before P of the tile holding the last key is handed over, the softmax
+// thread of each such row clears it in the landed V tile (tile rows
+// [lk - j BN, round_up(lk, 16) - j BN)); pages wholly past the length were
+// zero-filled by TMA.
+template <int KB, int BLOCK_BYTES>
+__device__ __forceinline__ void clear_v_tail(uint8_t* vtile, int row, int lk, int j) {
+  const int lo = lk - j * BN;
+  const int hi = min(BN, (lk + kPage - 1) / kPage * kPage - j * BN);
+  if (row >= lo && row < hi) {
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+      uint4* r = reinterpret_cast<uint4*>(vtile + kb * BLOCK_BYTES + row * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) r[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  fence_proxy_async_smem();  // the generic stores, then the tensor core's reads
+}
+
+// Whether tile j of a sequence of lk keys holds its last key inside a
+// partial page (the case clear_v_tail handles).
+__device__ __forceinline__ bool has_v_tail(int lk, int j) {
+  return (lk % kPage) != 0 && (lk - 1) / BN == j;
 }
 
 struct Item {
@@ -201,7 +307,7 @@ __device__ __forceinline__ Schedule make_schedule(int num_items, int num_pairs, 
   return sc;
 }
 
-template <bool kPacked>
+template <int kLayout>
 __device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int Hq, int num_pairs,
                                             const Geo& geo, int causal, int* status) {
   Item w;
@@ -213,7 +319,7 @@ __device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int Hq
     pair = num_pairs - 1 - it / BH;
     w.bh = it % BH;
   }
-  w.sq = seq_of<kPacked>(geo, w.bh / Hq, status);
+  w.sq = seq_of<kLayout>(geo, w.bh / Hq, status);
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
     w.qt[x] = 2 * pair + x;
@@ -224,7 +330,7 @@ __device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int Hq
   return w;
 }
 
-template <int D, bool kPacked>
+template <int D, int kLayout>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -233,6 +339,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         int causal, float scale_log2, int q_div, int* status) {
   using C = Cfg<D>;
   constexpr int NS = C::NS;
+  constexpr bool kPacked = kLayout != kDenseLayout;
+  constexpr bool kPaged = kLayout == kPagedLayout;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -302,7 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int nq[2] = {0, 0};       // Q tiles issued per slot
       bool ok = true;
       for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-        const Item w = decode_item<kPacked>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
+        const Item w = decode_item<kLayout>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
         const int nmax = max(w.n[0], w.n[1]);
         if (nmax == 0) continue;
         const int h = w.bh % Hq;
@@ -310,6 +418,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // packed ones [rows, heads].
         const int kv_c1 = packed ? h / group : 0;
         const int kv_c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
+        PageCursor pages;
+        if constexpr (kPaged) pages.begin(geo, w.bh / Hq, w.sq.lk);
         // K/V tile j of this item into the next ring slot.
         auto issue_kv = [&](int j) -> bool {
           const int st = g % NS;
@@ -317,14 +427,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             return false;
           uint8_t* kdst = smem + C::OFF_K + st * C::TILE_BYTES;
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
-          mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &k_full[st], kb * 64,
-                        packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
-          mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &v_full[st], kb * 64,
-                        packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
+          if constexpr (kPaged) {
+            int pg[PageCursor::NP];
+            pages.take(pg, geo, status);  // tile j (tiles are issued in order)
+            mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
+            tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[st], pg, kv_c1);
+            mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
+            tma_load_pages<C::KB, C::BLOCK_BYTES>(vdst, &tm_v, &v_full[st], pg, kv_c1);
+          } else {
+            mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &k_full[st], kb * 64,
+                          packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
+            mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &v_full[st], kb * 64,
+                          packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
+          }
           ++g;
           return true;
         };
@@ -407,7 +526,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
 
       for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-        const Item w = decode_item<kPacked>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
+        const Item w = decode_item<kLayout>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
         const int nmax = max(w.n[0], w.n[1]);
         if (nmax == 0) continue;
         // First QK^T of each present tile.
@@ -470,10 +589,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t s_addr = tmem + lane_off + x * BN;
     const uint32_t o_addr = tmem + lane_off + C::O_COL + x * D;
     int ns = 0, nitem = 0;
+    int g0 = 0;  // K/V tiles of the items before this one (the producer's ring count)
     bool ok = true;
     for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-      const Item w = decode_item<kPacked>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
+      const Item w = decode_item<kLayout>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
       const int n = w.n[x];
+      const int g_item = g0;
+      g0 += max(w.n[0], w.n[1]);
       const int grow = w.qt[x] * BM + row;
       const int h = w.bh % Hq;
       // Output row: dense [heads, rows], packed [rows, heads].
@@ -566,6 +688,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
             tmem_st32(o_addr + c * 32, o32);
+          }
+        }
+        if constexpr (kPaged) {
+          if (has_v_tail(w.sq.lk, j)) {
+            const int gt = g_item + j;  // this K/V tile's ring position
+            ok = __all_sync(FULL, mbar_wait(&v_full[gt % NS], (gt / NS) & 1, abort_flag,
+                                            kWaitLimitNs));
+            clear_v_tail<C::KB, C::BLOCK_BYTES>(smem + C::OFF_V + (gt % NS) * C::TILE_BYTES, row,
+                                                w.sq.lk, j);
           }
         }
         tmem_st_wait();
@@ -665,10 +796,11 @@ struct SeqCache {
   Seq sq;
 };
 
-template <bool kPacked>
+template <int kLayout>
 __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int Hq, int num_qt,
                                               const Geo& geo, int causal, int* status,
                                               SeqCache& cache) {
+  constexpr bool kPacked = kLayout != kDenseLayout;
   Item1 w;
   if (grouped) {
     w.bh = it / num_qt;
@@ -680,12 +812,12 @@ __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int 
   if constexpr (kPacked) {
     const int b = w.bh / Hq;
     if (b != cache.b) {
-      cache.sq = seq_of<true>(geo, b, status);
+      cache.sq = seq_of<kLayout>(geo, b, status);
       cache.b = b;
     }
     w.sq = cache.sq;
   } else {
-    w.sq = seq_of<false>(geo, w.bh / Hq, status);
+    w.sq = seq_of<kLayout>(geo, w.bh / Hq, status);
   }
   const int kv = kv_tiles(w.sq, w.qt, causal);
   w.n = kv > 0 ? kv : 0;
@@ -693,7 +825,7 @@ __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int 
   return w;
 }
 
-template <bool kPacked>
+template <int kLayout>
 __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     prefill_bf16_d64_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
@@ -703,6 +835,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
                             int* status) {
   using C = Cfg64;
   constexpr int D = C::D, NS = C::NS, NQ = C::NQ;
+  constexpr bool kPacked = kLayout != kDenseLayout;
+  constexpr bool kPaged = kLayout == kPagedLayout;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -747,7 +881,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   }
   SeqCache seq_cache;
   auto item_at = [&](int it) {
-    return decode_item1<kPacked>(it, sched.grouped, BH, Hq, num_qt, geo, causal, status,
+    return decode_item1<kLayout>(it, sched.grouped, BH, Hq, num_qt, geo, causal, status,
                                  seq_cache);
   };
   // The first item at or after `it` (in this CTA's order) with K/V work,
@@ -809,6 +943,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       prefetch_tmap(&tm_v);
       struct Cur {
         int it, j, n, c1, c2;  // tile j of n; TMA coordinates (rows, heads) of tile 0
+        PageCursor pages;      // paged cache: this item's pages, one tile ahead
       };
       auto enter = [&](Cur& c, int it) {
         Item1 w;
@@ -820,6 +955,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           c.n = w.n;
           c.c1 = packed ? h / group : 0;
           c.c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
+          if constexpr (kPaged) c.pages.begin(geo, w.bh / Hq, w.sq.lk);
         }
       };
       auto next = [&](Cur& c) {
@@ -835,8 +971,14 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         const int st = tk % NS;
         if (tk >= NS && !wait(&k_done[st], (tk / NS) + 1)) return false;
         mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
-        tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k, &k_full[st], 0,
-                    packed ? ck.c1 : ck.j * BN, packed ? ck.c2 + ck.j * BN : ck.c2);
+        if constexpr (kPaged) {
+          int pg[PageCursor::NP];
+          ck.pages.take(pg, geo, status);
+          tma_load_pages<1, C::TILE_BYTES>(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k,
+                                           &k_full[st], pg, ck.c1);
+        } else
+          tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k, &k_full[st], 0,
+                      packed ? ck.c1 : ck.j * BN, packed ? ck.c2 + ck.j * BN : ck.c2);
         ++tk;
         next(ck);
         return true;
@@ -845,8 +987,14 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         const int st = tv % NS;
         if (tv >= NS && !wait(&pv_done[st], (tv / NS) + 1)) return false;
         mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
-        tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v, &v_full[st], 0,
-                    packed ? cv.c1 : cv.j * BN, packed ? cv.c2 + cv.j * BN : cv.c2);
+        if constexpr (kPaged) {
+          int pg[PageCursor::NP];
+          cv.pages.take(pg, geo, status);
+          tma_load_pages<1, C::TILE_BYTES>(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v,
+                                           &v_full[st], pg, cv.c1);
+        } else
+          tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v, &v_full[st], 0,
+                      packed ? cv.c1 : cv.j * BN, packed ? cv.c2 + cv.j * BN : cv.c2);
         ++tv;
         next(cv);
         return true;
@@ -1114,6 +1262,13 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         }
         tmem_st32(p_addr, pk[0]);
         tmem_st32(p_addr + 32, pk[1]);
+        if constexpr (kPaged) {
+          if (has_v_tail(w.sq.lk, j)) {
+            ok = __all_sync(FULL, wait(&v_full[tt % NS], tt / NS));
+            clear_v_tail<1, C::TILE_BYTES>(smem + C::OFF_V + (tt % NS) * C::TILE_BYTES, row,
+                                           w.sq.lk, j);
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -1199,6 +1354,25 @@ bool make_map_packed(CUtensorMap* m, const void* base, int D, int H, int total) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Paged cache [num_pages, 16 slots, Hkv, d] bf16 viewed as {d, Hkv, 16,
+// num_pages}; box {64, 1, 16, 1}: one page of one KV head, 64 columns, in
+// the tile's 128-byte swizzle.  The page coordinate num_pages (past the
+// tensor) reads as zeros.
+bool make_map_pages(CUtensorMap* m, const void* base, int D, int Hkv, int num_pages) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(kPage), static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(Hkv) * D * 2,
+                                 static_cast<cuuint64_t>(kPage) * Hkv * D * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kPage), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [BH heads, L rows] x d bf16 viewed as a 3-D tensor {d, L, BH}; box
 // {64, 128, 1} with 128-byte swizzle.  Rows past L read as zeros.
 bool make_map(CUtensorMap* m, const void* base, int D, int L, int BH) {
@@ -1215,7 +1389,7 @@ bool make_map(CUtensorMap* m, const void* base, int D, int L, int BH) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kPacked>
+template <int D, int kLayout>
 attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                      int Hkv, const Geo& geo, int causal, float scale, int q_div,
                      cudaStream_t stream) {
@@ -1227,9 +1401,9 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   if (!attr_set) {
     const void* fn;
     if constexpr (kD64)
-      fn = reinterpret_cast<const void*>(prefill_bf16_d64_kernel<kPacked>);
+      fn = reinterpret_cast<const void*>(prefill_bf16_d64_kernel<kLayout>);
     else
-      fn = reinterpret_cast<const void*>(prefill_bf16_kernel<D, kPacked>);
+      fn = reinterpret_cast<const void*>(prefill_bf16_kernel<D, kLayout>);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
             cudaSuccess ||
         cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
@@ -1239,12 +1413,18 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   }
   CUtensorMap mq, mk, mv;
   if (q_div < 1 || (B * Hq) % q_div != 0) return ATTN_ERR_INVALID_ARG;
-  const bool maps_ok =
-      kPacked
-          ? make_map_packed(&mq, q, D, Hq, geo.total_q) && make_map_packed(&mk, k, D, Hkv, geo.total_k) &&
-                make_map_packed(&mv, v, D, Hkv, geo.total_k)
-          : make_map(&mq, q, D, geo.Lq, B * Hq / q_div) && make_map(&mk, k, D, geo.Lk, B * Hkv) &&
-                make_map(&mv, v, D, geo.Lk, B * Hkv);
+  bool maps_ok;
+  if constexpr (kLayout == kPagedLayout)
+    maps_ok = make_map_packed(&mq, q, D, Hq, geo.total_q) &&
+              make_map_pages(&mk, k, D, Hkv, geo.num_pages) &&
+              make_map_pages(&mv, v, D, Hkv, geo.num_pages);
+  else if constexpr (kLayout == kPackedLayout)
+    maps_ok = make_map_packed(&mq, q, D, Hq, geo.total_q) &&
+              make_map_packed(&mk, k, D, Hkv, geo.total_k) &&
+              make_map_packed(&mv, v, D, Hkv, geo.total_k);
+  else
+    maps_ok = make_map(&mq, q, D, geo.Lq, B * Hq / q_div) && make_map(&mk, k, D, geo.Lk, B * Hkv) &&
+              make_map(&mv, v, D, geo.Lk, B * Hkv);
   if (!maps_ok) return ATTN_ERR_CUDA;
   const int num_qt = (geo.Lq + BM - 1) / BM;
   const long long items = static_cast<long long>(B) * Hq * (kD64 ? num_qt : (num_qt + 1) / 2);
@@ -1255,11 +1435,11 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   const int grid = static_cast<int>(items < slots ? items : slots);
   const float scale_log2 = scale * attn::kLog2e;
   if constexpr (kD64) {
-    prefill_bf16_d64_kernel<kPacked><<<grid, Cfg64::THREADS, smem_bytes, stream>>>(
+    prefill_bf16_d64_kernel<kLayout><<<grid, Cfg64::THREADS, smem_bytes, stream>>>(
         mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, geo, causal,
         scale_log2, q_div, attn_host::device_status_ptr());
   } else {
-    prefill_bf16_kernel<D, kPacked><<<grid, NUM_THREADS, smem_bytes, stream>>>(
+    prefill_bf16_kernel<D, kLayout><<<grid, NUM_THREADS, smem_bytes, stream>>>(
         mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, geo, causal,
         scale_log2, q_div, attn_host::device_status_ptr());
   }
@@ -1273,10 +1453,10 @@ namespace attn_host {
 attn_status_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                                   float scale, int q_div, cudaStream_t stream) {
-  const Geo geo{nullptr, nullptr, Lq, Lk, 0, 0};
-  if (d == 64) return launch<64, false>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
+  const Geo geo{nullptr, nullptr, Lq, Lk, 0, 0, nullptr, nullptr, 0, 0};
+  if (d == 64) return launch<64, kDenseLayout>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
   if (d == 128)
-    return launch<128, false>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
+    return launch<128, kDenseLayout>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
   return ATTN_ERR_UNSUPPORTED;
 }
 
@@ -1285,9 +1465,28 @@ attn_status_t launch_prefill_bf16_varlen(const void* q, const void* k, const voi
                                          int max_q, int max_k, int total_q, int total_k, int Hq,
                                          int Hkv, int d, int causal, float scale,
                                          cudaStream_t stream) {
-  const Geo geo{cu_q, cu_k, max_q, max_k, total_q, total_k};
-  if (d == 64) return launch<64, true>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, 1, stream);
-  if (d == 128) return launch<128, true>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, 1, stream);
+  const Geo geo{cu_q, cu_k, max_q, max_k, total_q, total_k, nullptr, nullptr, 0, 0};
+  if (d == 64)
+    return launch<64, kPackedLayout>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, 1, stream);
+  if (d == 128)
+    return launch<128, kPackedLayout>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, 1, stream);
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+attn_status_t launch_prefill_bf16_paged(const void* q, const void* k_pages, const void* v_pages,
+                                        const int* block_table, const int* cu_q,
+                                        const int* seq_lens_k, void* o, float* lse, int B,
+                                        int max_q, int max_k, int total_q, int Hq, int Hkv, int d,
+                                        int max_pages, int num_pages, int causal, float scale,
+                                        cudaStream_t stream) {
+  const Geo geo{cu_q, nullptr, max_q, max_k, total_q, 0, seq_lens_k, block_table, max_pages,
+                num_pages};
+  if (d == 64)
+    return launch<64, kPagedLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal, scale, 1,
+                                    stream);
+  if (d == 128)
+    return launch<128, kPagedLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal, scale,
+                                     1, stream);
   return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -232,6 +232,42 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                               attn_stream_t stream);
 
 /*
+ * attn_prefill_paged - chunked prefill of packed queries against a paged KV
+ * cache ("Lecture 4" section 5.2: attention over KV in shuffled physical
+ * blocks equals attention over the blocks gathered contiguously; "10.3
+ * FlashAttention" 10.3.7 block-table addressing, 10.3.8 packing).
+ *
+ *   q [total_q, Hq, d] bf16 packed as in attn_fwd_varlen with
+ *   cu_seqlens_q [B + 1] (DEVICE int32); o [total_q, Hq, d] bf16; lse
+ *   [total_q, Hq] fp32 or NULL.
+ *   k_pages, v_pages [num_pages, 16, Hkv, d] bf16 (the decode cache layout);
+ *   block_table [B, max_pages_per_seq] int32 and seq_lens_k [B] int32, both
+ *   on the device: sequence b's keys are tokens 0 .. seq_lens_k[b]-1, token
+ *   t in page block_table[b][t / 16], slot t % 16.  Entries at or past
+ *   ceil(seq_lens_k[b] / 16) are never read.
+ *   max_seqlen_q / max_seqlen_k bound the lengths (max_seqlen_k <=
+ *   max_pages_per_seq * 16).
+ *
+ * Causal is aligned bottom-right as in attn_fwd_varlen: the chunk's queries
+ * are the last Lq of the sequence's Lk tokens (their K/V already appended).
+ * Slots of a sequence's last page past its length may hold anything: they
+ * never reach the result.  d in {64, 128}, page_size 16, bf16.  total_q = 0
+ * returns ATTN_OK without a launch.  Errors: ATTN_ERR_INVALID_ARG for NULLs,
+ * bad sizes or misalignment; ATTN_ERR_UNSUPPORTED for other d, page sizes
+ * or dtypes.  On the device, a cu_seqlens_q entry or length out of bounds,
+ * or a needed block-table entry outside [0, num_pages), is reported as
+ * ATTN_ERR_BAD_INDEX (the sequence is skipped, or the page reads as zeros and
+ * that sequence's rows are not meaningful); nothing outside the tensors is
+ * read or written.
+ */
+attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                 const int32_t* seq_lens_k, void* o, float* lse, int B,
+                                 int max_seqlen_q, int max_seqlen_k, int total_q, int Hq, int Hkv,
+                                 int d, int page_size, int max_pages_per_seq, int num_pages,
+                                 int causal, float scale, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
  * Cascade (shared-prefix) decode ([Lecture 4] 4.4 "cascade attention" and
  * 5.3 "composable formats").  B requests share one prefix of prefix_len
  * tokens, stored once as prefix_k / prefix_v [Hkv, prefix_len, d] bf16

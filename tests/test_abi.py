@@ -208,3 +208,33 @@ def test_varlen_rejects_on_host():
 def test_varlen_without_queries_is_a_no_op():
     """total_q = 0 (every sequence empty) succeeds without a launch, NULLs allowed."""
     assert varlen(q=None, k=None, v=None, o=None, cq=None, ck=None, tq=0, tk=0) == 0
+
+
+def paged(**kw):
+    args = dict(q=FAKE, kp=FAKE, vp=FAKE, table=FAKE, cq=FAKE, sk=FAKE, o=FAKE, lse=None, B=2, mq=8,
+                mk=40, tq=12, Hq=4, Hkv=2, d=128, page=16, max_pages=4, num_pages=8, causal=1,
+                scale=0.1, dtype=ea.ATTN_BF16)
+    args.update(kw)
+    a = args
+    return ea.lib().attn_prefill_paged(a["q"], a["kp"], a["vp"], a["table"], a["cq"], a["sk"],
+                                       a["o"], a["lse"], a["B"], a["mq"], a["mk"], a["tq"], a["Hq"],
+                                       a["Hkv"], a["d"], a["page"], a["max_pages"],
+                                       a["num_pages"], a["causal"], a["scale"], a["dtype"], None)
+
+
+def test_prefill_paged_rejects_on_host():
+    assert paged(q=None) == 1
+    assert paged(table=None) == 1
+    assert paged(sk=None) == 1
+    assert paged(B=0) == 1
+    assert paged(Hkv=3) == 1
+    assert paged(mq=0) == 1
+    assert paged(mk=65) == 1                  # longer than max_pages * 16
+    assert paged(num_pages=0) == 1
+    assert paged(scale=-1.0) == 1
+    assert paged(kp=MISALIGNED) == 1
+    assert paged(table=ctypes.c_void_p(0x10002)) == 1
+    assert paged(d=96) == 2
+    assert paged(page=32) == 2
+    assert paged(dtype=ea.ATTN_F32) == 2
+    assert paged(tq=0, q=None, o=None) == 0   # no query rows: no launch
