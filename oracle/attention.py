@@ -505,6 +505,61 @@ def decode_cascade(q, prefix_k, prefix_v, k_pages, v_pages, block_table, suffix_
 
 
 # --------------------------------------------------------------------------
+# Backward pass (training)
+# --------------------------------------------------------------------------
+
+def attention_backward(q, k, v, do, scale, causal=False):
+    """Gradients of O = softmax(scale Q K^T) V for one head, in float64.
+
+    [LLM book] "backward and recomputation" and [Tiling blog] section 07:
+    the forward keeps only O and the per-row LSE; the backward rebuilds
+    S = scale Q K^T and P = exp(S - LSE) and accumulates dQ, dK, dV.  The
+    pages print no gradient formulas; these are the chain rule through
+    O = P V and the row softmax, materialised whole:
+        dV = P^T dO
+        dP = dO V^T
+        D_i = sum_j P_ij dP_ij
+        dS = P * (dP - D)          (elementwise, D_i along row i)
+        dQ = scale dS K,   dK = scale dS^T Q
+    Masked entries (causal, square rule as attention_dense) have P = 0 and
+    contribute nothing; a row with no visible key gets dQ = 0.
+    Returns dQ [Lq, d], dK [Lk, d], dV [Lk, d] and D [Lq].
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    _, lse, s, _ = attention_dense(q, k, v, scale, causal)
+    with np.errstate(invalid="ignore"):
+        p = np.exp(s - lse[:, None])
+    p[~np.isfinite(lse)] = 0.0
+    p[~np.isfinite(p)] = 0.0
+    dv = p.T @ do
+    dp = do @ v.T
+    dd = (p * dp).sum(axis=1)
+    ds = p * (dp - dd[:, None])
+    return scale * (ds @ k), scale * (ds.T @ q), dv, dd
+
+
+def backward(q, k, v, do, scale, causal):
+    """attention_backward over [B, H, L, d] tensors with grouped-query
+    heads (kv_head_of): a KV head's dK, dV sum the contributions of all the
+    query heads that read it.  Returns dQ [B,Hq,Lq,d], dK and dV
+    [B,Hkv,Lk,d]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    b_, hq = q.shape[:2]
+    hkv = k.shape[1]
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for b in range(b_):
+        for h in range(hq):
+            kh = kv_head_of(h, hq, hkv)
+            gq, gk, gv, _ = attention_backward(q[b, h], k[b, kh], v[b, kh], do[b, h], scale, causal)
+            dq[b, h] = gq
+            dk[b, kh] += gk
+            dv[b, kh] += gv
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
 # Split planning (host integer logic)
 # --------------------------------------------------------------------------
 

@@ -566,3 +566,66 @@ def test_paged_prefill_with_whole_sequence_matches_varlen():
     vc = np.concatenate([vp[p].reshape(-1, hkv, d)[:n] for p, n in zip(pages, lens)])
     o2, lse2 = orc.prefill_varlen(q, kc, vc, cu, cu, 0.5, True)
     assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+# ---------------------------------------------------------------- backward
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_torch_autograd(causal):
+    """The chain-rule gradients equal torch autograd through torch's float64
+    math attention (independent code), with grouped-query heads."""
+    rng = np.random.default_rng(31)
+    q = rng.standard_normal((2, 4, 7, 5))
+    k = rng.standard_normal((2, 2, 7, 5))
+    v = rng.standard_normal((2, 2, 7, 5))
+    do = rng.standard_normal((2, 4, 7, 5))
+    dq, dk, dv = orc.backward(q, k, v, do, 0.4, causal)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    with sdpa_kernel(SDPBackend.MATH):
+        o = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk.repeat_interleave(2, dim=1), tv.repeat_interleave(2, dim=1), is_causal=causal,
+            scale=0.4)
+    (o * torch.tensor(do)).sum().backward()
+    assert np.abs(dq - tq.grad.numpy()).max() < 1e-12
+    assert np.abs(dk - tk.grad.numpy()).max() < 1e-12
+    assert np.abs(dv - tv.grad.numpy()).max() < 1e-12
+
+
+def test_backward_finite_differences():
+    """Central differences of the loss sum(dO * O) on a tiny head."""
+    rng = np.random.default_rng(32)
+    q, k, v, do = (rng.standard_normal((4, 3)) for _ in range(4))
+    dq, dk, dv, _ = orc.attention_backward(q, k, v, do, 0.7, True)
+
+    def loss(qq, kk, vv):
+        return float((orc.attention_dense(qq, kk, vv, 0.7, True)[0] * do).sum())
+
+    eps = 1e-6
+    for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += eps
+            up = loss(*args)
+            args[which][idx] -= 2 * eps
+            num[idx] = (up - loss(*args)) / (2 * eps)
+        assert np.abs(num - g).max() < 1e-7
+
+
+def test_backward_closed_forms():
+    rng = np.random.default_rng(33)
+    q, do = rng.standard_normal((5, 4)), rng.standard_normal((5, 4))
+    k, v = rng.standard_normal((1, 4)), rng.standard_normal((1, 4))
+    # one key: P = 1 everywhere, so dV = sum of dO, and dS = P (dP - D) = 0
+    dq, dk, dv, _ = orc.attention_backward(q, k, v, do, 0.5, False)
+    assert np.abs(dv[0] - do.sum(0)).max() < 1e-14
+    assert np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-14
+    # D_i = sum_j P_ij dP_ij equals rowsum(dO_i * O_i) (O = P V)
+    k, v = rng.standard_normal((6, 4)), rng.standard_normal((6, 4))
+    o = orc.attention_dense(q, k, v, 0.5, True)[0]
+    _, _, _, dd = orc.attention_backward(q, k, v, do, 0.5, True)
+    assert np.abs(dd - (do * o).sum(1)).max() < 1e-13
+    # no keys at all: every row sees nothing, so every gradient is zero
+    dq, dk, dv, _ = orc.attention_backward(q, k[:0], v[:0], do, 0.5, False)
+    assert (dq == 0).all() and dk.shape == (0, 4) and dv.shape == (0, 4)
