@@ -30,6 +30,9 @@ SIGNATURES = {
                              _I, _P]),
     "attn_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                 _I, _I, _I, _F, _I, _P]),
+    "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ,
+                      _I, _P]),
     "attn_decode_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F,
@@ -180,6 +183,30 @@ def attn_prefill_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_
                                   float(scale), _dtype_code(q), _stream(stream))
     _check(st, "attn_prefill_paged")
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, d_o, causal=False, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Backward of attn_fwd: q, o, d_o [B,Hq,Lq,d], k, v [B,Hkv,Lk,d] bf16, lse [B,Hq,Lq] fp32.
+    Returns (dq, dk, dv) in bf16."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (d_o, "d_o")):
+        _need(t, n)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(lib().attn_bwd_workspace_bytes(B, Hq, Lq), dtype=torch.uint8,
+                                device=q.device)
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq),
+                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Lq, Lk, d, 1 if causal else 0,
+                        float(scale), _ptr(workspace), workspace.numel(), _dtype_code(q),
+                        _stream(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_decode_plan(seq_lens_host, num_kv_heads, page_size=16, num_splits=0, slots=0):

@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cpp", "status.cu", "prefill_f32.cu", "prefill_sm103.cu", "decode_paged.cu",
-           "merge_states.cu", "decode_noalloc.cu", "cascade.cu"]
+           "merge_states.cu", "decode_noalloc.cu", "cascade.cu", "backward_sm103.cu"]
 
 
 def _nvcc():

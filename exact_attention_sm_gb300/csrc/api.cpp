@@ -29,6 +29,9 @@ attn_status_t launch_prefill_bf16_varlen(const void*, const void*, const void*, 
 attn_status_t launch_decode_bf16(const void*, const void*, const void*, const int32_t*,
                                  const int32_t*, int, int, int, void*, float*, float*, float*, int,
                                  int, int, int, int, int, float, const int32_t*, cudaStream_t);
+attn_status_t launch_bwd_bf16(const void*, const void*, const void*, const void*, const float*,
+                              const void*, void*, void*, void*, float*, int, int, int, int, int,
+                              int, int, float, cudaStream_t);
 attn_status_t launch_merge(const float*, const float*, int, int, int, void*, float*, attn_dtype_t,
                            cudaStream_t);
 attn_status_t launch_cascade_gather_q(const void*, void*, int, int, int, int, cudaStream_t);
@@ -209,6 +212,36 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void*
       q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_k, o, lse, B, max_seqlen_q,
       std::max(max_seqlen_k, 1), total_q, Hq, Hkv, d, max_pages_per_seq, num_pages,
       causal ? 1 : 0, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Lq) {
+  if (B <= 0 || Hq <= 0 || Lq <= 0) return 0;
+  return round_up(static_cast<size_t>(B) * Hq * Lq * sizeof(float), kAlign);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* d_o, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                       void* workspace, size_t workspace_bytes, attn_dtype_t dtype,
+                       attn_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (causal && Lq != Lk) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_bytes(B, Hq, Lq);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+    return ATTN_ERR_WORKSPACE;
+  return attn_host::launch_bwd_bf16(q, k, v, o, lse, d_o, dq, dk, dv,
+                                    static_cast<float*>(workspace), B, Hq, Hkv, Lq, Lk, d,
+                                    causal ? 1 : 0, scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_decode_plan(const int32_t* seq_lens_host, int B, int Hkv, int page_size,

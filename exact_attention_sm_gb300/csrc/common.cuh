@@ -70,6 +70,10 @@ attn_status_t launch_decode_bf16(const void* q, const void* k_pages, const void*
                                  float* part_lse, int B, int Hq, int Hkv, int d, int max_pages,
                                  int num_pages, float scale, const int32_t* lens_host,
                                  cudaStream_t stream);
+attn_status_t launch_bwd_bf16(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                              float* dd, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
+                              float scale, cudaStream_t stream);
 attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int rows, int S, int d,
                            void* o_out, float* lse_out, attn_dtype_t out_dtype, cudaStream_t stream);
 attn_status_t launch_cascade_gather_q(const void* q, void* q_stack, int B, int Hq, int Hkv, int d,

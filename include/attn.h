@@ -232,6 +232,35 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                               attn_stream_t stream);
 
 /*
+ * attn_bwd - backward pass of attn_fwd (bf16), for training.
+ *
+ * "10.3 FlashAttention", backward and recomputation: from Q, K, V, the
+ * forward's O and LSE, and the output gradient dO, the kernels rebuild
+ * S = scale Q K^T and P = exp(S - LSE) tile by tile on chip and return
+ *   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q
+ * (dK, dV of a KV head sum over its Hq / Hkv query heads).  No L x L matrix
+ * is stored.  Every gradient element is written by one CTA in a fixed
+ * order (no atomics): results are bitwise reproducible.
+ *
+ *   q, o, d_o, dq  [B, Hq, Lq, d] bf16     k, v, dk, dv  [B, Hkv, Lk, d] bf16
+ *   lse            [B, Hq, Lq] fp32 (natural log, as attn_fwd writes it)
+ *   workspace      attn_bwd_workspace_bytes(B, Hq, Lq) bytes, 256-byte
+ *                  aligned (holds D); device memory owned by the caller.
+ *   causal requires Lq == Lk (square rule, as attn_fwd).
+ * d in {64, 128}, bf16 only.  Errors: ATTN_ERR_INVALID_ARG for NULLs, bad
+ * sizes or misalignment; ATTN_ERR_UNSUPPORTED for other d or dtypes or
+ * causal with Lq != Lk; ATTN_ERR_WORKSPACE if the workspace is missing,
+ * short or misaligned; device timeouts through the status word.
+ */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Lq);
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* d_o, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
+                       void* workspace, size_t workspace_bytes, attn_dtype_t dtype,
+                       attn_stream_t stream);
+
+/*
  * attn_prefill_paged - chunked prefill of packed queries against a paged KV
  * cache ("Lecture 4" section 5.2: attention over KV in shuffled physical
  * blocks equals attention over the blocks gathered contiguously; "10.3

@@ -238,3 +238,30 @@ def test_prefill_paged_rejects_on_host():
     assert paged(page=32) == 2
     assert paged(dtype=ea.ATTN_F32) == 2
     assert paged(tq=0, q=None, o=None) == 0   # no query rows: no launch
+
+
+def bwd(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1,
+                Hq=4, Hkv=2, Lq=64, Lk=64, d=128, causal=1, scale=0.1, ws=FAKE, ws_bytes=4096,
+                dtype=ea.ATTN_BF16)
+    args.update(kw)
+    a = args
+    return ea.lib().attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                             a["dv"], a["B"], a["Hq"], a["Hkv"], a["Lq"], a["Lk"], a["d"],
+                             a["causal"], a["scale"], a["ws"], a["ws_bytes"], a["dtype"], None)
+
+
+def test_bwd_rejects_on_host():
+    assert ea.lib().attn_bwd_workspace_bytes(2, 4, 100) == 3328   # 800 floats -> 256-byte multiple
+    assert bwd(q=None) == 1
+    assert bwd(dv=None) == 1
+    assert bwd(Hkv=3) == 1
+    assert bwd(Lk=0) == 1
+    assert bwd(scale=0.0) == 1
+    assert bwd(dk=MISALIGNED) == 1
+    assert bwd(d=96) == 2
+    assert bwd(dtype=ea.ATTN_F32) == 2
+    assert bwd(Lk=65) == 2                    # causal needs Lq == Lk
+    assert bwd(ws=None) == 3
+    assert bwd(ws_bytes=100) == 3
+    assert bwd(ws=ctypes.c_void_p(0x10010)) == 3

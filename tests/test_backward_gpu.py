@@ -1,0 +1,83 @@
+"""Backward pass (dQ, dK, dV) on the GPU against the float64 oracle.
+
+Tolerance for bf16 gradients, from the arithmetic: the kernels round P and dS
+to bf16 (relative 2^-9 each) before the tensor-core products, take D from the
+bf16 O, and rebuild P from the forward's fp32 LSE (itself within 1e-2 of the
+exact value in the worst row, far less typically).  Each gradient element is
+a sum of such products, so its error is a small fraction of the gradient's
+own scale: max |err| <= 2e-2 * max |ref| and sum |err| <= 1e-2 * sum |ref|
+per tensor.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_sm_gb300 as ea
+from exact_attention_sm_gb300 import inputs
+from oracle import attention as orc
+from tests.gpu_util import to_np
+
+pytestmark = pytest.mark.gpu
+
+MAX_REL, SUM_REL = 2e-2, 1e-2
+
+
+def check_grad(got, want, name):
+    got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    assert got.shape == want.shape, name
+    assert np.isfinite(got).all(), f"{name}: non-finite"
+    err = np.abs(got - want)
+    scale = max(np.abs(want).max(), 1e-3)  # an all-zero gradient (one key) has no scale of its own
+    assert err.max() <= MAX_REL * scale, f"{name}: max {err.max():.3e} vs scale {scale:.3e}"
+    total = max(np.abs(want).sum(), 1e-3 * want.size)
+    assert err.sum() <= SUM_REL * total, f"{name}: sum-rel {err.sum() / total:.3e}"
+
+
+def run(B, Hq, Hkv, Lq, Lk, d, causal, seed=0):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Lq, Lk, d, "bf16", seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    do = torch.randn(B, Hq, Lq, d, generator=g).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = ea.attn_fwd(qc, kc, vc, causal=causal, scale=scale)
+    dq, dk, dv = ea.attn_bwd(qc, kc, vc, o, lse, doc, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ea.attn_get_device_status() == "ATTN_OK"
+    rq, rk, rv = orc.backward(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                              do.float().numpy(), scale, causal)
+    check_grad(to_np(dq), rq, "dQ")
+    check_grad(to_np(dk), rk, "dK")
+    check_grad(to_np(dv), rv, "dV")
+    return (qc, kc, vc, o, lse, doc), (dq, dk, dv)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_gqa(d, causal):
+    """Three Q/K tiles with a ragged tail, two query heads per KV head."""
+    run(2, 4, 2, 300, 300, d, causal, seed=1)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_exact_tile_and_single_row(d):
+    run(1, 2, 2, 128, 128, d, True, seed=2)
+    run(1, 2, 1, 1, 1, d, True, seed=3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_cross_lengths_non_causal(d):
+    run(2, 2, 1, 200, 333, d, False, seed=4)
+
+
+def test_longer_sequence_mha():
+    run(1, 4, 1, 1024, 1024, 128, True, seed=5)
+
+
+def test_deterministic():
+    args, (dq, dk, dv) = run(1, 4, 2, 257, 257, 64, True, seed=6)
+    for _ in range(2):
+        dq2, dk2, dv2 = ea.attn_bwd(*args, causal=True)
+        torch.cuda.synchronize()
+        assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
