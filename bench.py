@@ -61,6 +61,12 @@ WORKLOADS = {
     # tokens attend to its whole cached context (lengths U[1024, 8192], seed 4).
     "prefill-paged-chunk512-llama": dict(kind="paged", B=16, Hq=32, Hkv=8, chunk=512, d=128,
                                          lo=1024, hi=8192, causal=True, dtype="bf16"),
+    # Training: the backward pass of the GPT-2-medium-shaped causal attention
+    # (the forward's O and LSE precomputed; dO random).
+    "gpt2-medium-backward": dict(kind="backward", B=64, Hq=16, Hkv=16, L=1024, d=64, causal=True,
+                                 dtype="bf16"),
+    "llama3-8b-backward-8k": dict(kind="backward", B=1, Hq=32, Hkv=8, L=8192, d=128, causal=True,
+                                  dtype="bf16"),
     # Lecture 4, section 4.4 demo 4: a 4096-token prefix shared by 64 requests,
     # 256 unique tokens each.
     "decode-cascade-b64-prefix4096": dict(kind="cascade", B=64, Hq=32, Hkv=8, d=128, prefix=4096,
@@ -74,6 +80,9 @@ def describe(name):
     if w["kind"] == "prefill":
         return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} L={w['L']} d={w['d']} "
                 f"{'causal' if w['causal'] else 'non-causal'} {w['dtype']} + LSE")
+    if w["kind"] == "backward":
+        return (f"{name}: backward (dQ, dK, dV) of B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} "
+                f"L={w['L']} d={w['d']} causal bf16, from O, LSE and dO")
     if w["kind"] == "varlen":
         return (f"{name}: {w['B']} packed sequences, lengths U[1,{w['max_len']}] seed 3, "
                 f"Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} causal (bottom-right) bf16 + LSE")
@@ -103,6 +112,14 @@ def prefill_flops(w, rows=None):
         per_head = L * L * (0.5 if w["causal"] else 1.0)
         return 4.0 * d * w["B"] * w["Hq"] * per_head
     return float(sum(4.0 * d * ((i + 1) if w["causal"] else L) for (_, _, i) in rows))
+
+
+def backward_flops(w):
+    """FLOPs of the backward by the FlashAttention papers' count: five
+    matrix products (S, dP, dV, dK, dQ) of 2 d FLOP per visible pair, i.e.
+    2.5 x prefill_flops.  The kernels run seven (S and dP are built twice,
+    once per gradient kernel); the extra two are not counted."""
+    return 2.5 * prefill_flops(w)
 
 
 def varlen_lens(w):
@@ -147,7 +164,8 @@ def source_sha(files):
 
 KERNEL_SOURCES = {"prefill": ["prefill_sm103.cu", "sm103_ptx.cuh", "common.cuh"],
                   "prefill_f32": ["prefill_f32.cu", "common.cuh"],
-                  "decode": ["decode_paged.cu", "sm103_ptx.cuh", "tma_host.h", "common.cuh"]}
+                  "decode": ["decode_paged.cu", "sm103_ptx.cuh", "tma_host.h", "common.cuh"],
+                  "backward": ["backward_sm103.cu", "sm103_ptx.cuh", "tma_host.h", "common.cuh"]}
 
 
 def traffic_for(workload, kind):
@@ -266,6 +284,19 @@ def make_step(name, torch, ea, inputs):
         return step, 1, prefill_flops(w), "flops", None
     if w["kind"] == "cascade":
         return make_cascade_step(w, torch, ea, inputs)
+    if w["kind"] == "backward":
+        q, k, v = inputs.prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["L"], w["L"], w["d"], "bf16",
+                                        seed=0, device="cuda")
+        d_o = inputs.prefill_inputs(w["B"], w["Hq"], w["Hq"], w["L"], 1, w["d"], "bf16", seed=1,
+                                    device="cuda")[0]
+        o, lse = ea.attn_fwd(q, k, v, causal=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(ea.lib().attn_bwd_workspace_bytes(w["B"], w["Hq"], w["L"]),
+                         dtype=torch.uint8, device="cuda")
+
+        def step():
+            ea.attn_bwd(q, k, v, o, lse, d_o, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+        return step, 3, backward_flops(w), "flops", None
     if w["kind"] == "varlen":
         lens = varlen_lens(w)
         q, k, v, cq, ck = inputs.varlen_inputs(lens, lens, w["Hq"], w["Hkv"], w["d"], seed=0,
@@ -411,7 +442,8 @@ def measure(name, torch, ea, inputs, steps, warmup, flush, peaks, peak_src):
             # fp32 FFMA on CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz max clock
             roof = {"bound": "alu", "achieved": value, "peak": 152 * 128 * 2 * 2.07e9 / 1e12,
                     "unit": "TFLOP/s", "peak_source": "fp32 FMA: 152 SM x 128 lanes x 2 x 2.07 GHz"}
-        tkind = "prefill" if w["dtype"] == "bf16" else "prefill_f32"
+        tkind = ("backward" if w["kind"] == "backward"
+                 else "prefill" if w["dtype"] == "bf16" else "prefill_f32")
     else:
         value = work / (mean_ms * 1e-3) / 1e9
         unit = "GB/s"
