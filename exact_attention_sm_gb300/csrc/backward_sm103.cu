@@ -57,6 +57,26 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed two-lane fp32 FMA / add (one instruction for two lanes of work).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 template <int D>
 struct BwdCfg {
   static constexpr int KB = D / 64;             // 64-column, 128-byte swizzle blocks per row
@@ -74,25 +94,34 @@ __host__ __device__ constexpr uint32_t idesc(int N, bool b_mn_major) {
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(T >> 4) << 24);
 }
 
-// D(tmem) (+)= A B^T for two K-major smem tiles ([rows][D] bf16, 128-byte
-// swizzle, KB column blocks of BLOCK_BYTES): one MMA per 16 columns of D.
+// A tile is processed in two halves of H = 64 rows (queries in bwd_dkdv,
+// keys in bwd_dq): the elementwise warps start on the first half while the
+// tensor core computes the second.  Half h of a K-major or MN-major tile
+// starts 64 rows (8 KB, eight whole swizzle atoms) into each column block.
+constexpr int H = T / 2;
+constexpr uint64_t kHalfStep = (H * 128) >> 4;  // descriptor start-address step of a half
+
+// D(tmem, 128 x H fp32) = A B^T for the 128-row K-major tile A and half of
+// the K-major tile B ([rows][D] bf16, 128-byte swizzle, KB column blocks of
+// BLOCK_BYTES): one MMA per 16 columns of D.
 template <int D>
-__device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+__device__ __forceinline__ void mma_kmajor_half(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
   constexpr uint64_t kBlk = BwdCfg<D>::BLOCK_BYTES >> 4;
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint64_t off = (k >> 2) * kBlk + (k & 3) * 2;
-    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc(T, false), k > 0 ? 1u : 0u);
+    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc(H, false), k > 0 ? 1u : 0u);
   }
 }
 
-// D(tmem) (+)= A(tmem, 128 x 128 bf16 pairs) B, B an MN-major smem tile
-// ([128 rows = the K dimension][D] bf16): one MMA per 16 rows of B.
+// D(tmem) (+)= A(tmem, 128 rows x H bf16 in H / 2 columns) B, B half of an
+// MN-major smem tile ([H rows = the K dimension][D] bf16): one MMA per 16
+// rows of B.
 template <int D>
-__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           bool accumulate) {
+__device__ __forceinline__ void mma_tmem_a_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                bool accumulate) {
 #pragma unroll
-  for (int k = 0; k < T / 16; ++k)
+  for (int k = 0; k < H / 16; ++k)
     mma_bf16_ts(d_tmem, a_tmem + k * 8, b_desc + static_cast<uint64_t>(k) * 128, idesc(D, true),
                 (accumulate || k > 0) ? 1u : 0u);
 }
@@ -141,9 +170,10 @@ struct BwdBars {
   uint64_t* kv_empty;  // [2]
   uint64_t* q_full;    // [2]
   uint64_t* q_empty;   // [2]
-  uint64_t* s_full;
-  uint64_t* p_ready;
-  uint64_t* ds_ready;
+  uint64_t* s_full;    // [2] per half: S (S^T) of the half is in TMEM
+  uint64_t* dp_full;   // [2] per half: dP (dP^T)
+  uint64_t* p_ready;   // [2] per half: P^T written (bwd_dkdv)
+  uint64_t* ds_ready;  // [2] per half: dS (dS^T) written
   uint64_t* acc_done;
   uint64_t* drain;
   uint64_t* vec_full;  // [2] per-query values staged by the elementwise warps
@@ -159,12 +189,13 @@ __device__ __forceinline__ BwdBars carve_bars(uint8_t* base) {
   r.q_full = b + 4;
   r.q_empty = b + 6;
   r.s_full = b + 8;
-  r.p_ready = b + 9;
-  r.ds_ready = b + 10;
-  r.acc_done = b + 11;
-  r.drain = b + 12;
-  r.vec_full = b + 13;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 15);
+  r.dp_full = b + 10;
+  r.p_ready = b + 12;
+  r.ds_ready = b + 14;
+  r.acc_done = b + 16;
+  r.drain = b + 17;
+  r.vec_full = b + 18;
+  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 20);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
   return r;
 }
@@ -178,10 +209,11 @@ __device__ __forceinline__ bool bwd_prologue(const BwdBars& bb, int* status) {
       mbar_init(&bb.kv_empty[s], 1);
       mbar_init(&bb.q_full[s], 1);
       mbar_init(&bb.q_empty[s], 1);
+      mbar_init(&bb.s_full[s], 1);
+      mbar_init(&bb.dp_full[s], 1);
+      mbar_init(&bb.p_ready[s], 4);   // one arrival per elementwise warp
+      mbar_init(&bb.ds_ready[s], 4);
     }
-    mbar_init(bb.s_full, 1);
-    mbar_init(bb.p_ready, 4);   // one arrival per elementwise warp
-    mbar_init(bb.ds_ready, 4);
     mbar_init(bb.acc_done, 1);
     mbar_init(bb.drain, 1);
     mbar_init(&bb.vec_full[0], 4);
@@ -331,20 +363,36 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t do_addr = sbase + (TDO + st) * C::TILE_BYTES;
         if (!wait(&bb.q_full[st], n >> 1)) { ok = false; break; }
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T (keys as rows).
-        mma_kmajor<D>(tmem + C::S_COL, k_desc, smem_desc_sw128(q_addr, 16, 1024));
-        mma_kmajor<D>(tmem + C::DP_COL, v_desc, smem_desc_sw128(do_addr, 16, 1024));
-        mma_commit(bb.s_full);
-        // dV += P^T dO once P^T is in TMEM.
-        if (!wait(bb.p_ready, n)) { ok = false; break; }
-        tc_fence_after();
-        mma_tmem_a<D>(tmem + C::ACC1_COL, tmem + C::S_COL,
-                      smem_desc_sw128(do_addr, C::BLOCK_BYTES, 1024), n > 0);
-        // dK += dS^T Q once dS^T is in TMEM.
-        if (!wait(bb.ds_ready, n)) { ok = false; break; }
-        tc_fence_after();
-        mma_tmem_a<D>(tmem + C::ACC0_COL, tmem + C::DP_COL,
-                      smem_desc_sw128(q_addr, C::BLOCK_BYTES, 1024), n > 0);
+        // S^T = K Q^T, then dP^T = V dO^T (keys as rows), query half by half:
+        // columns h * 64.. of S^T and dP^T.
+        const uint64_t q_k = smem_desc_sw128(q_addr, 16, 1024);
+        const uint64_t do_k = smem_desc_sw128(do_addr, 16, 1024);
+        for (int hh = 0; hh < 2; ++hh) {
+          mma_kmajor_half<D>(tmem + C::S_COL + hh * H, k_desc, q_k + hh * kHalfStep);
+          mma_commit(&bb.s_full[hh]);
+        }
+        for (int hh = 0; hh < 2; ++hh) {
+          mma_kmajor_half<D>(tmem + C::DP_COL + hh * H, v_desc, do_k + hh * kHalfStep);
+          mma_commit(&bb.dp_full[hh]);
+        }
+        // dV += P^T dO, half by half as P^T arrives (P^T of half h in
+        // columns h * 32.. as bf16 pairs; dO rows h * 64..).
+        const uint64_t do_mn = smem_desc_sw128(do_addr, C::BLOCK_BYTES, 1024);
+        const uint64_t q_mn = smem_desc_sw128(q_addr, C::BLOCK_BYTES, 1024);
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          if (!wait(&bb.p_ready[hh], n)) { ok = false; break; }
+          tc_fence_after();
+          mma_tmem_a_half<D>(tmem + C::ACC1_COL, tmem + C::S_COL + hh * (H / 2),
+                             do_mn + hh * kHalfStep, n > 0 || hh > 0);
+        }
+        // dK += dS^T Q, half by half as dS^T arrives.
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          if (!wait(&bb.ds_ready[hh], n)) { ok = false; break; }
+          tc_fence_after();
+          mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + C::DP_COL + hh * (H / 2),
+                             q_mn + hh * kHalfStep, n > 0 || hh > 0);
+        }
+        if (!ok) break;
         mma_commit(&bb.q_empty[st]);  // Q and dO of this stage may be refilled
       }
       if (ok) mma_commit(bb.acc_done);
@@ -364,18 +412,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float scale_log2 = scale * attn::kLog2e;
     const int kk = j * T + c;                      // this thread's key
     // Per-query values of iteration n for query column c (this thread
-    // stages one of the 128): LSE in the log2 domain (+inf where the query
-    // row does not exist or sees no key, so that P = 0) and D.
+    // stages one of the 128), negated for the packed FMAs: -LSE in the log2
+    // domain (-inf where the query row does not exist or sees no key, so
+    // that P = 0) and -D.
     auto fetch = [&](int n, float& l2, float& dv_) {
-      l2 = INFINITY;
+      l2 = -INFINITY;
       dv_ = 0.f;
       if (n < n_iter) {
         const int bhq = b * Hq + hk * g + n / per_head;
         const int row = (i0 + n % per_head) * T + c;
         if (row < Lq) {
           const float x = lse[static_cast<size_t>(bhq) * Lq + row];
-          if (x != -INFINITY) l2 = x * attn::kLog2e;
-          dv_ = dd[static_cast<size_t>(bhq) * Lq + row];
+          if (x != -INFINITY) l2 = -x * attn::kLog2e;
+          dv_ = -dd[static_cast<size_t>(bhq) * Lq + row];
         }
       }
     };
@@ -399,56 +448,85 @@ __global__ void __launch_bounds__(THREADS, 1)
       fetch(n + 1, pre_l2, pre_d);
       const int i = i0 + n % per_head;
       const bool diag = causal && i == j;          // keys past the query are masked here
-      ok = __all_sync(FULL, wait(bb.s_full, n));
-      if (!ok) break;
-      tc_fence_after();
-      // P^T row c: P[r] = 2^(S^T[c][r] scale log2e - LSE_r log2e), packed to bf16 pairs.
+      // P^T row c, query half by half: P[r] = 2^(S^T[c][r] scale log2e -
+      // LSE_r log2e) as bf16 pairs, written to columns h * 32.. (over S^T
+      // columns this thread has already read).
       uint32_t pw[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t sr[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + q4 * 32, sr);
+      for (int hh = 0; ok && hh < 2; ++hh) {
+        ok = __all_sync(FULL, wait(&bb.s_full[hh], n));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[2][32];
+        tmem_ld32(tmem + lane_off + C::S_COL + hh * H, sr[0]);
+        tmem_ld32(tmem + lane_off + C::S_COL + hh * H + 32, sr[1]);
         tmem_ld_wait();
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int r = q4 * 32 + e;
-          float p0 = ex2(__uint_as_float(sr[e]) * scale_log2 - l2s[r]);
-          float p1 = ex2(__uint_as_float(sr[e + 1]) * scale_log2 - l2s[r + 1]);
+        for (int e = 0; e < H; e += 4) {
+          const int r = hh * H + e;
+          const float4 nl = *reinterpret_cast<const float4*>(&l2s[r]);
+          float2 pa = ffma2(make_float2(__uint_as_float(sr[e >> 5][e & 31]),
+                                        __uint_as_float(sr[e >> 5][(e & 31) + 1])),
+                            sc2, make_float2(nl.x, nl.y));
+          float2 pb = ffma2(make_float2(__uint_as_float(sr[e >> 5][(e & 31) + 2]),
+                                        __uint_as_float(sr[e >> 5][(e & 31) + 3])),
+                            sc2, make_float2(nl.z, nl.w));
+          pa.x = ex2(pa.x);
+          pa.y = ex2(pa.y);
+          pb.x = ex2(pb.x);
+          pb.y = ex2(pb.y);
           if (diag) {
-            if (kk > i * T + r) p0 = 0.f;
-            if (kk > i * T + r + 1) p1 = 0.f;
+            if (kk > i * T + r) pa.x = 0.f;
+            if (kk > i * T + r + 1) pa.y = 0.f;
+            if (kk > i * T + r + 2) pb.x = 0.f;
+            if (kk > i * T + r + 3) pb.y = 0.f;
           }
-          pw[(q4 * 32 + e) >> 1] = attn::pack_bf16x2(p0, p1);
+          pw[r >> 1] = attn::pack_bf16x2(pa.x, pa.y);
+          pw[(r >> 1) + 1] = attn::pack_bf16x2(pb.x, pb.y);
         }
+        tmem_st32(tmem + lane_off + C::S_COL + hh * (H / 2),
+                  *reinterpret_cast<uint32_t(*)[32]>(&pw[hh * 32]));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bb.p_ready[hh]);
       }
-      tmem_st32(tmem + lane_off + C::S_COL, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
-      tmem_st32(tmem + lane_off + C::S_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bb.p_ready);
-      // dS^T row c: dS[r] = P[r] (dP^T[c][r] - D_r), with P as handed to the MMA.
-      uint32_t sw[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t dr[32];
-        tmem_ld32(tmem + lane_off + C::DP_COL + q4 * 32, dr);
+      if (!ok) break;
+      // dS^T row c: dS[r] = P[r] (dP^T[c][r] - D_r), with P as handed to the
+      // MMA, written over dP^T columns this thread has already read.
+      for (int hh = 0; ok && hh < 2; ++hh) {
+        ok = __all_sync(FULL, wait(&bb.dp_full[hh], n));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dr[2][32];
+        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H, dr[0]);
+        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H + 32, dr[1]);
         tmem_ld_wait();
+        uint32_t sw[32];
+        const float2 zero2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int r = q4 * 32 + e;
-          const uint32_t p = pw[r >> 1];
-          const float s0 = attn::bf16_lo(p) * (__uint_as_float(dr[e]) - ds_[r]);
-          const float s1 = attn::bf16_hi(p) * (__uint_as_float(dr[e + 1]) - ds_[r + 1]);
-          sw[r >> 1] = attn::pack_bf16x2(s0, s1);
+        for (int e = 0; e < H; e += 4) {
+          const int r = hh * H + e;
+          const float4 nd = *reinterpret_cast<const float4*>(&ds_[r]);
+          const float2 xa = fadd2(make_float2(__uint_as_float(dr[e >> 5][e & 31]),
+                                              __uint_as_float(dr[e >> 5][(e & 31) + 1])),
+                                  make_float2(nd.x, nd.y));
+          const float2 xb = fadd2(make_float2(__uint_as_float(dr[e >> 5][(e & 31) + 2]),
+                                              __uint_as_float(dr[e >> 5][(e & 31) + 3])),
+                                  make_float2(nd.z, nd.w));
+          const uint32_t p0 = pw[r >> 1], p1 = pw[(r >> 1) + 1];
+          const float2 sa = ffma2(make_float2(attn::bf16_lo(p0), attn::bf16_hi(p0)), xa, zero2);
+          const float2 sb = ffma2(make_float2(attn::bf16_lo(p1), attn::bf16_hi(p1)), xb, zero2);
+          sw[e >> 1] = attn::pack_bf16x2(sa.x, sa.y);
+          sw[(e >> 1) + 1] = attn::pack_bf16x2(sb.x, sb.y);
         }
+        tmem_st32(tmem + lane_off + C::DP_COL + hh * (H / 2), sw);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bb.ds_ready[hh]);
       }
-      tmem_st32(tmem + lane_off + C::DP_COL, *reinterpret_cast<uint32_t(*)[32]>(&sw[0]));
-      tmem_st32(tmem + lane_off + C::DP_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(&sw[32]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bb.ds_ready);
+      if (!ok) break;
     }
     if (ok) ok = __all_sync(FULL, wait(bb.acc_done, 0));
     if (ok) {
@@ -551,15 +629,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t v_addr = sbase + (TV + st) * C::TILE_BYTES;
         if (!wait(&bb.kv_full[st], jt >> 1)) { ok = false; break; }
         tc_fence_after();
-        // S = Q K^T and dP = dO V^T (queries as rows).
-        mma_kmajor<D>(tmem + C::S_COL, q_desc, smem_desc_sw128(k_addr, 16, 1024));
-        mma_kmajor<D>(tmem + C::DP_COL, do_desc, smem_desc_sw128(v_addr, 16, 1024));
-        mma_commit(bb.s_full);
-        // dQ += dS K once dS is in TMEM.
-        if (!wait(bb.ds_ready, jt)) { ok = false; break; }
-        tc_fence_after();
-        mma_tmem_a<D>(tmem + C::ACC0_COL, tmem + C::DP_COL,
-                      smem_desc_sw128(k_addr, C::BLOCK_BYTES, 1024), jt > 0);
+        // S = Q K^T and dP = dO V^T (queries as rows), key half by half:
+        // columns h * 64.. of S and dP.
+        const uint64_t k_k = smem_desc_sw128(k_addr, 16, 1024);
+        const uint64_t v_k = smem_desc_sw128(v_addr, 16, 1024);
+        for (int hh = 0; hh < 2; ++hh) {
+          mma_kmajor_half<D>(tmem + C::S_COL + hh * H, q_desc, k_k + hh * kHalfStep);
+          mma_commit(&bb.s_full[hh]);
+          mma_kmajor_half<D>(tmem + C::DP_COL + hh * H, do_desc, v_k + hh * kHalfStep);
+          mma_commit(&bb.dp_full[hh]);
+        }
+        // dQ += dS K, half by half as dS arrives (dS of half h in columns
+        // DP_COL + h * 32.. as bf16 pairs; K rows h * 64..).
+        const uint64_t k_mn = smem_desc_sw128(k_addr, C::BLOCK_BYTES, 1024);
+        for (int hh = 0; ok && hh < 2; ++hh) {
+          if (!wait(&bb.ds_ready[hh], jt)) { ok = false; break; }
+          tc_fence_after();
+          mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + C::DP_COL + hh * (H / 2),
+                             k_mn + hh * kHalfStep, jt > 0 || hh > 0);
+        }
+        if (!ok) break;
         mma_commit(&bb.kv_empty[st]);  // K and V of this stage may be refilled
       }
       if (ok) mma_commit(bb.acc_done);
@@ -586,39 +675,48 @@ __global__ void __launch_bounds__(THREADS, 1)
       drow = dd[static_cast<size_t>(bhq) * Lq + qrow];
     }
     bool ok = true;
-    for (int jt = 0; jt < n_iter; ++jt) {
-      ok = __all_sync(FULL, wait(bb.s_full, jt));
-      if (!ok) break;
-      tc_fence_after();
+    for (int jt = 0; ok && jt < n_iter; ++jt) {
       // Keys past Lk, and past the query under the causal rule, get P = 0.
       const int kmax = causal ? min(Lk - 1, qrow) : Lk - 1;
-      uint32_t sw[64];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + C::S_COL + q4 * 32, sr);
-        tmem_ld32(tmem + lane_off + C::DP_COL + q4 * 32, dr);
+      for (int hh = 0; ok && hh < 2; ++hh) {
+        ok = __all_sync(FULL, wait(&bb.s_full[hh], jt)) &&
+             __all_sync(FULL, wait(&bb.dp_full[hh], jt));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[2][32], dr[2][32];
+        tmem_ld32(tmem + lane_off + C::S_COL + hh * H, sr[0]);
+        tmem_ld32(tmem + lane_off + C::S_COL + hh * H + 32, sr[1]);
+        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H, dr[0]);
+        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H + 32, dr[1]);
         tmem_ld_wait();
+        uint32_t sw[32];
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nl2 = make_float2(-l2, -l2), nd2 = make_float2(-drow, -drow);
+        const float2 zero2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int key = jt * T + q4 * 32 + e;
-          float p0 = ex2(__uint_as_float(sr[e]) * scale_log2 - l2);
-          float p1 = ex2(__uint_as_float(sr[e + 1]) * scale_log2 - l2);
-          if (key > kmax) p0 = 0.f;
-          if (key + 1 > kmax) p1 = 0.f;
+        for (int e = 0; e < H; e += 2) {
+          const int key = jt * T + hh * H + e;
+          float2 p = ffma2(make_float2(__uint_as_float(sr[e >> 5][e & 31]),
+                                       __uint_as_float(sr[e >> 5][(e & 31) + 1])),
+                           sc2, nl2);
+          p.x = key > kmax ? 0.f : ex2(p.x);
+          p.y = key + 1 > kmax ? 0.f : ex2(p.y);
           // P is rounded to bf16 as in the forward's P V product and in bwd_dkdv.
-          const uint32_t pw = attn::pack_bf16x2(p0, p1);
-          const float s0 = attn::bf16_lo(pw) * (__uint_as_float(dr[e]) - drow);
-          const float s1 = attn::bf16_hi(pw) * (__uint_as_float(dr[e + 1]) - drow);
-          sw[(q4 * 32 + e) >> 1] = attn::pack_bf16x2(s0, s1);
+          const uint32_t pw = attn::pack_bf16x2(p.x, p.y);
+          const float2 x = fadd2(make_float2(__uint_as_float(dr[e >> 5][e & 31]),
+                                             __uint_as_float(dr[e >> 5][(e & 31) + 1])),
+                                 nd2);
+          const float2 ds2 = ffma2(make_float2(attn::bf16_lo(pw), attn::bf16_hi(pw)), x, zero2);
+          sw[e >> 1] = attn::pack_bf16x2(ds2.x, ds2.y);
         }
+        // Over dP columns this thread has already read (half 1 lands on
+        // half 0's dP columns).
+        tmem_st32(tmem + lane_off + C::DP_COL + hh * (H / 2), sw);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bb.ds_ready[hh]);
       }
-      tmem_st32(tmem + lane_off + C::DP_COL, *reinterpret_cast<uint32_t(*)[32]>(&sw[0]));
-      tmem_st32(tmem + lane_off + C::DP_COL + 32, *reinterpret_cast<uint32_t(*)[32]>(&sw[32]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bb.ds_ready);
     }
     if (ok) ok = __all_sync(FULL, wait(bb.acc_done, 0));
     if (ok) {
