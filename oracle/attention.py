@@ -618,3 +618,46 @@ def plan_splits(seq_lens, num_kv_heads, slots, page_size, num_splits=0):
                 lo = mid + 1
         best_c = hi * page_size
     return [best_c] * bsz, [max(1, _cdiv(n, best_c)) for n in lens]
+
+
+def plan_balanced(seq_lens, num_groups, num_ctas, page_size, unit_cost=lambda n: n):
+    """Load-balanced split schedule for decode ([Lecture 4] section 5.6).
+
+    Follows the section's steps for decode (one query row per request, so
+    ceil(l_qo / T_q) = 1):
+      2. L_kv = ceil(sum_b l_kv(b) * num_groups / num_ctas), here rounded up
+         to a multiple of page_size (a segment starts on a page);
+      3. the KV of every (request, group) is cut into consecutive segments of
+         at most L_kv tokens, each a work unit (a request of length 0 keeps
+         one empty unit, so that its output is written);
+      4. units are sorted by cost (unit_cost(tokens), 1. in the section:
+         alpha l_q + beta l_kv with l_q = 1 fixed) from large to small, ties
+         in list order, and each goes to the CTA with the smallest total cost
+         so far (lowest index on ties): longest processing time first;
+      5. the units of one (request, group), in token order, are what the
+         merge combines.
+    Returns (units, cta_units): units[u] = (b, group, t_begin, t_end) in
+    list order (request, group, segment), cta_units[c] = the unit ids of CTA
+    c in the order they were assigned.
+    """
+    import heapq
+    lens = [max(0, int(x)) for x in seq_lens]
+    total = sum(lens) * num_groups
+    lkv = max(1, -(-total // num_ctas))
+    lkv = -(-lkv // page_size) * page_size
+    units = []
+    for b, n in enumerate(lens):
+        for grp in range(num_groups):
+            if n == 0:
+                units.append((b, grp, 0, 0))
+            for t0 in range(0, n, lkv):
+                units.append((b, grp, t0, min(n, t0 + lkv)))
+    order = sorted(range(len(units)), key=lambda u: (-unit_cost(units[u][3] - units[u][2]), u))
+    heap = [(0, c) for c in range(num_ctas)]
+    cta_units = [[] for _ in range(num_ctas)]
+    for u in order:
+        load, c = heapq.heappop(heap)
+        cta_units[c].append(u)
+        heapq.heappush(heap, (load + unit_cost(units[u][3] - units[u][2]), c))
+    return units, cta_units
+

@@ -629,3 +629,55 @@ def test_backward_closed_forms():
     # no keys at all: every row sees nothing, so every gradient is zero
     dq, dk, dv, _ = orc.attention_backward(q, k[:0], v[:0], do, 0.5, False)
     assert (dq == 0).all() and dk.shape == (0, 4) and dv.shape == (0, 4)
+
+
+# ---------------------------------------------------------------- load-balanced schedule
+
+def test_balanced_plan_segments_lecture_5_6():
+    """Steps 2-3 of [Lecture 4] section 5.6 on a hand example: L_kv =
+    ceil(150 / 4) = 38 tokens, on a 16-token page grid 48; every request is
+    cut into consecutive segments of at most 48 tokens."""
+    units, cta_units = orc.plan_balanced([100, 50, 0], 1, 4, 16)
+    assert units == [(0, 0, 0, 48), (0, 0, 48, 96), (0, 0, 96, 100), (1, 0, 0, 48),
+                     (1, 0, 48, 50), (2, 0, 0, 0)]
+    assert sorted(u for c in cta_units for u in c) == list(range(len(units)))
+
+
+def test_balanced_plan_covers_every_token_once():
+    rng = np.random.default_rng(41)
+    for _ in range(100):
+        lens = rng.integers(0, 20000, size=int(rng.integers(1, 9))).tolist()
+        groups, ctas = int(rng.choice([1, 2, 8])), int(rng.choice([4, 132, 456]))
+        units, cta_units = orc.plan_balanced(lens, groups, ctas, 16)
+        lkv = -(-max(1, -(-sum(lens) * groups // ctas)) // 16) * 16
+        for b, n in enumerate(lens):
+            for grp in range(groups):
+                segs = [u for u in units if u[0] == b and u[1] == grp]
+                assert segs[0][2] == 0 and segs[-1][3] == n
+                for a, c in zip(segs, segs[1:]):
+                    assert a[3] == c[2]
+                assert all(u[2] % 16 == 0 and u[3] - u[2] <= lkv for u in segs)
+        assert sorted(u for c in cta_units for u in c) == list(range(len(units)))
+
+
+def test_balanced_plan_lpt_bound_against_brute_force():
+    """Step 4 is the longest-processing-time greedy: on tiny instances its
+    makespan stays within Graham's bound (4/3 - 1/(3m)) of the optimum found
+    by trying every assignment."""
+    import itertools
+    rng = np.random.default_rng(42)
+    for _ in range(40):
+        lens = rng.integers(1, 200, size=int(rng.integers(2, 5))).tolist()
+        m = int(rng.integers(2, 4))
+        units, cta_units = orc.plan_balanced(lens, 1, m, 16, unit_cost=lambda n: n)
+        if len(units) > 8:
+            continue
+        cost = [u[3] - u[2] for u in units]
+        span = max(sum(cost[u] for u in c) for c in cta_units)
+        best = min(max(sum(cost[u] for u, a in zip(range(len(cost)), assign) if a == k)
+                       for k in range(m))
+                   for assign in itertools.product(range(m), repeat=len(cost)))
+        assert span <= (4 / 3 - 1 / (3 * m)) * best + 1e-9
+        # each CTA received its units from the longest down
+        for c in cta_units:
+            assert all(cost[a] >= cost[b] for a, b in zip(c, c[1:]))
