@@ -33,6 +33,11 @@ SIGNATURES = {
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ,
                       _I, _P]),
+    "attn_decode_sched_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "attn_decode_schedule": (_I, [_P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "attn_decode_schedule_host": (_I, [_P, _I, _I, _I, _I, _I, _P, _SZ]),
+    "attn_decode_paged_balanced": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F,
+                                        _I, _P, _SZ, _I, _P]),
     "attn_decode_plan": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F,
@@ -207,6 +212,55 @@ def attn_bwd(q, k, v, o, lse, d_o, causal=False, scale=None, dq=None, dk=None, d
                         _stream(stream))
     _check(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_decode_schedule(seq_lens_host, num_heads, num_kv_heads, workspace, page_size=16,
+                         num_ctas=0, stream=None):
+    """Load-balanced plan for attn_decode_paged_balanced, written into `workspace`."""
+    lens = (ctypes.c_int32 * len(seq_lens_host))(*[int(x) for x in seq_lens_host])
+    st = lib().attn_decode_schedule(ctypes.cast(lens, ctypes.c_void_p), len(seq_lens_host),
+                                    int(num_heads), int(num_kv_heads), int(page_size),
+                                    int(num_ctas), _ptr(workspace), workspace.numel(),
+                                    _stream(stream))
+    _check(st, "attn_decode_schedule")
+
+
+def attn_decode_schedule_host(seq_lens_host, num_heads, num_kv_heads, num_ctas, page_size=16):
+    """The same plan on the host: a list of int32 (layout documented in attn.h / api.cpp)."""
+    B = len(seq_lens_host)
+    G = num_kv_heads * ((num_heads // num_kv_heads + 3) // 4)
+    U = num_ctas + B * G
+    n = 1 + (num_ctas + 1) + U + 4 * U + (B * G + 1) + U
+    lens = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens_host])
+    out = (ctypes.c_int32 * n)()
+    st = lib().attn_decode_schedule_host(ctypes.cast(lens, ctypes.c_void_p), B, int(num_heads),
+                                         int(num_kv_heads), int(page_size), int(num_ctas),
+                                         ctypes.cast(out, ctypes.c_void_p), n)
+    _check(st, "attn_decode_schedule_host")
+    return list(out)
+
+
+def attn_decode_paged_balanced(q, k_pages, v_pages, block_table, seq_lens, workspace, out=None,
+                               lse=None, want_lse=True, scale=None, num_ctas=0, stream=None):
+    """Fixed-grid decode following the plan in `workspace` (attn_decode_schedule)."""
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"),
+                 (block_table, "block_table"), (seq_lens, "seq_lens"), (workspace, "workspace")):
+        _need(t, n)
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    st = lib().attn_decode_paged_balanced(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                          _ptr(seq_lens), page_size, _ptr(out), _ptr(lse), B, Hq,
+                                          Hkv, d, block_table.shape[1], num_pages, float(scale),
+                                          int(num_ctas), _ptr(workspace), workspace.numel(),
+                                          _dtype_code(q), _stream(stream))
+    _check(st, "attn_decode_paged_balanced")
+    return out, lse
 
 
 def attn_decode_plan(seq_lens_host, num_kv_heads, page_size=16, num_splits=0, slots=0):

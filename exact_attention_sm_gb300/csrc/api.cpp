@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <functional>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "attn.h"
@@ -32,6 +33,12 @@ attn_status_t launch_decode_bf16(const void*, const void*, const void*, const in
 attn_status_t launch_bwd_bf16(const void*, const void*, const void*, const void*, const float*,
                               const void*, void*, void*, void*, float*, int, int, int, int, int,
                               int, int, float, cudaStream_t);
+int decode_balanced_ctas_per_sm();
+attn_status_t launch_decode_balanced(const void*, const void*, const void*, const int32_t*,
+                                     const int32_t*, const int32_t*, const int32_t*,
+                                     const int32_t*, const int32_t*, const int32_t*, int, int, float*,
+                                     float*, void*, float*, int, int, int, int, int, int, int,
+                                     float, cudaStream_t);
 attn_status_t launch_merge(const float*, const float*, int, int, int, void*, float*, attn_dtype_t,
                            cudaStream_t);
 attn_status_t launch_cascade_gather_q(const void*, void*, int, int, int, int, cudaStream_t);
@@ -109,6 +116,104 @@ void plan_cached(const int32_t* lens, int B, int Hkv, int page, int num_splits, 
   cache.slots = slots;
   cache.chunk = *chunk;
   cache.max_splits = *max_splits;
+}
+
+// ---------------------------------------------------------------------------
+// Load-balanced decode schedule ("Lecture 4" section 5.6; the reading is in
+// attn.h).  Plan layout in the workspace (int32, then the fp32 partials):
+//   [0] number of units
+//   cta_off[num_ctas + 1], cta_units[U], unit[U][4] (request, group, t_begin,
+//   t_end), seg_off[B * G + 1], seg_units[U]
+// with G = Hkv * ceil((Hq / Hkv) / 4) head groups and U = num_ctas + B * G,
+// the most units any lengths can produce, so the layout (and a captured
+// graph) only depends on (B, Hq, Hkv, num_ctas).
+constexpr int kHeadsPerCta = 4;
+
+struct BalancedLayout {
+  int G, U;
+  size_t cta_off, cta_units, unit, seg_off, seg_units, ints;  // int32 offsets
+  size_t part_o, part_lse, total;                           // byte offsets
+};
+
+BalancedLayout balanced_layout(int B, int Hq, int Hkv, int d, int num_ctas) {
+  BalancedLayout L;
+  L.G = Hkv * ((Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta);
+  L.U = num_ctas + B * L.G;
+  L.cta_off = 1;
+  L.cta_units = L.cta_off + num_ctas + 1;
+  L.unit = L.cta_units + L.U;
+  L.seg_off = L.unit + 4 * static_cast<size_t>(L.U);
+  L.seg_units = L.seg_off + static_cast<size_t>(B) * L.G + 1;
+  L.ints = L.seg_units + L.U;
+  L.part_o = round_up(L.ints * sizeof(int32_t), kAlign);
+  L.part_lse = L.part_o + round_up(static_cast<size_t>(L.U) * kHeadsPerCta * d * sizeof(float), kAlign);
+  L.total = L.part_lse + round_up(static_cast<size_t>(L.U) * kHeadsPerCta * sizeof(float), kAlign);
+  return L;
+}
+
+// Steps 2-5 of the section: L_kv from the total work, page-aligned segments
+// of at most L_kv tokens per (request, group) (an empty request keeps one
+// empty unit), units sorted by token count from large to small (ties in
+// list order) and each given to the least-loaded CTA (lowest index on ties).
+void plan_balanced(const int32_t* lens, int B, int G, int num_ctas, int page,
+                   const BalancedLayout& L, int32_t* out) {
+  int64_t total = 0;
+  for (int b = 0; b < B; ++b) total += std::max<int32_t>(lens[b], 0);
+  total *= G;
+  int64_t lkv = std::max<int64_t>(1, cdiv(total, num_ctas));
+  lkv = cdiv(lkv, page) * page;
+  struct U4 {
+    int32_t b, g, t0, t1;
+  };
+  std::vector<U4> units;
+  std::vector<int32_t> seg_off(static_cast<size_t>(B) * G + 1, 0);
+  for (int b = 0; b < B; ++b) {
+    const int64_t n = std::max<int32_t>(lens[b], 0);
+    for (int g = 0; g < G; ++g) {
+      if (n == 0) units.push_back({b, g, 0, 0});
+      for (int64_t t0 = 0; t0 < n; t0 += lkv)
+        units.push_back({b, g, static_cast<int32_t>(t0), static_cast<int32_t>(std::min(n, t0 + lkv))});
+      seg_off[static_cast<size_t>(b) * G + g + 1] = static_cast<int32_t>(units.size());
+    }
+  }
+  const int nu = static_cast<int>(units.size());
+  std::vector<int32_t> order(nu);
+  for (int u = 0; u < nu; ++u) order[u] = u;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t c) {
+    return units[a].t1 - units[a].t0 > units[c].t1 - units[c].t0;
+  });
+  std::priority_queue<std::pair<int64_t, int>, std::vector<std::pair<int64_t, int>>,
+                      std::greater<std::pair<int64_t, int>>>
+      heap;
+  for (int c = 0; c < num_ctas; ++c) heap.push({0, c});
+  std::vector<std::vector<int32_t>> per(num_ctas);
+  for (int32_t u : order) {
+    const auto top = heap.top();
+    heap.pop();
+    per[top.second].push_back(u);
+    heap.push({top.first + (units[u].t1 - units[u].t0), top.second});
+  }
+  out[0] = nu;
+  int32_t k = 0;
+  for (int c = 0; c < num_ctas; ++c) {
+    out[L.cta_off + c] = k;
+    for (int32_t u : per[c]) out[L.cta_units + k++] = u;
+  }
+  out[L.cta_off + num_ctas] = k;
+  for (int u = 0; u < nu; ++u) {
+    out[L.unit + 4 * u + 0] = units[u].b;
+    out[L.unit + 4 * u + 1] = units[u].g;
+    out[L.unit + 4 * u + 2] = units[u].t0;
+    out[L.unit + 4 * u + 3] = units[u].t1;
+  }
+  for (size_t i = 0; i < seg_off.size(); ++i) out[L.seg_off + i] = seg_off[i];
+  for (int u = 0; u < nu; ++u) out[L.seg_units + u] = u;  // list order is token order
+}
+
+int balanced_ctas(int num_ctas) {
+  if (num_ctas > 0) return num_ctas;
+  const int sms = attn_host::num_sms();
+  return sms <= 0 ? -1 : sms * attn_host::decode_balanced_ctas_per_sm();
 }
 
 }  // namespace
@@ -212,6 +317,80 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void*
       q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_k, o, lse, B, max_seqlen_q,
       std::max(max_seqlen_k, 1), total_q, Hq, Hkv, d, max_pages_per_seq, num_pages,
       causal ? 1 : 0, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_decode_sched_workspace_bytes(int B, int Hq, int Hkv, int d, int num_ctas) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 0;
+  const int ctas = balanced_ctas(num_ctas);
+  if (ctas <= 0) return 0;
+  return balanced_layout(B, Hq, Hkv, d, ctas).total;
+}
+
+attn_status_t attn_decode_schedule_host(const int32_t* seq_lens_host, int B, int Hq, int Hkv,
+                                        int page_size, int num_ctas, int32_t* plan_out,
+                                        size_t plan_ints) {
+  if (!seq_lens_host || !plan_out || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 ||
+      page_size <= 0 || num_ctas <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  const BalancedLayout L = balanced_layout(B, Hq, Hkv, 128, num_ctas);
+  if (plan_ints < L.ints) return ATTN_ERR_WORKSPACE;
+  plan_balanced(seq_lens_host, B, L.G, num_ctas, page_size, L, plan_out);
+  return ATTN_OK;
+}
+
+attn_status_t attn_decode_schedule(const int32_t* seq_lens_host, int B, int Hq, int Hkv,
+                                   int page_size, int num_ctas, void* workspace,
+                                   size_t workspace_bytes, attn_stream_t stream) {
+  if (!seq_lens_host || B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens_host[b] < 0) return ATTN_ERR_INVALID_ARG;
+  const int ctas = balanced_ctas(num_ctas);
+  if (ctas <= 0) return ATTN_ERR_CUDA;
+  const BalancedLayout L = balanced_layout(B, Hq, Hkv, 128, ctas);
+  if (workspace == nullptr || workspace_bytes < L.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+    return ATTN_ERR_WORKSPACE;
+  thread_local std::vector<int32_t> host;
+  host.assign(L.ints, 0);
+  plan_balanced(seq_lens_host, B, L.G, ctas, page_size, L, host.data());
+  // From pageable memory: the copy is staged before the call returns, so the
+  // host vector may be reused right away.
+  return cudaMemcpyAsync(workspace, host.data(), L.ints * sizeof(int32_t), cudaMemcpyHostToDevice,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_decode_paged_balanced(const void* q, const void* k_pages, const void* v_pages,
+                                         const int32_t* block_table, const int32_t* seq_lens,
+                                         int page_size, void* o, float* lse, int B, int Hq,
+                                         int Hkv, int d, int max_pages_per_seq, int num_pages,
+                                         float scale, int num_ctas, void* workspace,
+                                         size_t workspace_bytes, attn_dtype_t dtype,
+                                         attn_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128 || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o))
+    return ATTN_ERR_INVALID_ARG;
+  const int ctas = balanced_ctas(num_ctas);
+  if (ctas <= 0) return ATTN_ERR_CUDA;
+  const BalancedLayout L = balanced_layout(B, Hq, Hkv, d, ctas);
+  if (workspace == nullptr || workspace_bytes < L.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+    return ATTN_ERR_WORKSPACE;
+  const int32_t* plan = static_cast<const int32_t*>(workspace);
+  char* ws = static_cast<char*>(workspace);
+  return attn_host::launch_decode_balanced(
+      q, k_pages, v_pages, block_table, seq_lens, plan + L.cta_off, plan + L.cta_units,
+      plan + L.unit, plan + L.seg_off, plan + L.seg_units, ctas, L.U,
+      reinterpret_cast<float*>(ws + L.part_o), reinterpret_cast<float*>(ws + L.part_lse), o, lse, B,
+      Hq, Hkv, d, page_size, max_pages_per_seq, num_pages, scale,
+      reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Lq) {

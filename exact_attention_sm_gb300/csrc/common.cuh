@@ -74,6 +74,15 @@ attn_status_t launch_bwd_bf16(const void* q, const void* k, const void* v, const
                               const float* lse, const void* d_o, void* dq, void* dk, void* dv,
                               float* dd, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                               float scale, cudaStream_t stream);
+int decode_balanced_ctas_per_sm();
+attn_status_t launch_decode_balanced(const void* q, const void* k_pages, const void* v_pages,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     const int32_t* cta_off, const int32_t* cta_units,
+                                     const int32_t* unit, const int32_t* seg_off,
+                                     const int32_t* seg_units, int num_ctas, int U, float* part_o,
+                                     float* part_lse, void* o, float* lse, int B, int Hq, int Hkv,
+                                     int d, int page_size, int max_pages, int num_pages,
+                                     float scale, cudaStream_t stream);
 attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int rows, int S, int d,
                            void* o_out, float* lse_out, attn_dtype_t out_dtype, cudaStream_t stream);
 attn_status_t launch_cascade_gather_q(const void* q, void* q_stack, int B, int Hq, int Hkv, int d,

@@ -104,6 +104,106 @@ struct SegMap {
   int off[kSegMapMax + 1];
 };
 
+// One page of K and V (16 tokens, the first `valid` of them live) against
+// the query rows in qw: scores, online softmax in base 2 and P V into the
+// lane's accumulators (lane layout as described at the top of the file).
+__device__ __forceinline__ void consume_page(const uint8_t* kst, const uint8_t* vst, int valid,
+                                             const uint32_t (&qw)[HG][8], float (&acc)[HG][16],
+                                             float (&m_run)[HG], float& l_own, float scale_log2,
+                                             int lane, int grp, int l8, int own_h) {
+
+    // Partial dots of this lane's 16 dims: value index x = h * 4 + tt.
+    float part[HG * 4];
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      const int slot = grp + 4 * tt;
+      const uint4 k0 = *reinterpret_cast<const uint4*>(kst + slot * 256);
+      const uint4 k1 = *reinterpret_cast<const uint4*>(kst + slot * 256 + 16);
+      const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          a0 = fma_bf16_lo(qw[h][w], kw[w], a0);
+          a1 = fma_bf16_hi(qw[h][w], kw[w], a1);
+        }
+        part[h * 4 + tt] = a0 + a1;
+      }
+    }
+    // Transposed butterfly over the 8 lanes of the group (bits 2, 1, 0).
+    {
+      int n = HG * 4;
+#pragma unroll
+      for (int bit = 2; bit >= 0; --bit) {
+        const bool upper = (l8 >> bit) & 1;
+#pragma unroll
+        for (int x = 0; x < HG * 2; ++x) {
+          if (x < n / 2) {
+            const float send = upper ? part[x] : part[x + n / 2];
+            const float keep = upper ? part[x + n / 2] : part[x];
+            part[x] = keep + __shfl_xor_sync(FULL, send, 1 << bit);
+          }
+        }
+        n /= 2;
+      }
+    }
+    // Lane now holds x = 2 * l8 + e (e = 0, 1): head l8 / 2, tokens 2 (l8 & 1) + e.
+    float sv[2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int tt = 2 * (l8 & 1) + e;
+      sv[e] = (grp + 4 * tt < valid) ? part[e] * scale_log2 : -INFINITY;
+      mx = fmaxf(mx, sv[e]);
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+    float m_own = 0.f;
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      const float pm = __shfl_sync(FULL, mx, 2 * h);
+      if (pm > m_run[h] + kRescaleThreshold) {  // warp-uniform
+        const float alpha = ex2(m_run[h] - pm);  // 0 on the first page (m_run = -inf)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[h][j] *= alpha;
+        if (h == own_h) l_own *= alpha;
+        m_run[h] = pm;
+      }
+      if (h == own_h) m_own = m_run[h];
+    }
+    const float p0 = ex2(sv[0] - m_own), p1 = ex2(sv[1] - m_own);
+    l_own += p0 + p1;
+    const uint32_t pw = attn::pack_bf16x2(p0, p1);
+
+#pragma unroll
+    for (int tp = 0; tp < 2; ++tp) {        // token pair (tokens 2tp, 2tp+1)
+      uint32_t ph[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) ph[h] = __shfl_sync(FULL, pw, (lane & ~7) | (2 * h + tp));
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tt = 2 * tp + e;
+        const int slot = grp + 4 * tt;
+        uint4 v0 = *reinterpret_cast<const uint4*>(vst + slot * 256);
+        uint4 v1 = *reinterpret_cast<const uint4*>(vst + slot * 256 + 16);
+        if (slot >= valid) {  // rows past the segment may hold anything
+          v0 = make_uint4(0u, 0u, 0u, 0u);
+          v1 = v0;
+        }
+        const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int h = 0; h < HG; ++h)
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            if (e == 0) fma_plo_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
+            else fma_phi_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
+          }
+      }
+    }
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 3)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -242,99 +342,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
       if (!ok) break;
       if (!skip[st]) {
         const uint8_t* kst = ring + st * STAGE_BYTES + l8 * 32;
-        const uint8_t* vst = kst + PAGE_BYTES;
-        const int valid = t_end - (p_begin + i) * PAGE;  // slots < valid hold tokens (>= 1)
-
-        // Partial dots of this lane's 16 dims: value index x = h * 4 + tt.
-        float part[HG * 4];
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          const int slot = grp + 4 * tt;
-          const uint4 k0 = *reinterpret_cast<const uint4*>(kst + slot * 256);
-          const uint4 k1 = *reinterpret_cast<const uint4*>(kst + slot * 256 + 16);
-          const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-#pragma unroll
-          for (int h = 0; h < HG; ++h) {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              a0 = fma_bf16_lo(qw[h][w], kw[w], a0);
-              a1 = fma_bf16_hi(qw[h][w], kw[w], a1);
-            }
-            part[h * 4 + tt] = a0 + a1;
-          }
-        }
-        // Transposed butterfly over the 8 lanes of the group (bits 2, 1, 0).
-        {
-          int n = HG * 4;
-#pragma unroll
-          for (int bit = 2; bit >= 0; --bit) {
-            const bool upper = (l8 >> bit) & 1;
-#pragma unroll
-            for (int x = 0; x < HG * 2; ++x) {
-              if (x < n / 2) {
-                const float send = upper ? part[x] : part[x + n / 2];
-                const float keep = upper ? part[x + n / 2] : part[x];
-                part[x] = keep + __shfl_xor_sync(FULL, send, 1 << bit);
-              }
-            }
-            n /= 2;
-          }
-        }
-        // Lane now holds x = 2 * l8 + e (e = 0, 1): head l8 / 2, tokens 2 (l8 & 1) + e.
-        float sv[2];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tt = 2 * (l8 & 1) + e;
-          sv[e] = (grp + 4 * tt < valid) ? part[e] * scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sv[e]);
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
-        float m_own = 0.f;
-#pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const float pm = __shfl_sync(FULL, mx, 2 * h);
-          if (pm > m_run[h] + kRescaleThreshold) {  // warp-uniform
-            const float alpha = ex2(m_run[h] - pm);  // 0 on the first page (m_run = -inf)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[h][j] *= alpha;
-            if (h == own_h) l_own *= alpha;
-            m_run[h] = pm;
-          }
-          if (h == own_h) m_own = m_run[h];
-        }
-        const float p0 = ex2(sv[0] - m_own), p1 = ex2(sv[1] - m_own);
-        l_own += p0 + p1;
-        const uint32_t pw = attn::pack_bf16x2(p0, p1);
-
-#pragma unroll
-        for (int tp = 0; tp < 2; ++tp) {        // token pair (tokens 2tp, 2tp+1)
-          uint32_t ph[HG];
-#pragma unroll
-          for (int h = 0; h < HG; ++h) ph[h] = __shfl_sync(FULL, pw, (lane & ~7) | (2 * h + tp));
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tt = 2 * tp + e;
-            const int slot = grp + 4 * tt;
-            uint4 v0 = *reinterpret_cast<const uint4*>(vst + slot * 256);
-            uint4 v1 = *reinterpret_cast<const uint4*>(vst + slot * 256 + 16);
-            if (slot >= valid) {  // rows past the segment may hold anything
-              v0 = make_uint4(0u, 0u, 0u, 0u);
-              v1 = v0;
-            }
-            const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-            for (int h = 0; h < HG; ++h)
-#pragma unroll
-              for (int w = 0; w < 8; ++w) {
-                if (e == 0) fma_plo_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
-                else fma_phi_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
-              }
-          }
-        }
+        consume_page(kst, kst + PAGE_BYTES, t_end - (p_begin + i) * PAGE, qw, acc, m_run, l_own,
+                     scale_log2, lane, grp, l8, own_h);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
@@ -412,6 +421,329 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Load-balanced decode with a fixed grid ("Lecture 4" section 5.6).  The host
+// schedule (attn_decode_schedule) cuts every (request, KV-head group) into
+// page-aligned segments of at most L_kv tokens and deals them to num_ctas
+// CTAs, longest first; the plan sits in a device workspace, so the grid and
+// every pointer stay the same from one decode step to the next and one
+// captured CUDA graph can replay them all while the plan changes.  A CTA
+// walks its segments with the ring position, the page counter and the
+// barrier phases running on across segments (no pipeline drain between
+// them) and writes every segment as a normalised partial state;
+// decode_merge_kernel combines the segments of each output row in token
+// order.
+struct BalancedPlan {
+  const int* cta_off;    // [num_ctas + 1]: the CTA's entries in cta_units
+  const int* cta_units;  // unit ids, per CTA in the order they were assigned
+  const int* unit;       // [units][4]: request, group, t_begin, t_end
+  const int* seg_off;    // [B * G + 1]: the (request, group)'s entries in seg_units
+  const int* seg_units;  // unit ids of each (request, group) in token order
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 3)
+    decode_balanced_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __nv_bfloat16* __restrict__ q,
+                           const int32_t* __restrict__ block_table,
+                           const int32_t* __restrict__ seq_lens, const BalancedPlan plan,
+                           float* __restrict__ part_o, float* __restrict__ part_lse, int B,
+                           int Hq, int Hkv, int U, int max_pages, int num_pages, float scale_log2,
+                           int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* ring = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  __shared__ uint64_t full[NST], empty[NST], st_ready, st_free;
+  __shared__ int skip[NST];
+  __shared__ float sm_m[NCW][HG];
+  __shared__ float sm_l[NCW][HG];
+  __shared__ __align__(16) float sm_acc[NCW][HG][D];
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
+
+  const int group = Hq / Hkv;
+  const int gpk = (group + HG - 1) / HG;  // head groups per KV head
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The plan is checked before use: an entry out of range is reported
+  // (ATTN_ERR_BAD_INDEX) and skipped, so a damaged plan never reads or
+  // writes outside the plan, the partial states or the block table.
+  int k0 = plan.cta_off[blockIdx.x];
+  int n_units = plan.cta_off[blockIdx.x + 1] - k0;
+  if (k0 < 0 || n_units < 0 || k0 + n_units > U) {
+    if (threadIdx.x == 0) attn::record_status(status, ATTN_ERR_BAD_INDEX);
+    k0 = 0;
+    n_units = 0;
+  }
+  struct Seg {
+    int u, b, grp, t_begin, t_end, p_begin, n_pages;  // u < 0: skipped
+  };
+  // Segment k of this CTA.  Its bounds are clamped to the request's device
+  // length and to the block table's capacity (reported), so a stale plan
+  // never reads past either.
+  auto seg_at = [&](int k) {
+    Seg sg;
+    sg.u = plan.cta_units[k0 + k];
+    sg.n_pages = 0;
+    sg.t_begin = sg.t_end = sg.p_begin = 0;
+    if (sg.u < 0 || sg.u >= U) {
+      if (threadIdx.x == 0) attn::record_status(status, ATTN_ERR_BAD_INDEX);
+      sg.u = -1;
+      return sg;
+    }
+    const int* e = plan.unit + 4 * sg.u;
+    sg.b = e[0];
+    sg.grp = e[1];
+    if (sg.b < 0 || sg.b >= B || sg.grp < 0 || sg.grp >= Hkv * gpk || e[2] < 0 || e[3] < e[2]) {
+      if (threadIdx.x == 0) attn::record_status(status, ATTN_ERR_BAD_INDEX);
+      sg.u = -1;
+      return sg;
+    }
+    int len = seq_lens[sg.b];
+    if (len < 0 || len > max_pages * PAGE) {
+      if (threadIdx.x == 0) attn::record_status(status, ATTN_ERR_BAD_INDEX);
+      len = len < 0 ? 0 : max_pages * PAGE;
+    }
+    sg.t_begin = min(e[2], len);
+    sg.t_end = min(e[3], len);
+    sg.p_begin = sg.t_begin / PAGE;
+    sg.n_pages = sg.t_end > sg.t_begin ? (sg.t_end + PAGE - 1) / PAGE - sg.p_begin : 0;
+    return sg;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&st_ready, NCW);
+    mbar_init(&st_free, NCW);
+    abort_flag_s = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    bool ok = true;
+    int gi = 0;  // pages issued over all segments (ring position)
+    for (int k = 0; ok && k < n_units; ++k) {
+      const Seg sg = seg_at(k);
+      if (sg.u < 0) continue;
+      const int kvh = sg.grp / gpk;
+      const int32_t* row = block_table + static_cast<size_t>(sg.b) * max_pages + sg.p_begin;
+      for (int i0 = 0; ok && i0 < sg.n_pages; i0 += 32) {
+        const int entry = i0 + lane < sg.n_pages ? row[i0 + lane] : 0;
+        const int cnt = min(32, sg.n_pages - i0);
+        for (int kk = 0; kk < cnt; ++kk) {
+          const int page = __shfl_sync(FULL, entry, kk);
+          const int st = gi % NST;
+          if (lane == 0) {
+            if (gi >= NST && !mbar_wait(&empty[st], ((gi / NST) + 1) & 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+            } else if (page < 0 || page >= num_pages) {
+              attn::record_status(status, ATTN_ERR_BAD_INDEX);
+              skip[st] = 1;
+              mbar_arrive(&full[st]);  // an empty page: nothing is read
+            } else {
+              skip[st] = 0;
+              uint8_t* dst = ring + st * STAGE_BYTES;
+              mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
+              tma_load_4d(dst, &tm_k, &full[st], 0, kvh, 0, page);
+              tma_load_4d(dst + PAGE_BYTES, &tm_v, &full[st], 0, kvh, 0, page);
+            }
+          }
+          ok = __shfl_sync(FULL, ok, 0);
+          if (!ok) break;
+          ++gi;
+        }
+      }
+    }
+    if (lane == 0) {
+      if (!ok) {
+        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      int no_abort = 0;
+      for (int i = gi > NST ? gi - NST : 0; i < gi; ++i)
+        mbar_wait(&full[i % NST], (i / NST) & 1, &no_abort, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int cw = warp - 1;
+    const int grp_l = lane >> 3;     // token group within the warp
+    const int l8 = lane & 7;         // owns dims [16 l8, 16 l8 + 16)
+    const int own_h = l8 >> 1;       // head of the values this lane holds after the reduction
+    const int t = threadIdx.x - 32;  // output dim in the combine step
+    bool ok = true;
+    int gbase = 0;                   // ring position of the segment's first page
+    int kc = 0;                      // segments combined so far (barrier phases)
+    for (int k = 0; ok && k < n_units; ++k) {
+      const Seg sg = seg_at(k);
+      if (sg.u < 0) continue;
+      const int kvh = sg.grp / gpk, gi_h = sg.grp % gpk;
+      const int h0 = kvh * group + gi_h * HG;
+      const int nh = min(HG, group - gi_h * HG);
+      uint32_t qw[HG][8];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        const int hq = h0 + min(h, nh - 1);  // padded heads reuse a real head's q
+        const uint4* qp =
+            reinterpret_cast<const uint4*>(q + (static_cast<size_t>(sg.b) * Hq + hq) * D + 16 * l8);
+        const uint4 a = qp[0], c = qp[1];
+        qw[h][0] = a.x; qw[h][1] = a.y; qw[h][2] = a.z; qw[h][3] = a.w;
+        qw[h][4] = c.x; qw[h][5] = c.y; qw[h][6] = c.z; qw[h][7] = c.w;
+      }
+      float acc[HG][16];
+      float m_run[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        m_run[h] = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[h][j] = 0.f;
+      }
+      float l_own = 0.f;
+      // Page i of the segment is ring entry gbase + i, taken by consumer
+      // warp (gbase + i) % NCW.
+      for (int i = ((cw - gbase) % NCW + NCW) % NCW; i < sg.n_pages; i += NCW) {
+        const int gi = gbase + i, st = gi % NST;
+        ok = __all_sync(FULL, mbar_wait(&full[st], (gi / NST) & 1, abort_flag, kWaitLimitNs));
+        if (!ok) break;
+        if (!skip[st]) {
+          const uint8_t* kst = ring + st * STAGE_BYTES + l8 * 32;
+          consume_page(kst, kst + PAGE_BYTES, sg.t_end - (sg.p_begin + i) * PAGE, qw, acc, m_run,
+                       l_own, scale_log2, lane, grp_l, l8, own_h);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      if (!ok) break;
+      gbase += sg.n_pages;
+      // Combine the 4 token groups of the warp, then the consumer warps
+      // (shared memory, reused once every warp has read the previous
+      // segment's values: st_free; all written: st_ready).
+#pragma unroll
+      for (int h = 0; h < HG; ++h)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          acc[h][j] += __shfl_xor_sync(FULL, acc[h][j], 8);
+          acc[h][j] += __shfl_xor_sync(FULL, acc[h][j], 16);
+        }
+      float lsum = l_own;
+      lsum += __shfl_xor_sync(FULL, lsum, 1);
+      lsum += __shfl_xor_sync(FULL, lsum, 8);
+      lsum += __shfl_xor_sync(FULL, lsum, 16);
+      if (kc > 0) {
+        ok = __all_sync(FULL, mbar_wait(&st_free, (kc - 1) & 1, abort_flag, kWaitLimitNs));
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        const float lh = __shfl_sync(FULL, lsum, 2 * h);
+        if (lane == 0) {
+          sm_m[cw][h] = m_run[h];
+          sm_l[cw][h] = lh;
+        }
+        if (grp_l == 0) {
+          float4* dst = reinterpret_cast<float4*>(&sm_acc[cw][h][16 * l8]);
+          dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+          dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+          dst[2] = make_float4(acc[h][8], acc[h][9], acc[h][10], acc[h][11]);
+          dst[3] = make_float4(acc[h][12], acc[h][13], acc[h][14], acc[h][15]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st_ready);
+      ok = __all_sync(FULL, mbar_wait(&st_ready, kc & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      ++kc;
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        if (h >= nh) break;
+        float big = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) big = fmaxf(big, sm_m[w][h]);
+        float lw = 0.f, ow = 0.f;
+        if (big != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < NCW; ++w) {
+            const float c = ex2(sm_m[w][h] - big);
+            lw = fmaf(c, sm_l[w][h], lw);
+            ow = fmaf(c, sm_acc[w][h][t], ow);
+          }
+        }
+        const bool empty_row = !(lw > 0.f);
+        const size_t slot = static_cast<size_t>(sg.u) * HG + h;
+        part_o[slot * D + t] = empty_row ? 0.f : ow / lw;
+        if (t == 0) part_lse[slot] = empty_row ? -INFINITY : (big + log2f(lw)) * attn::kLn2;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st_free);
+    }
+    if (!ok) {
+      if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+}
+
+// Output row r = (request b, query head hq): the partial states of its
+// (request, group) segments, merged in token order (one warp per row, lane
+// l owns dims 4l .. 4l+3; sums in a fixed order, no atomics).
+__global__ void __launch_bounds__(128)
+    decode_merge_kernel(const BalancedPlan plan, const float* __restrict__ part_o,
+                        const float* __restrict__ part_lse, int B, int Hq, int Hkv, int U,
+                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int* status) {
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= B * Hq) return;
+  const int group = Hq / Hkv, gpk = (group + HG - 1) / HG;
+  const int b = r / Hq, hq = r % Hq;
+  const int kvh = hq / group, hin = hq % group;
+  const int grp = kvh * gpk + hin / HG, h = hin % HG;
+  int s0 = plan.seg_off[b * Hkv * gpk + grp], s1 = plan.seg_off[b * Hkv * gpk + grp + 1];
+  if (s0 < 0 || s1 < s0 || s1 > U) {  // a damaged plan: reported, the row left empty
+    if (lane == 0) attn::record_status(status, ATTN_ERR_BAD_INDEX);
+    s0 = s1 = 0;
+  }
+  auto unit_of = [&](int s) {
+    const int u = plan.seg_units[s];
+    return (u >= 0 && u < U) ? u : -1;
+  };
+  float big = -INFINITY;
+  for (int s = s0 + lane; s < s1; s += 32) {
+    const int u = unit_of(s);
+    if (u >= 0) big = fmaxf(big, part_lse[static_cast<size_t>(u) * HG + h]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) big = fmaxf(big, __shfl_xor_sync(FULL, big, off));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  if (big != -INFINITY) {
+    for (int s = s0; s < s1; ++s) {
+      const int u = unit_of(s);
+      if (u < 0) continue;
+      const size_t slot = static_cast<size_t>(u) * HG + h;
+      const float ls = part_lse[slot];
+      if (ls == -INFINITY) continue;  // an empty segment: weight 0, O not read
+      const float w = expf(ls - big);
+      const float4 x = *reinterpret_cast<const float4*>(part_o + slot * D + 4 * lane);
+      wsum += w;
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
+    }
+  }
+  const bool empty = !(wsum > 0.f);
+  const float inv = empty ? 0.f : 1.f / wsum;
+  *reinterpret_cast<uint2*>(o + static_cast<size_t>(r) * D + 4 * lane) =
+      make_uint2(attn::pack_bf16x2(acc.x * inv, acc.y * inv), attn::pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (lane == 0 && lse != nullptr) lse[r] = empty ? -INFINITY : big + logf(wsum);
+}
+
 // k_pages / v_pages [num_pages, 16, Hkv, 128] bf16 as a 4-D tensor
 // {128, Hkv, 16, num_pages}; box {128, 1, 16, 1} = one page of one KV head.
 bool make_page_map(CUtensorMap* m, const void* base, int Hkv, int num_pages) {
@@ -440,9 +772,60 @@ bool set_smem_attr() {
   return true;
 }
 
+bool set_balanced_smem_attr() {
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(decode_balanced_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return false;
+    done = true;
+  }
+  return true;
+}
+
 }  // namespace
 
 namespace attn_host {
+
+int decode_balanced_ctas_per_sm() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (!set_balanced_smem_attr() ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel, NUM_THREADS,
+                                                      SMEM_BYTES) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+attn_status_t launch_decode_balanced(const void* q, const void* k_pages, const void* v_pages,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     const int32_t* cta_off, const int32_t* cta_units,
+                                     const int32_t* unit, const int32_t* seg_off,
+                                     const int32_t* seg_units, int num_ctas, int U, float* part_o,
+                                     float* part_lse, void* o, float* lse, int B, int Hq, int Hkv,
+                                     int d, int page_size, int max_pages, int num_pages,
+                                     float scale, cudaStream_t stream) {
+  if (d != D || page_size != PAGE) return ATTN_ERR_UNSUPPORTED;
+  if (!set_balanced_smem_attr()) return ATTN_ERR_CUDA;
+  CUtensorMap mk, mv;
+  if (!make_page_map(&mk, k_pages, Hkv, num_pages) || !make_page_map(&mv, v_pages, Hkv, num_pages))
+    return ATTN_ERR_CUDA;
+  const BalancedPlan plan{cta_off, cta_units, unit, seg_off, seg_units};
+  decode_balanced_kernel<<<num_ctas, NUM_THREADS, SMEM_BYTES, stream>>>(
+      mk, mv, static_cast<const __nv_bfloat16*>(q), block_table, seq_lens, plan, part_o, part_lse,
+      B, Hq, Hkv, U, max_pages, num_pages, scale * attn::kLog2e, device_status_ptr());
+  const int rows = B * Hq;
+  decode_merge_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(
+      plan, part_o, part_lse, B, Hq, Hkv, U, static_cast<__nv_bfloat16*>(o), lse,
+      device_status_ptr());
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
 int decode_ctas_per_sm() {
   static int cached[64] = {0};

@@ -232,6 +232,53 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                               attn_stream_t stream);
 
 /*
+ * Load-balanced decode with a fixed grid ("Lecture 4" section 5.6: the
+ * FlashInfer-style scheduler and its CUDA-graph workspace).
+ *
+ * attn_decode_schedule (host work plus one host-to-device copy into the
+ * workspace; not inside a stream capture): with G = Hkv * ceil((Hq/Hkv) / 4)
+ * head groups (a CTA serves up to 4 query heads of one KV head),
+ *   L_kv = ceil(ceil(sum_b len_b * G / num_ctas) / page_size) * page_size,
+ *   every (request, group) is cut into consecutive segments of at most L_kv
+ *   tokens (a request of length 0 keeps one empty segment), and the segments
+ *   are dealt longest first (ties in (request, group, segment) order) to the
+ *   CTA with the least work so far (lowest index on ties).
+ * attn_decode_paged_balanced: num_ctas persistent CTAs (the same grid for
+ *   every plan of a given (B, Hq, Hkv, num_ctas)) walk their segments and
+ *   write each as a normalised partial state; a merge kernel combines the
+ *   segments of every output row in token order (bitwise reproducible).
+ *   The plan is read from the workspace at run time, so one captured CUDA
+ *   graph of this call replays correctly after attn_decode_schedule has
+ *   written a new plan for new lengths.  Plan entries are checked on the
+ *   device (ATTN_ERR_BAD_INDEX, entry skipped), and each segment is clamped
+ *   to the device seq_lens and the block table's capacity.
+ * attn_decode_schedule_host: the same plan into host memory (plan_ints
+ *   >= the plan's int32 count), for inspection and tests.
+ * attn_decode_sched_workspace_bytes: plan + partial states for (B, Hq, Hkv,
+ *   d, num_ctas), 256-byte aligned.
+ *
+ *   num_ctas <= 0: SM count x resident CTAs per SM of the balanced kernel.
+ *   Other arguments as attn_decode_paged (d = 128, page_size 16, bf16).
+ *   Errors: ATTN_ERR_INVALID_ARG for NULLs, bad sizes, negative lengths or
+ *   misalignment; ATTN_ERR_UNSUPPORTED for other d, page sizes or dtypes;
+ *   ATTN_ERR_WORKSPACE if the workspace is missing, short or misaligned.
+ */
+size_t attn_decode_sched_workspace_bytes(int B, int Hq, int Hkv, int d, int num_ctas);
+attn_status_t attn_decode_schedule(const int32_t* seq_lens_host, int B, int Hq, int Hkv,
+                                   int page_size, int num_ctas, void* workspace,
+                                   size_t workspace_bytes, attn_stream_t stream);
+attn_status_t attn_decode_schedule_host(const int32_t* seq_lens_host, int B, int Hq, int Hkv,
+                                        int page_size, int num_ctas, int32_t* plan_out,
+                                        size_t plan_ints);
+attn_status_t attn_decode_paged_balanced(const void* q, const void* k_pages, const void* v_pages,
+                                         const int32_t* block_table, const int32_t* seq_lens,
+                                         int page_size, void* o, float* lse, int B, int Hq,
+                                         int Hkv, int d, int max_pages_per_seq, int num_pages,
+                                         float scale, int num_ctas, void* workspace,
+                                         size_t workspace_bytes, attn_dtype_t dtype,
+                                         attn_stream_t stream);
+
+/*
  * attn_bwd - backward pass of attn_fwd (bf16), for training.
  *
  * "10.3 FlashAttention", backward and recomputation: from Q, K, V, the

@@ -265,3 +265,63 @@ def test_bwd_rejects_on_host():
     assert bwd(ws=None) == 3
     assert bwd(ws_bytes=100) == 3
     assert bwd(ws=ctypes.c_void_p(0x10010)) == 3
+
+
+def parse_balanced_plan(plan, B, G, ctas):
+    U = ctas + B * G
+    n = plan[0]
+    cta_off = plan[1:1 + ctas + 1]
+    cu0 = 1 + ctas + 1
+    cta_units = plan[cu0:cu0 + U]
+    u0 = cu0 + U
+    units = [tuple(plan[u0 + 4 * u:u0 + 4 * u + 4]) for u in range(n)]
+    per_cta = [cta_units[cta_off[c]:cta_off[c + 1]] for c in range(ctas)]
+    s0 = u0 + 4 * U
+    seg_off = plan[s0:s0 + B * G + 1]
+    return units, per_cta, seg_off
+
+
+def test_balanced_schedule_matches_oracle_bit_exact():
+    rng = np.random.default_rng(43)
+    cases = [([16384, 16384], 32, 8, 132), ([0, 5, 17], 8, 2, 10), ([1024] * 256, 32, 8, 456)]
+    for _ in range(60):
+        b = int(rng.integers(1, 9))
+        hkv = int(rng.choice([1, 2, 8]))
+        hq = hkv * int(rng.choice([1, 4, 6, 8]))
+        cases.append((rng.integers(0, 140000, size=b).tolist(), hq, hkv,
+                      int(rng.choice([8, 132, 456]))))
+    for lens, hq, hkv, ctas in cases:
+        G = hkv * ((hq // hkv + 3) // 4)
+        plan = ea.attn_decode_schedule_host(lens, hq, hkv, ctas)
+        units, per_cta, seg_off = parse_balanced_plan(plan, len(lens), G, ctas)
+        o_units, o_cta = orc.plan_balanced(lens, G, ctas, 16)
+        assert units == o_units, (lens, hq, hkv, ctas)
+        assert per_cta == o_cta
+        # the units of (request, group) i are seg_off[i] .. seg_off[i + 1] - 1, in token order
+        for i in range(len(lens) * G):
+            segs = units[seg_off[i]:seg_off[i + 1]]
+            assert all(s[:2] == (i // G, i % G) for s in segs)
+
+
+def test_balanced_rejects_on_host():
+    lens = (ctypes.c_int32 * 2)(100, 0)
+    lh = ctypes.cast(lens, ctypes.c_void_p)
+    assert ea.lib().attn_decode_schedule(None, 2, 8, 2, 16, 10, FAKE, 1 << 20, None) == 1
+    assert ea.lib().attn_decode_schedule(lh, 2, 8, 3, 16, 10, FAKE, 1 << 20, None) == 1
+    assert ea.lib().attn_decode_schedule(lh, 2, 8, 2, 16, 10, None, 0, None) == 3
+    assert ea.lib().attn_decode_schedule(lh, 2, 8, 2, 16, 10, FAKE, 64, None) == 3
+    bad = (ctypes.c_int32 * 2)(100, -1)
+    assert ea.lib().attn_decode_schedule(ctypes.cast(bad, ctypes.c_void_p), 2, 8, 2, 16, 10, FAKE,
+                                         1 << 20, None) == 1
+    bd = lambda **kw: ea.lib().attn_decode_paged_balanced(
+        kw.get("q", FAKE), FAKE, FAKE, FAKE, FAKE, kw.get("page", 16), FAKE, None, 2, 8, 2,
+        kw.get("d", 128), 7, 14, 0.1, 10, kw.get("ws", FAKE), kw.get("wsb", 1 << 20),
+        kw.get("dtype", ea.ATTN_BF16), None)
+    assert bd(q=None) == 1
+    assert bd(q=MISALIGNED) == 1
+    assert bd(d=64) == 2
+    assert bd(page=32) == 2
+    assert bd(dtype=ea.ATTN_F32) == 2
+    assert bd(ws=None) == 3
+    assert bd(wsb=100) == 3
+    assert ea.lib().attn_decode_sched_workspace_bytes(2, 8, 2, 128, 10) > 0
