@@ -67,6 +67,9 @@ WORKLOADS = {
                                  dtype="bf16"),
     "llama3-8b-backward-8k": dict(kind="backward", B=1, Hq=32, Hkv=8, L=8192, d=128, causal=True,
                                   dtype="bf16"),
+    # The long split-KV batch through the fixed-grid, load-balanced path of
+    # Lecture 4 section 5.6 (plan in the workspace, replayed as a CUDA graph).
+    "decode-b4-long-balanced": dict(kind="balanced", B=4, Hq=32, Hkv=8, d=128, lens="uniform"),
     # Lecture 4, section 4.4 demo 4: a 4096-token prefix shared by 64 requests,
     # 256 unique tokens each.
     "decode-cascade-b64-prefix4096": dict(kind="cascade", B=64, Hq=32, Hkv=8, d=128, prefix=4096,
@@ -94,6 +97,9 @@ def describe(name):
         return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, shared prefix "
                 f"{w['prefix']} + {w['suffix']} unique tokens per request (16-token shuffled pages)")
     lens = "ctx 1024 each" if w["lens"] == "1024x256" else "ctx U[4096,131072] seed 2"
+    if w["kind"] == "balanced":
+        return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, {lens}, 16-token "
+                f"shuffled pages, load-balanced fixed grid (CUDA graph)")
     return f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, {lens}, 16-token shuffled pages"
 
 
@@ -322,6 +328,20 @@ def make_step(name, torch, ea, inputs):
         def step():
             ea.attn_prefill_paged(q, kp, vp, table, cq, sl, mq, mk, causal=True, out=o, lse=lse)
         return step, 1, paged_flops(w, lens_q, lens_k), "flops", None
+    if w["kind"] == "balanced":
+        lens = decode_lens(w)
+        q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0,
+                                                    device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty(w["B"], w["Hq"], dtype=torch.float32, device="cuda")
+        ws = torch.empty(ea.lib().attn_decode_sched_workspace_bytes(w["B"], w["Hq"], w["Hkv"],
+                                                                    w["d"], 0),
+                         dtype=torch.uint8, device="cuda")
+        ea.attn_decode_schedule(lens, w["Hq"], w["Hkv"], ws)
+
+        def call():
+            ea.attn_decode_paged_balanced(q, kp, vp, table, sl, ws, out=o, lse=lse)
+        return graphed(torch, call), 2, decode_bytes(w, lens), "bytes", None
     lens = decode_lens(w)
     q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0,
                                                 device="cuda")
