@@ -758,14 +758,16 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
                          float* dd, int B, int Hq, int Hkv, int Lq, int Lk, int causal,
                          float scale, cudaStream_t stream) {
   using L = BwdSmem<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[64] = {};  // per device: kernel attributes are per device
+  const int dev = attn_host::current_device_slot();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   CUtensorMap mq, mk, mv, mdo;
   if (!make_map_rows(&mq, q, D, Lq, B * Hq) || !make_map_rows(&mk, k, D, Lk, B * Hkv) ||

@@ -41,6 +41,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // Host-side launchers (one per kernel family) used by api.cpp.
 namespace attn_host {
+// Index of the current device for per-device caches (kernel attributes,
+// occupancy): -1 on error or for device numbers past 63.
+inline int current_device_slot() {
+  int d = 0;
+  return (cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < 64) ? d : -1;
+}
+
 int* device_status_ptr();  // address of the status word on the current device (nullptr on error)
 int num_sms();             // SM count of the current device (cached per device)
 int decode_ctas_per_sm();  // resident decode CTAs per SM for the decode kernel

@@ -762,23 +762,27 @@ bool make_page_map(CUtensorMap* m, const void* base, int Hkv, int num_pages) {
 }
 
 bool set_smem_attr() {
-  static bool done = false;
-  if (!done) {
+  static bool done[64] = {};  // per device: kernel attributes are per device
+  const int dev = attn_host::current_device_slot();
+  if (dev < 0) return false;
+  if (!done[dev]) {
     if (cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
       return false;
-    done = true;
+    done[dev] = true;
   }
   return true;
 }
 
 bool set_balanced_smem_attr() {
-  static bool done = false;
-  if (!done) {
+  static bool done[64] = {};
+  const int dev = attn_host::current_device_slot();
+  if (dev < 0) return false;
+  if (!done[dev]) {
     if (cudaFuncSetAttribute(decode_balanced_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
       return false;
-    done = true;
+    done[dev] = true;
   }
   return true;
 }

@@ -1397,8 +1397,10 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   // Q-tile-pair ping-pong kernel.
   constexpr bool kD64 = D == 64;
   constexpr int smem_bytes = kD64 ? Cfg64::SMEM_BYTES : Cfg<D>::SMEM_BYTES;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[64] = {};  // per device: kernel attributes are per device
+  const int dev = attn_host::current_device_slot();
+  if (dev < 0) return ATTN_ERR_CUDA;
+  if (!attr_set[dev]) {
     const void* fn;
     if constexpr (kD64)
       fn = reinterpret_cast<const void*>(prefill_bf16_d64_kernel<kLayout>);
@@ -1409,7 +1411,7 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
         cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
             cudaSuccess)
       return ATTN_ERR_CUDA;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   CUtensorMap mq, mk, mv;
   if (q_div < 1 || (B * Hq) % q_div != 0) return ATTN_ERR_INVALID_ARG;
