@@ -76,6 +76,7 @@ struct Cfg {
   static constexpr int OFF_K = 2 * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+  static constexpr int OFF_LIST = OFF_BAR + 512;           // packed layouts: the item list
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t O_COL = 2 * BN;     // S_X at X * 128, O_X at O_COL + X * D
 };
@@ -276,10 +277,13 @@ struct Item {
 };
 
 // Work-item order and assignment.
-//  * Long causal rows (more than kGroupedMaxPairs pairs per head) and every
-//    packed (variable-length) batch: items are listed heaviest pair first
-//    across all heads and dealt round-robin to the persistent CTAs, which
-//    keeps them balanced when the work per item varies.
+//  * Long causal rows (more than kGroupedMaxPairs pairs per head): items are
+//    listed heaviest pair first across all heads and dealt round-robin to the
+//    persistent CTAs, which keeps them balanced when the work per item varies.
+//  * Packed (variable-length) batches: each CTA works through its list from
+//    build_item_list (units sorted by decreasing cost, dealt round-robin with
+//    odd rounds reversed); batches too large for the list fall back to the
+//    round-robin order of long causal rows.
 //  * Short rows or non-causal: items are listed head by head and every CTA
 //    takes one contiguous run of them, so the pairs of a head run back to back
 //    on the same SM and re-read that head's K/V from L2; each run spans whole
@@ -307,12 +311,155 @@ __device__ __forceinline__ Schedule make_schedule(int num_items, int num_pairs, 
   return sc;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// The item slot of this CTA's round-robin position it = r * gridDim.x +
+// blockIdx.x: even rounds deal slots in CTA order, odd rounds in reverse.
+__device__ __forceinline__ int dealt_slot(int it) {
+  const int G = gridDim.x, r = it / G;
+  return (r & 1) ? r * G + (G - 1 - static_cast<int>(blockIdx.x)) : it;
+}
+
+// Packed batches: each CTA's list of work items, built once in the prologue.
+// Unit u is Q-tile position num_pos - 1 - u / B of sequence u % B (u counts
+// heaviest position first, as the natural order does); a position is one Q
+// tile, or a pair of Q tiles (kTiles = 2).  A unit's cost is the K/V tiles its
+// Q tiles read plus one per Q tile present (its Q load and output write).
+// Every CTA sorts the units by decreasing cost with the same deterministic,
+// stable counting sort, lists the items (unit, head) in that order, and takes
+// the items of its round-robin positions, odd rounds dealt in reverse CTA
+// order: each CTA's sum of costs comes out close to the mean (a static form
+// of longest-processing-time-first).  An entry is bh | position << 20, or
+// ~0u for a position without work.  Batches with more than kMaxSortUnits
+// units or kMaxListItems positions per CTA keep the natural order.
+constexpr int kMaxSortUnits = 4096;
+constexpr int kCostBins = 2048;  // higher costs share the top bin
+constexpr int kMaxListItems = 2048;
+constexpr int kListBytes = kMaxListItems * 4;
+// cost[kMaxSortUnits], start[kCostBins] (int), order[kMaxSortUnits] (uint16)
+constexpr int kSortScratchBytes = (kMaxSortUnits + kCostBins) * 4 + kMaxSortUnits * 2;
+
+template <int kLayout, int kTiles>
+__device__ __forceinline__ int unit_cost(const Geo& geo, int u, int B, int num_pos, int causal,
+                                         int* status) {
+  const int pos = num_pos - 1 - u / B;
+  const Seq sq = seq_of<kLayout>(geo, u % B, status);
+  int c = 0;
+#pragma unroll
+  for (int x = 0; x < kTiles; ++x) {
+    const int kv = kv_tiles(sq, kTiles * pos + x, causal);
+    if (kv >= 0) c += kv + 1;
+  }
+  return min(c, kCostBins - 1);
+}
+
+// Called by every thread of the CTA (it holds block-wide barriers); scratch
+// is kSortScratchBytes of shared memory, free until the list is built.
+// Returns the list length (this CTA's positions up to its last item with
+// work), or -1 for a batch that keeps the natural order.
+template <int kLayout, int kTiles>
+__device__ int build_item_list(uint32_t* list, uint8_t* scratch, int BH, int Hq, int num_pos,
+                               const Geo& geo, int causal, int* status) {
+  const int B = BH / Hq, U = B * num_pos, G = gridDim.x;
+  const long long num_items = static_cast<long long>(BH) * num_pos;
+  const long long npos = (num_items + G - 1) / G;
+  if (U > kMaxSortUnits || npos > kMaxListItems || BH >= (1 << 20) || num_pos >= (1 << 12))
+    return -1;
+  int* cost = reinterpret_cast<int*>(scratch);
+  int* start = cost + kMaxSortUnits;  // per cost: count, then first position
+  uint16_t* order = reinterpret_cast<uint16_t*>(start + kCostBins);
+  const int nbins = min(kCostBins, kTiles * ((geo.Lk + BN - 1) / BN + 1) + 1);
+  for (int i = threadIdx.x; i < nbins; i += blockDim.x) start[i] = 0;
+  for (int u = threadIdx.x; u < U; u += blockDim.x)
+    cost[u] = unit_cost<kLayout, kTiles>(geo, u, B, num_pos, causal, status);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const unsigned below = (1u << lane) - 1u;
+    // Counts: 32 units at a time; the lowest lane of each group of equal
+    // costs adds the group's size.
+    for (int base = 0; base < U; base += 32) {
+      const int c = base + lane < U ? cost[base + lane] : -1;
+      const unsigned same = __match_any_sync(FULL, c);
+      if (c >= 0 && (same & below) == 0) start[c] += __popc(same);
+      __syncwarp();
+    }
+    // First position of each cost in decreasing cost order: lane L sums the
+    // bins at descending positions [L S, (L + 1) S), a warp scan gives each
+    // lane its offset, and the lane rewrites its bins as running offsets.
+    const int S = (nbins + 31) / 32, p0 = lane * S, p1 = min(nbins, p0 + S);
+    int sum = 0;
+    for (int p = p0; p < p1; ++p) sum += start[nbins - 1 - p];
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(FULL, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+    for (int p = p0; p < p1; ++p) {
+      const int cnt = start[nbins - 1 - p];
+      start[nbins - 1 - p] = run;
+      run += cnt;
+    }
+    __syncwarp();
+    // Stable scatter, 32 units at a time in order of u.
+    for (int base = 0; base < U; base += 32) {
+      const int c = base + lane < U ? cost[base + lane] : -1;
+      const unsigned same = __match_any_sync(FULL, c);
+      if (c >= 0) order[start[c] + __popc(same & below)] = static_cast<uint16_t>(base + lane);
+      __syncwarp();
+      if (c >= 0 && (same & below) == 0) start[c] += __popc(same);
+      __syncwarp();
+    }
+    if (lane == 0) start[0] = 0;  // from here on: the list length
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < npos; k += blockDim.x) {
+    const int slot = dealt_slot(k * G + static_cast<int>(blockIdx.x));
+    uint32_t e = ~0u;
+    if (slot < num_items) {
+      const int u = order[slot / Hq];
+      if (cost[u] > 0) {
+        e = static_cast<uint32_t>((u % B) * Hq + slot % Hq) |
+            static_cast<uint32_t>(num_pos - 1 - u / B) << 20;
+        atomicMax(&start[0], k + 1);
+      }
+    }
+    list[k] = e;
+  }
+  __syncthreads();
+  return start[0];
+}
+
+// Packed batches with an item list (`list`: its shared-memory address, 0 for
+// none): item `it` is the list's entry it.
 template <int kLayout>
 __device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int Hq, int num_pairs,
-                                            const Geo& geo, int causal, int* status) {
+                                            const Geo& geo, int causal, int* status,
+                                            uint32_t list) {
   Item w;
   int pair;
-  if (grouped) {
+  if (kLayout != kDenseLayout && list != 0) {
+    const uint32_t e = ld_shared_u32(list + 4u * it);
+    if (e == ~0u) {  // a position without work
+      w.bh = 0;
+      w.sq = Seq{0, 0, 0, 0};
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        w.qt[x] = x;
+        w.n[x] = 0;
+        w.zero[x] = false;
+      }
+      return w;
+    }
+    w.bh = static_cast<int>(e & 0xFFFFFu);
+    pair = static_cast<int>(e >> 20);
+  } else if (grouped) {
     w.bh = it / num_pairs;
     pair = num_pairs - 1 - it % num_pairs;
   } else {
@@ -366,7 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_items = BH * num_pairs;
   constexpr bool packed = kPacked;
   const int group = Hq / Hkv;
-  const Schedule sched = make_schedule(num_items, num_pairs, causal, kPacked);
+  Schedule sched = make_schedule(num_items, num_pairs, causal, kPacked);
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -389,6 +536,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
   if (*abort_flag == 2) return;
+  // Packed batches: this CTA's item list (the K ring, not yet in use, is the
+  // sort's scratch); `list` is its shared-memory address, 0 if the batch
+  // keeps the natural order.
+  uint32_t list = 0;
+  if constexpr (kPacked) {
+    static_assert(kSortScratchBytes <= NS * C::TILE_BYTES, "sort scratch fits the K ring");
+    const int n = build_item_list<kLayout, 2>(reinterpret_cast<uint32_t*>(smem + C::OFF_LIST),
+                                              smem + C::OFF_K, BH, Hq, num_pairs, geo, causal,
+                                              status);
+    if (n >= 0) {
+      list = sbase + C::OFF_LIST;
+      sched.first = 0;
+      sched.last = n;
+      sched.step = 1;
+    }
+  }
+  auto item_of = [&](int it) {
+    return decode_item<kLayout>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status, list);
+  };
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
@@ -410,7 +576,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int nq[2] = {0, 0};       // Q tiles issued per slot
       bool ok = true;
       for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-        const Item w = decode_item<kLayout>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
+        const Item w = item_of(it);
         const int nmax = max(w.n[0], w.n[1]);
         if (nmax == 0) continue;
         const int h = w.bh % Hq;
@@ -526,7 +692,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
 
       for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-        const Item w = decode_item<kLayout>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
+        const Item w = item_of(it);
         const int nmax = max(w.n[0], w.n[1]);
         if (nmax == 0) continue;
         // First QK^T of each present tile.
@@ -592,7 +758,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int g0 = 0;  // K/V tiles of the items before this one (the producer's ring count)
     bool ok = true;
     for (int it = sched.first; ok && it < sched.last; it += sched.step) {
-      const Item w = decode_item<kLayout>(it, sched.grouped, BH, Hq, num_pairs, geo, causal, status);
+      const Item w = item_of(it);
       const int n = w.n[x];
       const int g_item = g0;
       g0 += max(w.n[0], w.n[1]);
@@ -776,6 +942,7 @@ struct Cfg64 {
   static constexpr int OFF_K = NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+  static constexpr int OFF_LIST = OFF_BAR + 256;  // packed layouts: the item list
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr uint32_t COLS = 256;
   static constexpr uint32_t P_COL = BN;
@@ -799,10 +966,22 @@ struct SeqCache {
 template <int kLayout>
 __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int Hq, int num_qt,
                                               const Geo& geo, int causal, int* status,
-                                              SeqCache& cache) {
+                                              SeqCache& cache, uint32_t list) {
   constexpr bool kPacked = kLayout != kDenseLayout;
   Item1 w;
-  if (grouped) {
+  if (kPacked && list != 0) {  // the CTA's item list (packed batches)
+    const uint32_t e = ld_shared_u32(list + 4u * it);
+    if (e == ~0u) {  // a position without work
+      w.bh = 0;
+      w.qt = 0;
+      w.n = 0;
+      w.zero = false;
+      w.sq = Seq{0, 0, 0, 0};
+      return w;
+    }
+    w.bh = static_cast<int>(e & 0xFFFFFu);
+    w.qt = static_cast<int>(e >> 20);
+  } else if (grouped) {
     w.bh = it / num_qt;
     w.qt = num_qt - 1 - it % num_qt;
   } else {
@@ -864,10 +1043,11 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   constexpr bool packed = kPacked;
   const int group = Hq / Hkv;
   // Dense short rows (or no mask): each CTA takes a contiguous run of items,
-  // head by head, so a head's K/V is re-read from L2.  Long causal rows and
-  // every packed batch: items heaviest first (Q tile index descending over
-  // all heads), dealt round-robin, which balances the CTAs when the work per
-  // item varies (causal, or sequences of mixed lengths).
+  // head by head, so a head's K/V is re-read from L2.  Long causal rows:
+  // items heaviest first (Q tile index descending over all heads), dealt
+  // round-robin, which balances the CTAs when the work per item varies.
+  // Packed batches: the item list of build_item_list (units sorted by cost),
+  // else the round-robin order.
   Schedule sched;
   sched.grouped = !kPacked && (!causal || num_qt <= 2 * kGroupedMaxPairs);
   if (sched.grouped) {
@@ -879,10 +1059,11 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     sched.last = num_items;
     sched.step = gridDim.x;
   }
+  uint32_t list = 0;  // packed batches: the item list's shared address (set below), or 0
   SeqCache seq_cache;
   auto item_at = [&](int it) {
     return decode_item1<kLayout>(it, sched.grouped, BH, Hq, num_qt, geo, causal, status,
-                                 seq_cache);
+                                 seq_cache, list);
   };
   // The first item at or after `it` (in this CTA's order) with K/V work,
   // described in w (set only when the result is < sched.last).  Items
@@ -919,6 +1100,20 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   }
   __syncthreads();
   if (*abort_flag == 2) return;
+  // Packed batches: this CTA's item list (the K ring, not yet in use, is the
+  // sort's scratch).
+  if constexpr (kPacked) {
+    static_assert(kSortScratchBytes <= NS * C::TILE_BYTES, "sort scratch fits the K ring");
+    const int n = build_item_list<kLayout, 1>(reinterpret_cast<uint32_t*>(smem + C::OFF_LIST),
+                                              smem + C::OFF_K, BH, Hq, num_qt, geo, causal,
+                                              status);
+    if (n >= 0) {
+      list = sbase + C::OFF_LIST;
+      sched.first = 0;
+      sched.last = n;
+      sched.step = 1;
+    }
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::COLS);
     tmem_relinquish();
@@ -1396,7 +1591,8 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   // d = 64 runs the two-CTAs-per-SM kernel on single Q tiles, d = 128 the
   // Q-tile-pair ping-pong kernel.
   constexpr bool kD64 = D == 64;
-  constexpr int smem_bytes = kD64 ? Cfg64::SMEM_BYTES : Cfg<D>::SMEM_BYTES;
+  constexpr int smem_bytes = (kD64 ? Cfg64::SMEM_BYTES : Cfg<D>::SMEM_BYTES) +
+                             (kLayout != kDenseLayout ? kListBytes : 0);
   static bool attr_set[64] = {};  // per device: kernel attributes are per device
   const int dev = attn_host::current_device_slot();
   if (dev < 0) return ATTN_ERR_CUDA;

@@ -98,6 +98,17 @@ def test_equals_packed_prefill_bitwise(d, causal):
     assert torch.equal(o_p, o_v) and torch.equal(lse_p, lse_v)
 
 
+@pytest.mark.parametrize("d,B", [(128, 4096), (64, 4097)])
+def test_many_requests_sorted_list_and_fallback(d, B):
+    """4096 work units fill the per-CTA sorted item list; 4097 keep the
+    round-robin order.  Chunks of 1 to 128 tokens after up to 300 cached
+    ones."""
+    g = np.random.default_rng(60 + B)
+    lens_q = g.integers(1, 129, B)
+    lens_k = lens_q + g.integers(0, 301, B)
+    run(lens_q.tolist(), lens_k.tolist(), d, True, Hq=2, Hkv=1, seed=10)
+
+
 def test_long_context_chunks_sampled():
     """A serving-like batch (Hq 32, Hkv 8, d 128): 8 requests with cached
     contexts up to 8192 tokens and new chunks up to 512, checked on sampled

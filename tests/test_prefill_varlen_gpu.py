@@ -55,6 +55,20 @@ def test_more_queries_than_keys(d):
     assert torch.isneginf(lse[:130]).all() and (o[:130] == 0).all()
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B", [4096, 4097])
+def test_many_sequences_sorted_list_and_fallback(d, B):
+    """Each CTA sorts at most 4096 work units (a sequence's Q-tile position)
+    into its item list; one more unit keeps the round-robin order.  Chunks of
+    1 to 128 queries after 0 to 300 earlier keys give units of unequal cost,
+    so the sort does reorder them; every 97th sequence has no queries."""
+    g = np.random.default_rng(40 + B)
+    lens_q = g.integers(1, 129, B)
+    lens_q[::97] = 0
+    lens_k = lens_q + g.integers(0, 301, B)
+    run_varlen(lens_q.tolist(), lens_k.tolist(), d, True, Hq=1, Hkv=1, seed=5)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_no_keys_anywhere(causal):
     """total_k = 0: every row sees no key (O = 0, LSE = -inf)."""
