@@ -279,7 +279,9 @@ struct Item {
 // Work-item order and assignment.
 //  * Long causal rows (more than kGroupedMaxPairs pairs per head): items are
 //    listed heaviest pair first across all heads and dealt round-robin to the
-//    persistent CTAs, which keeps them balanced when the work per item varies.
+//    persistent CTAs, odd rounds in reverse CTA order (the d = 128 kernel,
+//    through build_item_list), which keeps them balanced when the work per
+//    item varies.
 //  * Packed (variable-length) batches: each CTA works through its list from
 //    build_item_list (units sorted by decreasing cost, dealt round-robin with
 //    odd rounds reversed); batches too large for the list fall back to the
@@ -367,8 +369,20 @@ __device__ int build_item_list(uint32_t* list, uint8_t* scratch, int BH, int Hq,
   const int B = BH / Hq, U = B * num_pos, G = gridDim.x;
   const long long num_items = static_cast<long long>(BH) * num_pos;
   const long long npos = (num_items + G - 1) / G;
-  if (U > kMaxSortUnits || npos > kMaxListItems || BH >= (1 << 20) || num_pos >= (1 << 12))
-    return -1;
+  if (npos > kMaxListItems || BH >= (1 << 20) || num_pos >= (1 << 12)) return -1;
+  if constexpr (kLayout == kDenseLayout) {
+    // Equal rows: the natural order (position-major) is already heaviest
+    // first and every unit has work; only the dealing changes.
+    for (int k = threadIdx.x; k < npos; k += blockDim.x) {
+      const int slot = dealt_slot(k * G + static_cast<int>(blockIdx.x));
+      list[k] = slot < num_items ? static_cast<uint32_t>(slot % BH) |
+                                       static_cast<uint32_t>(num_pos - 1 - slot / BH) << 20
+                                 : ~0u;
+    }
+    __syncthreads();
+    return static_cast<int>(npos);
+  }
+  if (U > kMaxSortUnits) return -1;
   int* cost = reinterpret_cast<int*>(scratch);
   int* start = cost + kMaxSortUnits;  // per cost: count, then first position
   uint16_t* order = reinterpret_cast<uint16_t*>(start + kCostBins);
@@ -436,15 +450,15 @@ __device__ int build_item_list(uint32_t* list, uint8_t* scratch, int BH, int Hq,
   return start[0];
 }
 
-// Packed batches with an item list (`list`: its shared-memory address, 0 for
-// none): item `it` is the list's entry it.
+// With an item list (`list`: its shared-memory address, 0 for none): item
+// `it` is the list's entry it.
 template <int kLayout>
 __device__ __forceinline__ Item decode_item(int it, bool grouped, int BH, int Hq, int num_pairs,
                                             const Geo& geo, int causal, int* status,
                                             uint32_t list) {
   Item w;
   int pair;
-  if (kLayout != kDenseLayout && list != 0) {
+  if (list != 0) {
     const uint32_t e = ld_shared_u32(list + 4u * it);
     if (e == ~0u) {  // a position without work
       w.bh = 0;
@@ -536,11 +550,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
   if (*abort_flag == 2) return;
-  // Packed batches: this CTA's item list (the K ring, not yet in use, is the
-  // sort's scratch); `list` is its shared-memory address, 0 if the batch
-  // keeps the natural order.
+  // Packed batches and long causal rows: this CTA's item list (the K ring,
+  // not yet in use, is the sort's scratch); `list` is its shared-memory
+  // address, 0 if the batch keeps the natural order.
   uint32_t list = 0;
-  if constexpr (kPacked) {
+  if (!sched.grouped) {
     static_assert(kSortScratchBytes <= NS * C::TILE_BYTES, "sort scratch fits the K ring");
     const int n = build_item_list<kLayout, 2>(reinterpret_cast<uint32_t*>(smem + C::OFF_LIST),
                                               smem + C::OFF_K, BH, Hq, num_pairs, geo, causal,
@@ -1592,7 +1606,7 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   // Q-tile-pair ping-pong kernel.
   constexpr bool kD64 = D == 64;
   constexpr int smem_bytes = (kD64 ? Cfg64::SMEM_BYTES : Cfg<D>::SMEM_BYTES) +
-                             (kLayout != kDenseLayout ? kListBytes : 0);
+                             (!kD64 || kLayout != kDenseLayout ? kListBytes : 0);
   static bool attr_set[64] = {};  // per device: kernel attributes are per device
   const int dev = attn_host::current_device_slot();
   if (dev < 0) return ATTN_ERR_CUDA;
