@@ -512,8 +512,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* q_empty = q_full + 2;     // [2]
   uint64_t* k_full = q_empty + 2;     // [NS]
   uint64_t* v_full = k_full + NS;     // [NS]
-  uint64_t* kv_empty = v_full + NS;   // [NS]
-  uint64_t* s_full = kv_empty + NS;   // [2]
+  uint64_t* k_empty = v_full + NS;    // [NS] the slot's last QK^T done
+  uint64_t* v_empty = k_empty + NS;   // [NS] the slot's last PV done
+  uint64_t* s_full = v_empty + NS;    // [2]
   uint64_t* p_full = s_full + 2;      // [2]
   uint64_t* o_done = p_full + 2;      // [2]
   uint64_t* o_free = o_done + 2;      // [2]
@@ -541,7 +542,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = (status != nullptr &&
@@ -600,18 +602,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int kv_c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
         PageCursor pages;
         if constexpr (kPaged) pages.begin(geo, w.bh / Hq, w.sq.lk);
-        // K/V tile j of this item into the next ring slot.
+        // K/V tile j of this item into the next ring slot.  The K and V halves
+        // of a slot free separately: K after the slot's last QK^T, which the
+        // MMA issuer commits one K/V tile before the slot's last PV, so K(j)
+        // goes out as soon as V(j - 1) has (the two frees come together).
         auto issue_kv = [&](int j) -> bool {
           const int st = g % NS;
-          if (g >= NS && !mbar_wait(&kv_empty[st], ((g / NS) + 1) & 1, abort_flag, kWaitLimitNs))
+          const uint32_t ph = ((g / NS) + 1) & 1;
+          // Giving up between the K and V copies: K(j) lands before the
+          // producer moves on (the drain below covers whole tiles only).
+          auto drain_k = [&](int slot) {
+            int no_abort = 0;
+            mbar_wait(&k_full[slot], (g / NS) & 1, &no_abort, kWaitLimitNs);
             return false;
+          };
           uint8_t* kdst = smem + C::OFF_K + st * C::TILE_BYTES;
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
+          if (g >= NS && !mbar_wait(&k_empty[st], ph, abort_flag, kWaitLimitNs)) return false;
           if constexpr (kPaged) {
             int pg[PageCursor::NP];
             pages.take(pg, geo, status);  // tile j (tiles are issued in order)
             mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
             tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[st], pg, kv_c1);
+            if (g >= NS && !mbar_wait(&v_empty[st], ph, abort_flag, kWaitLimitNs))
+              return drain_k(st);
             mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
             tma_load_pages<C::KB, C::BLOCK_BYTES>(vdst, &tm_v, &v_full[st], pg, kv_c1);
           } else {
@@ -619,6 +633,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < C::KB; ++kb)
               tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &k_full[st], kb * 64,
                           packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
+            if (g >= NS && !mbar_wait(&v_empty[st], ph, abort_flag, kWaitLimitNs))
+              return drain_k(st);
             mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb)
               tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &v_full[st], kb * 64,
@@ -717,6 +733,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           issue_qk(x, g % NS, w.n[x] == 1);
         }
+        if (ok) mma_commit(&k_empty[g % NS]);  // K(0) of the item is read
         for (int j = 0; ok && j < nmax; ++j) {
           const int st = (g + j) % NS, ph = ((g + j) / NS) & 1;
           const int st1 = (g + j + 1) % NS, ph1 = ((g + j + 1) / NS) & 1;
@@ -743,7 +760,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               mma_commit(&o_done[x]);
             }
           }
-          if (ok) mma_commit(&kv_empty[st]);
+          if (ok) {
+            if (j + 1 < nmax) mma_commit(&k_empty[st1]);  // K(j + 1) is read
+            mma_commit(&v_empty[st]);
+          }
         }
         g += nmax;
         for (int x = 0; x < 2; ++x)
