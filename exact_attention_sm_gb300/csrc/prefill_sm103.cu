@@ -326,7 +326,9 @@ __device__ __forceinline__ int dealt_slot(int it) {
   return (r & 1) ? r * G + (G - 1 - static_cast<int>(blockIdx.x)) : it;
 }
 
-// Packed batches: each CTA's list of work items, built once in the prologue.
+// Each CTA's list of work items, built once in the prologue (packed batches,
+// and the d = 128 kernel's long causal rows of the dense layout, whose equal
+// rows already come heaviest first: their list skips the sort).
 // Unit u is Q-tile position num_pos - 1 - u / B of sequence u % B (u counts
 // heaviest position first, as the natural order does); a position is one Q
 // tile, or a pair of Q tiles (kTiles = 2).  A unit's cost is the K/V tiles its
