@@ -38,9 +38,13 @@ def test_rectangular_non_causal(d):
 
 
 def sampled_case(B, Hq, Hkv, L, d, causal):
+    """Sampled rows against the oracle.  O and LSE start as NaN, so a work
+    item that no CTA took would leave non-finite rows behind."""
     q, k, v = inputs.prefill_inputs(B, Hq, Hkv, L, L, d, "bf16", seed=0)
     scale = 1.0 / math.sqrt(d)
-    o, lse = ea.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    o = torch.full((B, Hq, L, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hq, L), float("nan"), dtype=torch.float32, device="cuda")
+    ea.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, out=o, lse=lse)
     torch.cuda.synchronize()
     assert ea.attn_get_device_status() == "ATTN_OK"
     rows = inputs.sample_rows(B, Hq, L)
@@ -58,6 +62,13 @@ def sampled_case(B, Hq, Hkv, L, d, causal):
 
 def test_gpt2_medium_shape_B64_H16_L1024_d64_causal():
     sampled_case(64, 16, 16, 1024, 64, True)
+
+
+def test_long_causal_rows_dealt_in_reversed_odd_rounds():
+    """17 pair positions x 32 heads = 544 items on the persistent grid: the
+    smallest d = 128 causal rows dealt from the per-CTA item list, with odd
+    rounds in reverse CTA order."""
+    sampled_case(1, 32, 8, 4352, 128, True)
 
 
 def test_llama3_8b_shape_L8192_gqa_causal():
