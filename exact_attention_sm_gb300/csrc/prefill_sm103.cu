@@ -71,10 +71,11 @@ struct Cfg {
   static constexpr int KB = D / 64;             // 128-byte swizzle column blocks per row
   static constexpr int BLOCK_BYTES = BM * 128;  // one 128-row x 128-byte column block
   static constexpr int TILE_BYTES = BM * D * 2; // a Q, K or V tile
-  static constexpr int NS = D == 64 ? 5 : 2;    // K/V pipeline stages
+  static constexpr int NS = D == 64 ? 5 : 2;    // V pipeline stages
+  static constexpr int NSK = D == 64 ? 5 : 3;   // K pipeline stages (K runs further ahead)
   static constexpr int OFF_Q = 0;               // Q_A, Q_B
   static constexpr int OFF_K = 2 * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
   static constexpr int OFF_LIST = OFF_BAR + 512;           // packed layouts: the item list
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // barriers + alignment slack
@@ -342,7 +343,7 @@ __device__ __forceinline__ int dealt_slot(int it) {
 // units or kMaxListItems positions per CTA keep the natural order.
 constexpr int kMaxSortUnits = 4096;
 constexpr int kCostBins = 2048;  // higher costs share the top bin
-constexpr int kMaxListItems = 2048;
+constexpr int kMaxListItems = 256;  // 1 KB: what the d = 128 kernel's three K stages leave
 constexpr int kListBytes = kMaxListItems * 4;
 // cost[kMaxSortUnits], start[kCostBins] (int), order[kMaxSortUnits] (uint16)
 constexpr int kSortScratchBytes = (kMaxSortUnits + kCostBins) * 4 + kMaxSortUnits * 2;
@@ -501,7 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float* __restrict__ lse, int BH, int Hq, int Hkv, const Geo geo,
                         int causal, float scale_log2, int q_div, int* status) {
   using C = Cfg<D>;
-  constexpr int NS = C::NS;
+  constexpr int NS = C::NS, NSK = C::NSK;
   constexpr bool kPacked = kLayout != kDenseLayout;
   constexpr bool kPaged = kLayout == kPagedLayout;
   extern __shared__ uint8_t smem_raw[];
@@ -512,10 +513,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;            // [2]
   uint64_t* q_empty = q_full + 2;     // [2]
-  uint64_t* k_full = q_empty + 2;     // [NS]
-  uint64_t* v_full = k_full + NS;     // [NS]
-  uint64_t* k_empty = v_full + NS;    // [NS] the slot's last QK^T done
-  uint64_t* v_empty = k_empty + NS;   // [NS] the slot's last PV done
+  uint64_t* k_full = q_empty + 2;     // [NSK]
+  uint64_t* v_full = k_full + NSK;    // [NS]
+  uint64_t* k_empty = v_full + NS;    // [NSK] the slot's last QK^T done
+  uint64_t* v_empty = k_empty + NSK;  // [NS] the slot's last PV done
   uint64_t* s_full = v_empty + NS;    // [2]
   uint64_t* p_full = s_full + 2;      // [2]
   uint64_t* o_done = p_full + 2;      // [2]
@@ -541,10 +542,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&o_done[x], 1);
       mbar_init(&o_free[x], 128);
     }
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(drain, 1);
@@ -559,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // address, 0 if the batch keeps the natural order.
   uint32_t list = 0;
   if (!sched.grouped) {
-    static_assert(kSortScratchBytes <= NS * C::TILE_BYTES, "sort scratch fits the K ring");
+    static_assert(kSortScratchBytes <= NSK * C::TILE_BYTES, "sort scratch fits the K ring");
     const int n = build_item_list<kLayout, 2>(reinterpret_cast<uint32_t*>(smem + C::OFF_LIST),
                                               smem + C::OFF_K, BH, Hq, num_pairs, geo, causal,
                                               status);
@@ -609,34 +612,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // MMA issuer commits one K/V tile before the slot's last PV, so K(j)
         // goes out as soon as V(j - 1) has (the two frees come together).
         auto issue_kv = [&](int j) -> bool {
-          const int st = g % NS;
-          const uint32_t ph = ((g / NS) + 1) & 1;
+          const int sk = g % NSK, st = g % NS;  // K slot, V slot
+          const uint32_t phk = ((g / NSK) + 1) & 1, ph = ((g / NS) + 1) & 1;
           // Giving up between the K and V copies: K(j) lands before the
           // producer moves on (the drain below covers whole tiles only).
           auto drain_k = [&](int slot) {
             int no_abort = 0;
-            mbar_wait(&k_full[slot], (g / NS) & 1, &no_abort, kWaitLimitNs);
+            mbar_wait(&k_full[slot], (g / NSK) & 1, &no_abort, kWaitLimitNs);
             return false;
           };
-          uint8_t* kdst = smem + C::OFF_K + st * C::TILE_BYTES;
+          uint8_t* kdst = smem + C::OFF_K + sk * C::TILE_BYTES;
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
-          if (g >= NS && !mbar_wait(&k_empty[st], ph, abort_flag, kWaitLimitNs)) return false;
+          if (g >= NSK && !mbar_wait(&k_empty[sk], phk, abort_flag, kWaitLimitNs)) return false;
           if constexpr (kPaged) {
             int pg[PageCursor::NP];
             pages.take(pg, geo, status);  // tile j (tiles are issued in order)
-            mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
-            tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[st], pg, kv_c1);
+            mbar_arrive_expect_tx(&k_full[sk], C::TILE_BYTES);
+            tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[sk], pg, kv_c1);
             if (g >= NS && !mbar_wait(&v_empty[st], ph, abort_flag, kWaitLimitNs))
-              return drain_k(st);
+              return drain_k(sk);
             mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
             tma_load_pages<C::KB, C::BLOCK_BYTES>(vdst, &tm_v, &v_full[st], pg, kv_c1);
           } else {
-            mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
+            mbar_arrive_expect_tx(&k_full[sk], C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb)
-              tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &k_full[st], kb * 64,
+              tma_load_3d(kdst + kb * C::BLOCK_BYTES, &tm_k, &k_full[sk], kb * 64,
                           packed ? kv_c1 : j * BN, packed ? kv_c2 + j * BN : kv_c2);
             if (g >= NS && !mbar_wait(&v_empty[st], ph, abort_flag, kWaitLimitNs))
-              return drain_k(st);
+              return drain_k(sk);
             mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb)
               tma_load_3d(vdst + kb * C::BLOCK_BYTES, &tm_v, &v_full[st], kb * 64,
@@ -673,10 +676,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int no_abort = 0;
       for (int x = 0; x < 2; ++x)
         if (nq[x] > 0) mbar_wait(&q_full[x], (nq[x] - 1) & 1, &no_abort, kWaitLimitNs);
-      for (int t = g > NS ? g - NS : 0; t < g; ++t) {
-        mbar_wait(&k_full[t % NS], (t / NS) & 1, &no_abort, kWaitLimitNs);
+      for (int t = g > NSK ? g - NSK : 0; t < g; ++t)
+        mbar_wait(&k_full[t % NSK], (t / NSK) & 1, &no_abort, kWaitLimitNs);
+      for (int t = g > NS ? g - NS : 0; t < g; ++t)
         mbar_wait(&v_full[t % NS], (t / NS) & 1, &no_abort, kWaitLimitNs);
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -728,17 +731,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int nmax = max(w.n[0], w.n[1]);
         if (nmax == 0) continue;
         // First QK^T of each present tile.
-        if (!mbar_wait(&k_full[g % NS], (g / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        if (!mbar_wait(&k_full[g % NSK], (g / NSK) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
         for (int x = 0; x < 2 && ok; ++x) {
           if (w.n[x] == 0) continue;
           if (!mbar_wait(&q_full[x], nitem[x] & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
-          issue_qk(x, g % NS, w.n[x] == 1);
+          issue_qk(x, g % NSK, w.n[x] == 1);
         }
-        if (ok) mma_commit(&k_empty[g % NS]);  // K(0) of the item is read
+        if (ok) mma_commit(&k_empty[g % NSK]);  // K(0) of the item is read
         for (int j = 0; ok && j < nmax; ++j) {
           const int st = (g + j) % NS, ph = ((g + j) / NS) & 1;
-          const int st1 = (g + j + 1) % NS, ph1 = ((g + j + 1) / NS) & 1;
+          const int st1 = (g + j + 1) % NSK, ph1 = ((g + j + 1) / NSK) & 1;  // K slot
           bool v_ready = false, k_ready = false;  // each K/V tile is waited for once
           for (int x = 0; x < 2; ++x) {
             if (j >= w.n[x]) continue;

@@ -69,6 +69,16 @@ def test_many_sequences_sorted_list_and_fallback(d, B):
     run_varlen(lens_q.tolist(), lens_k.tolist(), d, True, Hq=1, Hkv=1, seed=5)
 
 
+def test_more_positions_than_the_item_list_holds():
+    """2500 sequences x 16 heads = 40000 items: at d = 128 that is 264
+    positions per CTA on 152 SMs, more than the item list holds, so the
+    batch keeps the round-robin order."""
+    g = np.random.default_rng(77)
+    lens_q = g.integers(1, 129, 2500)
+    lens_k = lens_q + g.integers(0, 65, 2500)
+    run_varlen(lens_q.tolist(), lens_k.tolist(), 128, True, Hq=16, Hkv=2, seed=8)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_no_keys_anywhere(causal):
     """total_k = 0: every row sees no key (O = 0, LSE = -inf)."""
