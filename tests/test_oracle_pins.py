@@ -267,6 +267,88 @@ def test_merge_skips_empty_segments():
     assert abs(orc.merge_states(op[:1], lp[:1])[1] - lp[0]) < 1e-15
 
 
+def _segment_states(scores, values, cuts):
+    """(O_s, LSE_s) of one row whose score list is cut at `cuts`, each segment by
+    the dense definition (d = 1, q = 1, k = the scores)."""
+    s, v = np.asarray(scores, float), np.asarray(values, float)
+    bounds = [0] + list(cuts) + [len(s)]
+    op, lp = [], []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        oo, ll, _, _ = orc.attention_dense([[1.0]], s[a:b, None], v[a:b, None], 1.0)
+        op.append(oo[0] if b > a else np.zeros(1))
+        lp.append(ll[0] if b > a else -math.inf)
+    return np.array(op), np.array(lp)
+
+
+def test_merge_batched_worked_examples_by_row():
+    """merge_states_batched on a batch whose rows are the pages' split examples:
+    [LLM book] 10.3.2's scores [1,3,2] / values [10,20,30] split [1,3]|[2]
+    (O = 21.547, LSE = 3.4076), the same row split [1]|[3,2], [CUDA book]
+    exercise 1 ([1,3]|[2,5] with [10,20]|[30,40], O = 36.88), a row whose
+    middle segment is empty, and a row with every segment empty (O = 0,
+    LSE = -inf).  Rows and segments are shuffled: each output row must be its
+    own example's value."""
+    g = GOLD["llm_book_softmax_weights_and_lse"]
+    c = GOLD["cuda_book_exercise_1"]
+    cases = [
+        (_segment_states(g["scores"], g["values"], [2]), g["o"], g["lse"]),
+        (_segment_states(g["scores"], g["values"], [1]), g["o"], g["lse"]),
+        (_segment_states(c["blocks_scores"][0] + c["blocks_scores"][1],
+                         c["blocks_values"][0] + c["blocks_values"][1], [2]), c["o"], None),
+        (_segment_states(g["scores"], g["values"], [2, 2]), g["o"], g["lse"]),
+    ]
+    S = 3
+    rows_o, rows_l, want = [], [], []
+    rng = np.random.default_rng(11)
+    for (op, lp), o_want, lse_want in cases:
+        # pad to S segments with empty states (garbage O, LSE = -inf), then shuffle
+        pad = S - len(lp)
+        op = np.concatenate([op, np.full((pad, 1), np.nan)])
+        lp = np.concatenate([lp, np.full(pad, -math.inf)])
+        perm = rng.permutation(S)
+        rows_o.append(op[perm]); rows_l.append(lp[perm]); want.append((o_want, lse_want))
+    rows_o.append(np.full((S, 1), 7.0)); rows_l.append(np.full(S, -math.inf))
+    want.append((0.0, -math.inf))
+    order = rng.permutation(len(want))
+    o, lse = orc.merge_states_batched(np.array(rows_o)[order], np.array(rows_l)[order])
+    assert o.shape == (len(want), 1) and lse.shape == (len(want),)
+    for out_row, src in enumerate(order):
+        o_want, lse_want = want[src]
+        if lse_want == -math.inf:
+            assert o[out_row, 0] == 0.0 and lse[out_row] == -math.inf
+            continue
+        assert close(o[out_row, 0], o_want, 2), (src, o[out_row, 0], o_want)
+        if lse_want is not None:
+            assert close(lse[out_row], lse_want, 4)
+
+
+def test_merge_batched_equals_dense_rows():
+    """Split-then-merge over a batch of rows equals the dense attention of each
+    row over all its keys ([Lecture 4] 4.3), with rows of different queries and
+    key sets so that a transposed row or segment index shows."""
+    rng = np.random.default_rng(12)
+    rows, n, d, S = 6, 300, 8, 5
+    q = rng.standard_normal((rows, d))
+    k = rng.standard_normal((rows, n, d))
+    v = rng.standard_normal((rows, n, d))
+    op = np.zeros((rows, S, d)); lp = np.zeros((rows, S))
+    o_ref = np.zeros((rows, d)); lse_ref = np.zeros(rows)
+    for r in range(rows):
+        oo, ll, _, _ = orc.attention_dense(q[r][None], k[r], v[r], 0.3)
+        o_ref[r], lse_ref[r] = oo[0], ll[0]
+        op[r], lp[r] = orc.decode_split_states(q[r], k[r], v[r], 0.3, 60)
+    o, lse = orc.merge_states_batched(op, lp)
+    assert np.abs(o - o_ref).max() < 1e-13 and np.abs(lse - lse_ref).max() < 1e-12
+    # the segments of a row are an unordered set; the rows keep their order
+    perm_s = rng.permutation(S)
+    o2, lse2 = orc.merge_states_batched(op[:, perm_s], lp[:, perm_s])
+    assert np.abs(o2 - o_ref).max() < 1e-13 and np.abs(lse2 - lse_ref).max() < 1e-12
+    perm_r = rng.permutation(rows)
+    o3, lse3 = orc.merge_states_batched(op[perm_r], lp[perm_r])
+    assert np.abs(o3 - o_ref[perm_r]).max() < 1e-13
+    assert np.abs(lse3 - lse_ref[perm_r]).max() < 1e-12
+
+
 # ---------------------------------------------------------------- paging and GQA
 
 def test_bsr_page_tables_lecture_5_2():
