@@ -1632,6 +1632,10 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   constexpr bool kD64 = D == 64;
   constexpr int smem_bytes = (kD64 ? Cfg64::SMEM_BYTES : Cfg<D>::SMEM_BYTES) +
                              (!kD64 || kLayout != kDenseLayout ? kListBytes : 0);
+  // Opt-in limit of one CTA (227 KB); at d = 64 two CTAs (each with 1 KB the
+  // hardware reserves) share the SM's 228 KB.
+  static_assert(Cfg<128>::SMEM_BYTES + kListBytes <= 227 * 1024, "d = 128 shared memory");
+  static_assert(2 * (Cfg64::SMEM_BYTES + kListBytes + 1024) <= 228 * 1024, "d = 64 shared memory");
   static bool attr_set[64] = {};  // per device: kernel attributes are per device
   const int dev = attn_host::current_device_slot();
   if (dev < 0) return ATTN_ERR_CUDA;

@@ -30,8 +30,11 @@ def check_grad(got, want, name):
     assert np.isfinite(got).all(), f"{name}: non-finite"
     err = np.abs(got - want)
     scale = max(np.abs(want).max(), 1e-3)  # an all-zero gradient (one key) has no scale of its own
-    assert err.max() <= MAX_REL * scale, f"{name}: max {err.max():.3e} vs scale {scale:.3e}"
     total = max(np.abs(want).sum(), 1e-3 * want.size)
+    # The measured margins, printed beside the bounds (pytest -s or -rP shows them).
+    print(f"{name}: max|err|/scale {err.max() / scale:.2e} (bound {MAX_REL:.0e}), "
+          f"sum|err|/sum|ref| {err.sum() / total:.2e} (bound {SUM_REL:.0e})")
+    assert err.max() <= MAX_REL * scale, f"{name}: max {err.max():.3e} vs scale {scale:.3e}"
     assert err.sum() <= SUM_REL * total, f"{name}: sum-rel {err.sum() / total:.3e}"
 
 
@@ -81,3 +84,46 @@ def test_deterministic():
         dq2, dk2, dv2 = ea.attn_bwd(*args, causal=True)
         torch.cuda.synchronize()
         assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
+def run_sampled_groups(B, Hq, Hkv, L, d, groups, seed):
+    """Full-size causal backward on the GPU; the oracle checks the sampled
+    (batch, KV head) groups: dQ of every query head of the group, and the
+    group's dK, dV (summed over its query heads, as the GQA rule says)."""
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, L, L, d, "bf16", seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    do = torch.randn(B, Hq, L, d, generator=g).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = ea.attn_fwd(qc, kc, vc, causal=True, scale=scale)
+    dq, dk, dv = ea.attn_bwd(qc, kc, vc, o, lse, doc, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert ea.attn_get_device_status() == "ATTN_OK"
+    per = Hq // Hkv
+    f = lambda t: t.float().numpy()
+    for b, kh in groups:
+        rk = np.zeros((L, d))
+        rv = np.zeros((L, d))
+        for h in range(kh * per, (kh + 1) * per):
+            gq, gk, gv, _ = orc.attention_backward(f(q[b, h]), f(k[b, kh]), f(v[b, kh]), f(do[b, h]),
+                                                   scale, True)
+            check_grad(to_np(dq[b, h]), gq, f"dQ[{b},{h}]")
+            rk += gk
+            rv += gv
+        check_grad(to_np(dk[b, kh]), rk, f"dK[{b},{kh}]")
+        check_grad(to_np(dv[b, kh]), rv, f"dV[{b},{kh}]")
+
+
+def test_gpt2_medium_shape_sampled_heads():
+    """The benchmarked GPT-2-medium shape (B 64, H 16, L 1024, d 64, causal):
+    three (batch, head) pairs from randperm(B * H, seed 3)."""
+    B, H = 64, 16
+    pick = torch.randperm(B * H, generator=torch.Generator().manual_seed(3))[:3].tolist()
+    run_sampled_groups(B, H, H, 1024, 64, [(i // H, i % H) for i in pick], seed=0)
+
+
+def test_llama3_8k_shape_sampled_group():
+    """The benchmarked Llama-3-8B shape (Hq 32, Hkv 8, L 8192, d 128, causal):
+    one KV head from randperm(Hkv, seed 3) with its four query heads."""
+    kh = int(torch.randperm(8, generator=torch.Generator().manual_seed(3))[0])
+    run_sampled_groups(1, 32, 8, 8192, 128, [(0, kh)], seed=0)

@@ -70,13 +70,17 @@ def test_many_sequences_sorted_list_and_fallback(d, B):
 
 
 def test_more_positions_than_the_item_list_holds():
-    """2500 sequences x 16 heads = 40000 items: at d = 128 that is 264
-    positions per CTA on 152 SMs, more than the item list holds, so the
-    batch keeps the round-robin order."""
+    """More positions per CTA than the 256-entry item list holds: the batch
+    keeps the round-robin order.  At d = 128 a CTA per SM takes
+    ceil(sequences x 16 heads / SMs) single-pair items (chunks of at most 128
+    queries), so the batch is sized from this GPU's SM count."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nseq, heads, list_items = 16 * sms + 100, 16, 256
+    assert -(-nseq * heads // sms) > list_items
     g = np.random.default_rng(77)
-    lens_q = g.integers(1, 129, 2500)
-    lens_k = lens_q + g.integers(0, 65, 2500)
-    run_varlen(lens_q.tolist(), lens_k.tolist(), 128, True, Hq=16, Hkv=2, seed=8)
+    lens_q = g.integers(1, 129, nseq)
+    lens_k = lens_q + g.integers(0, 65, nseq)
+    run_varlen(lens_q.tolist(), lens_k.tolist(), 128, True, Hq=heads, Hkv=2, seed=8)
 
 
 @pytest.mark.parametrize("causal", [False, True])

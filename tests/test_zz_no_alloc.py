@@ -1,12 +1,13 @@
-"""attn_decode_paged_noalloc against attn_decode_paged.
+"""attn_decode_paged_noalloc against the float64 oracle and attn_decode_paged.
 
 The allocation-free entry point serves callers that may not allocate device
 memory (it uses a fixed scratch array inside the library instead of a
-caller-provided workspace).  Its output must match the regular entry point,
-which takes an explicit workspace, within the bf16 tolerances the other
-parity tests use, on two calls in a row (the scratch keeps the previous
-call's contents, so the second call checks that nothing stale leaks in).
-This file is collected last so a failure here cannot hide the other tests.
+caller-provided workspace).  Its output must match the oracle's paged decode
+within the bf16 tolerances the other parity tests use, and the regular entry
+point (explicit workspace) within the same tolerances, on two calls in a row:
+the scratch keeps the previous call's contents, so the second call checks
+that nothing stale leaks in.  This file is collected last so a failure here
+cannot hide the other tests.
 """
 import ctypes
 import math
@@ -17,7 +18,8 @@ import torch
 
 import exact_attention_sm_gb300 as ea
 from exact_attention_sm_gb300 import inputs
-from tests.gpu_util import BF16_LSE, BF16_O_MAX, BF16_O_MEAN
+from oracle import attention as orc
+from tests.gpu_util import BF16_LSE, BF16_O_MAX, BF16_O_MEAN, check_lse, check_o, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +53,11 @@ def close(got_o, got_l, ref_o, ref_l):
     ([0, 70000, 333, 123457], 0),
 ])
 def test_noalloc_matches_workspace_entry_point(lens, num_splits):
-    q, kp, vp, table, sl = (t.cuda() for t in inputs.decode_inputs(lens, 32, 8, 128, seed=7))
+    host = inputs.decode_inputs(lens, 32, 8, 128, seed=7)
+    q, kp, vp, table, sl = (t.cuda() for t in host)
+    f = lambda t: t.float().numpy()
+    orc_o, orc_l = orc.decode_paged(f(host[0]), f(host[1]), f(host[2]), host[3].numpy(), lens,
+                                    1.0 / math.sqrt(128))
     ref_o, ref_l = ea.attn_decode_paged(q, kp, vp, table, sl, seq_lens_host=lens,
                                         num_splits=num_splits)
     for _ in range(2):
@@ -61,6 +67,8 @@ def test_noalloc_matches_workspace_entry_point(lens, num_splits):
         assert st == 0, ea.STATUS.get(st)
         torch.cuda.synchronize()
         assert ea.attn_get_device_status() == "ATTN_OK"
+        check_o(to_np(o), orc_o, "bf16")
+        check_lse(to_np(lse), orc_l, "bf16")
         close(o, lse, ref_o, ref_l)
 
 
