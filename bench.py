@@ -547,9 +547,26 @@ def e2e_prefill(torch, ea, steps, warmup, chunks=8, lanes=3):
 
 # ---------------------------------------------------------------- CPU oracle leg
 
+# Oracle legs of the CPU baseline: (workload, seconds of CPU work).  The main
+# workload runs twice (all host cores, then one core in a child process with
+# BLAS held to one thread); each other configuration gets a short sample.
+ORACLE_CONFIGS = [("single-head-f32-causal", 1.0), ("llama3-8b-prefill-8k", 2.5),
+                  ("llama3-8b-prefill-32k", 2.5), ("decode-b256-ctx1024", 2.5),
+                  ("decode-b4-long-splitkv", 2.5)]
+
+
+def full_work(name):
+    """The workload's whole-problem work in its unit's base (FLOPs or bytes)."""
+    w = WORKLOADS[name]
+    if w["kind"] == "prefill":
+        return prefill_flops(w)
+    return decode_bytes(w, decode_lens(w))
+
+
 def oracle_sample(name, budget_s):
     """Times the float64 oracle, as it stands, on a bounded sample of the
-    workload; returns (value in the workload's unit, seconds, sample text)."""
+    workload.  Returns a dict: value (the workload's unit), wall and CPU
+    seconds, the work done, and a description of the sample."""
     import numpy as np
     from exact_attention_sm_gb300 import inputs
     from oracle import attention as orc
@@ -558,28 +575,32 @@ def oracle_sample(name, budget_s):
         q, k, v = inputs.prefill_inputs(w["B"], w["Hq"], w["Hkv"], w["L"], w["L"], w["d"],
                                         w["dtype"], seed=0)
         qn, kn, vn = (t.float().numpy() for t in (q, k, v))
+        del q, k, v
         rows = inputs.sample_rows(w["B"], w["Hq"], w["L"], n_random=100000, seed=3)
-        done, flops, t0 = 0, 0.0, time.perf_counter()
+        batch_rows = 256 if w["L"] <= 1024 else 32
+        done, work, t0, c0 = 0, 0.0, time.perf_counter(), time.process_time()
         while done < len(rows) and time.perf_counter() - t0 < budget_s:
-            batch = rows[done:done + 256]
+            batch = rows[done:done + batch_rows]
             orc.prefill_rows(qn, kn, vn, 1.0 / math.sqrt(w["d"]), w["causal"], batch)
-            flops += prefill_flops(w, batch)
+            work += prefill_flops(w, batch)
             done += len(batch)
-        dt = time.perf_counter() - t0
-        return flops / dt / 1e12, dt, f"{done} sampled query rows (seeded), each the full dense row"
+        dt, cpu = time.perf_counter() - t0, time.process_time() - c0
+        return {"value": work / dt / 1e12, "unit": "TFLOP/s", "wall_s": dt, "cpu_s": cpu,
+                "work": work, "sample": f"{done} seeded query rows (full dense rows)"}
     lens = decode_lens(w)
     nreq = 1 if w["lens"] != "1024x256" else 16
     q, kp, vp, table, sl = inputs.decode_inputs(lens, w["Hq"], w["Hkv"], w["d"], seed=0)
     qn, kpn, vpn = (t.float().numpy() for t in (q, kp, vp))
-    done, nbytes, t0 = 0, 0.0, time.perf_counter()
+    done, work, t0, c0 = 0, 0.0, time.perf_counter(), time.process_time()
     while done < len(lens) and time.perf_counter() - t0 < budget_s:
         idx = list(range(done, min(done + nreq, len(lens))))
         orc.decode_paged(qn[idx], kpn, vpn, table.numpy()[idx], [lens[i] for i in idx],
                          1.0 / math.sqrt(w["d"]))
-        nbytes += decode_bytes(w, [lens[i] for i in idx])
+        work += decode_bytes(w, [lens[i] for i in idx])
         done += len(idx)
-    dt = time.perf_counter() - t0
-    return nbytes / dt / 1e9, dt, f"{done} of {len(lens)} requests, all heads"
+    dt, cpu = time.perf_counter() - t0, time.process_time() - c0
+    return {"value": work / dt / 1e9, "unit": "GB/s", "wall_s": dt, "cpu_s": cpu, "work": work,
+            "sample": f"{done} of {len(lens)} requests, all heads"}
 
 
 def cpu_cores():
@@ -589,26 +610,94 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def oracle_one_core(name, budget_s):
+    """The same oracle sample in a child process pinned to one core, with the
+    BLAS thread pools held to one thread (set before numpy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", name,
+                        "--cpu-budget", str(budget_s)], capture_output=True, text=True, env=env,
+                       timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr.strip().splitlines() or ["child failed"])[-1][:200]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_child(args):
+    try:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    except (AttributeError, OSError):
+        pass
+    print(json.dumps(oracle_sample(args.oracle_child, args.cpu_budget)), flush=True)
+
+
+def sig(x, n=4):
+    """x rounded to n significant digits (keeps the printed line short)."""
+    if x is None or not isinstance(x, float) or x == 0.0 or not math.isfinite(x):
+        return x
+    return round(x, n - 1 - int(math.floor(math.log10(abs(x)))))
+
+
+def cpu_baseline(main_name, budget_s, with_configs=True):
+    """The oracle timed on the host: the main workload on every core the
+    process may use (``cores`` = CPU seconds / wall seconds, the threads BLAS
+    actually kept busy; ``affinity_cores`` = the cores allowed), the same
+    sample on one core, and short samples of the other configurations.  Each
+    entry's ``full_s_extrapolated`` scales the sample's time to the whole
+    problem by the work ratio (FLOPs for prefill, KV bytes for decode): an
+    extrapolation, not a measurement."""
+    m = oracle_sample(main_name, budget_s)
+    one = oracle_one_core(main_name, max(2.0, budget_s / 2))
+    full = full_work(main_name)
+    out = {"value": m["value"], "unit": m["unit"],
+           "cores": max(1, round(m["cpu_s"] / m["wall_s"])), "kind": "oracle",
+           "sample": f"{m['sample']}; {m['wall_s']:.1f} s wall, {m['cpu_s']:.1f} s CPU",
+           "affinity_cores": cpu_cores(),
+           "full_s_extrapolated": sig(m["wall_s"] * full / m["work"])}
+    if "error" in one:
+        out["one_core"] = one
+    else:
+        out["one_core"] = {"value": sig(one["value"]), "cores": 1,
+                           "full_s_extrapolated": sig(one["wall_s"] * full / one["work"])}
+    if with_configs:
+        cfgs = {}
+        for name, b in ORACLE_CONFIGS:
+            if name == main_name:
+                continue
+            r = oracle_sample(name, b)
+            cfgs[name] = {"value": sig(r["value"], 3), "unit": r["unit"],
+                          "full_s_extrapolated": sig(r["wall_s"] * full_work(name) / r["work"], 3)}
+        out["configs"] = cfgs
+    return out
+
+
+def config_dict(name, world):
+    """The `config` object of a line: the same for the GPU and reference arms."""
+    return {"workload": describe(name), "l2": "flushed before every timed step (256 MiB write)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
     per_step = []
     for _ in range(args.warmup):
-        oracle_sample(MAIN, 1.0)
+        oracle_sample(MAIN, 0.5)
     sample = ""
     for _ in range(args.steps):
-        v, dt, sample = oracle_sample(MAIN, args.ref_budget)
-        per_step.append((v, dt))
-    value = sum(v for v, _ in per_step) / len(per_step)
-    ms = sum(dt for _, dt in per_step) / len(per_step) * 1e3
+        r = oracle_sample(MAIN, args.ref_budget)
+        per_step.append(r)
+        sample = r["sample"]
+    value = sum(r["value"] for r in per_step) / len(per_step)
+    ms = sum(r["wall_s"] for r in per_step) / len(per_step) * 1e3
+    cores = max(1, round(sum(r["cpu_s"] for r in per_step) / sum(r["wall_s"] for r in per_step)))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": describe(MAIN), "parallelism": "replicas"},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
-                             "kind": "oracle", "sample": sample},
+            "data": "synthetic", "config": config_dict(MAIN, world),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample, "affinity_cores": cpu_cores()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -664,23 +753,51 @@ def run_gpu(args):
         return
     cpu = None
     if world == 1 and not args.no_cpu:
-        v, dt, sample = oracle_sample(main_name, args.cpu_budget)
-        cpu = {"value": v, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{sample}; {dt:.1f} s of CPU time"}
+        cpu = cpu_baseline(main_name, args.cpu_budget, with_configs=not args.main_only)
     w = WORKLOADS[main_name]
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": w.get("dtype", "bf16"), "data": "synthetic",
-        "config": {"workload": res["workload"],
-                   "l2": "flushed before every timed step (256 MiB write)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": config_dict(main_name, world),
         "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches * args.steps, "clocks": clk.summary(),
-        "workloads": secondary,
     }
-    print(json.dumps(line), flush=True)
+    if args.detail:
+        # Full detail (every workload's description, roofline and extras).
+        with open(args.detail, "w") as f:
+            json.dump(dict(line, workloads=secondary), f, indent=1)
+    # stdout carries one compact line, short enough (under 3 KB) that a reader
+    # keeping only the tail of the output still sees every workload.
+    line["roofline"] = {k: sig(v) if isinstance(v, float) else v
+                        for k, v in res["roofline"].items() if k not in ("datasheet", "peak_source")}
+    line["roofline"]["peak_source"] = peak_src
+    if e2e is not None:
+        line["e2e"] = {k: sig(v) if isinstance(v, float) else v for k, v in e2e.items()
+                       if k != "pipeline"}
+    if line["clocks"]:
+        line["clocks"].pop("samples", None)
+    grouped = {}
+    for r in secondary:
+        unit, entry = compact(r)
+        grouped.setdefault(unit, []).append(entry)
+    line["workloads"] = grouped
+    print(json.dumps(line, separators=(",", ":")), flush=True)
+
+
+def compact(r):
+    """One workload's short entry (grouped by unit in the line): name, value,
+    mean ms, roofline fraction and DRAM traffic per launch (or its error)."""
+    name = r["workload"].split(":")[0]
+    if "error" in r:
+        return "error", {"name": name, "error": r["error"][:120]}
+    roof = r["roofline"]
+    out = {"name": name, "value": sig(r["value"]), "ms": sig(r["ms_per_step"], 3),
+           "frac": sig(roof["frac"], 3)}
+    if roof.get("traffic"):
+        out["traffic"] = sig(float(roof["traffic"]), 3)
+    return r["unit"], out
 
 
 def main():
@@ -692,9 +809,14 @@ def main():
     ap.add_argument("--workload", default=MAIN, choices=sorted(WORKLOADS))
     ap.add_argument("--main-only", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=8.0)
     ap.add_argument("--ref-budget", type=float, default=2.0)
+    ap.add_argument("--detail", default=None, help="also write the full per-workload JSON here")
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
