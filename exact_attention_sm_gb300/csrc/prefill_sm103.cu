@@ -88,6 +88,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// s if column c <= kv (visible), else -inf: one compare and one select.
+__device__ __forceinline__ float mask_col(float s, int c, int kv) {
+  float r;
+  asm("{\n\t.reg .pred q;\n\tsetp.gt.s32 q, %2, %3;\n\tselp.f32 %0, 0fFF800000, %1, q;\n\t}"
+      : "=f"(r)
+      : "f"(s), "r"(c), "r"(kv));
+  return r;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -832,10 +841,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool need_mask = kPacked ? tile_needs_mask(w.sq, w.qt[x], j, causal)
                                        : (j == n - 1) && (causal || (geo.Lk % BN) != 0);
         if (need_mask) {
-          const int kmax = row_kmax(w.sq, grow, causal);  // last visible key
+          // Element mask by compare-and-select (straight-line, no branches).
+          const int kv = row_kmax(w.sq, grow, causal) - j * BN;  // last visible column
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (j * BN + c > kmax) s[c] = -INFINITY;
+          for (int c = 0; c < BN; ++c) s[c] = mask_col(s[c], c, kv);
         }
         // Row max as 8 independent chains (short dependency depth).
         float mx[8];
@@ -963,14 +972,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // other's gaps on the tensor core and on the MUFU.
 //   TMEM columns (per CTA): S 0..127, P 128..191 (bf16 pairs), O 192..255.
 // P has its own columns, so S(t+1) is written while the softmax still works
-// on P(t).  Each MMA group waits on ONE barrier that already combines what it
-// needs:
-//   qk_ready[slot of tile t]: K(t) arrived and the softmax has read S(t-1);
-//   pv_ready[slot of tile t]: V(t) arrived and the softmax wrote P(t).
-// A forwarder warp turns the TMA completions (k_full, v_full) into one
-// arrival each; each softmax warp adds one.  pv_done[slot] (one commit per
-// PV) releases the K/V slot to the producer and tells the softmax that P and
-// O may be rewritten.  Work items are single Q tiles.
+// on P(t).  Two threads issue the MMAs: one the QK^T groups, one the PV
+// groups.  tcgen05.mma issue blocks while the tensor pipe is busy (its queue
+// holds about one MMA), so with a single issuer S(t+1) waited behind the
+// eight MMAs of PV(t-1); with two, each group goes out as soon as its inputs
+// are ready and the pipe interleaves them.
+//   QK issuer: S(t) once K(t) has landed (k_full) and the softmax has read
+//              S(t-1) (s_read); commits s_full and k_done.
+//   PV issuer: PV(t) once V(t) has landed (v_full) and the softmax wrote P(t)
+//              (p_ready); commits pv_done (V slot free, P and O may be
+//              rewritten) and, after an item's last PV, o_done.
+// Epilogue (dense layout): the softmax threads write O / l as bf16 rows into
+// the item's Q buffer (its last QK^T is done) in the tensor map's 128-byte
+// swizzle, and the Q producer stores the tile with one TMA copy before it
+// refills that buffer; rows past L are clipped by the map.  Packed and paged
+// layouts store rows directly (a tile may reach into the next sequence).
+// Work items are single Q tiles.
 struct Cfg64 {
   static constexpr int D = 64;
   static constexpr int THREADS = 256;            // 8 warps; two CTAs per SM
@@ -1048,6 +1065,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     prefill_bf16_d64_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_o,
                             __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int BH, int Hq,
                             int Hkv, const Geo geo, int causal, float scale_log2, int q_div,
                             int* status) {
@@ -1055,6 +1073,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   constexpr int D = C::D, NS = C::NS, NQ = C::NQ;
   constexpr bool kPacked = kLayout != kDenseLayout;
   constexpr bool kPaged = kLayout == kPagedLayout;
+  constexpr bool kTmaStore = kLayout == kDenseLayout;  // O tile through the Q buffer
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -1062,19 +1081,21 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;                 // [NQ]
-  uint64_t* q_empty = q_full + NQ;         // [NQ]
-  uint64_t* k_full = q_empty + NQ;         // [NS] TMA only
-  uint64_t* v_full = k_full + NS;          // [NS] TMA only
-  uint64_t* qk_ready = v_full + NS;        // [NS]
-  uint64_t* pv_ready = qk_ready + NS;      // [NS]
-  uint64_t* pv_done = pv_ready + NS;       // [NS] PV of the slot's tile done (V slot free)
-  uint64_t* k_done = pv_done + NS;         // [NS] QK^T of the slot's tile done (K slot free)
-  uint64_t* s_full = k_done + NS;
-  uint64_t* o_done = s_full + 1;
+  uint64_t* q_empty = q_full + NQ;         // [NQ] packed / paged: the item's last QK^T done
+  uint64_t* k_full = q_empty + NQ;         // [NS] TMA
+  uint64_t* v_full = k_full + NS;          // [NS] TMA
+  uint64_t* k_done = v_full + NS;          // [NS] QK^T of the slot's tile done (K slot free)
+  uint64_t* pv_done = k_done + NS;         // [NS] PV of the slot's tile done (V slot free)
+  uint64_t* s_full = pv_done + NS;         // S(t) written
+  uint64_t* s_read = s_full + 1;           // the softmax has read S(t) (one arrival per warp)
+  uint64_t* p_ready = s_read + 1;          // the softmax wrote P(t) (one arrival per warp)
+  uint64_t* o_done = p_ready + 1;
   uint64_t* o_free = o_done + 1;
-  uint64_t* drain = o_free + 1;
+  uint64_t* st_ready = o_free + 1;         // dense: the item's O rows are staged (per warp)
+  uint64_t* drain = st_ready + 1;          // both issuers' MMAs complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  static_assert(8 * (6 * 2 + 7) + 8 <= 256, "d = 64 barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_qt = (geo.Lq + BM - 1) / BM;
@@ -1124,15 +1145,16 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&qk_ready[s], C::kSoftmaxWarps + 1);
-      mbar_init(&pv_ready[s], C::kSoftmaxWarps + 1);
-      mbar_init(&pv_done[s], 1);
       mbar_init(&k_done[s], 1);
+      mbar_init(&pv_done[s], 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(s_read, C::kSoftmaxWarps);
+    mbar_init(p_ready, C::kSoftmaxWarps);
     mbar_init(o_done, 1);
-    mbar_init(o_free, 128);
-    mbar_init(drain, 1);
+    mbar_init(o_free, C::kSoftmaxWarps);
+    mbar_init(st_ready, C::kSoftmaxWarps);
+    mbar_init(drain, 2);
     *abort_flag = (status != nullptr &&
                    *reinterpret_cast<volatile int*>(status) == ATTN_ERR_DEVICE_TIMEOUT) ? 2 : 0;
     fence_mbar_init();
@@ -1164,10 +1186,13 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   auto wait = [&](uint64_t* bar, int parity) {
     return mbar_wait(bar, static_cast<uint32_t>(parity) & 1u, abort_flag, kWaitLimitNs);
   };
+  constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+  constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+  constexpr uint64_t kTileStep = C::TILE_BYTES >> 4;
 
   if (warp < 4) {
-    // 128 x 64 + 128 x 192 registers = the 256 x 128 the CTA launched with.
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+    // 128 x 72 + 128 x 184 registers = the 256 x 128 the CTA launched with.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       // K runs one tile ahead of V: a K slot frees when its QK^T is done
@@ -1251,24 +1276,44 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         mbar_wait(&v_full[u % NS], (u / NS) & 1, &no_abort, kWaitLimitNs);
     } else if (warp == 3 && lane == 0) {
       // ---------------------------------------------------------- Q producer
-      // Q tiles go out as soon as their buffer frees (the item NQ back has
-      // issued its last S), about an item ahead of the K/V stream.
+      // Q tiles go out as soon as their buffer frees, about an item ahead of
+      // the K/V stream.  Dense layout: the buffer of the item NQ back holds
+      // that item's staged O tile, which is stored first.
       prefetch_tmap(&tm_q);
+      if constexpr (kTmaStore) prefetch_tmap(&tm_o);
       int nq = 0;
       bool ok = true;
       Item1 w;
+      int back_bh[NQ], back_qt[NQ];  // dense: the item whose O a buffer holds
+      auto store_o = [&](int i) -> bool {  // O tile of the nq-th item i (dense)
+        const int qs = i % NQ;
+        if (!wait(st_ready, i)) return false;
+        tma_store_3d(&tm_o, smem + C::OFF_Q + qs * C::TILE_BYTES, 0, back_qt[qs] * BM, back_bh[qs]);
+        bulk_commit_group();
+        bulk_wait_read_all();
+        return true;
+      };
       for (int it = next_active(sched.first, w); ok && it < sched.last;
            it = next_active(it + sched.step, w)) {
         const int qs = nq % NQ;
-        if (nq >= NQ && !wait(&q_empty[qs], (nq / NQ) - 1)) {
-          ok = false;
-          break;
+        if (nq >= NQ) {
+          if constexpr (kTmaStore) ok = store_o(nq - NQ);
+          else ok = wait(&q_empty[qs], (nq / NQ) - 1);
+          if (!ok) break;
+        }
+        if constexpr (kTmaStore) {
+          back_bh[qs] = w.bh;
+          back_qt[qs] = w.qt;
         }
         mbar_arrive_expect_tx(&q_full[qs], C::TILE_BYTES);
         tma_load_3d(smem + C::OFF_Q + qs * C::TILE_BYTES, &tm_q, &q_full[qs], 0,
                     packed ? w.bh % Hq : w.qt * BM,
                     packed ? w.sq.q_off + w.qt * BM : w.bh / q_div);
         ++nq;
+      }
+      if constexpr (kTmaStore) {
+        for (int i = nq > NQ ? nq - NQ : 0; ok && i < nq; ++i) ok = store_o(i);
+        bulk_wait_all();  // every O store has completed before the CTA exits
       }
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
@@ -1277,114 +1322,82 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       int no_abort = 0;
       for (int i = nq > NQ ? nq - NQ : 0; i < nq; ++i)
         mbar_wait(&q_full[i % NQ], (i / NQ) & 1, &no_abort, kWaitLimitNs);
-    } else if (warp == 2 && lane == 0) {
-      // ---------------------------------------------------------- forwarder
-      int total = 0;
-      for (int it = sched.first; it < sched.last; it += sched.step) total += item_at(it).n;
-      // Same order as the loads: K one tile ahead of V.
-      bool ok = total == 0 || wait(&k_full[0], 0);
-      if (ok && total > 0) mbar_arrive(&qk_ready[0]);
-      for (int t = 0; ok && t < total; ++t) {
-        if (t + 1 < total) {
-          ok = wait(&k_full[(t + 1) % NS], (t + 1) / NS);
-          if (!ok) break;
-          mbar_arrive(&qk_ready[(t + 1) % NS]);
-        }
-        ok = wait(&v_full[t % NS], t / NS);
-        if (!ok) break;
-        mbar_arrive(&pv_ready[t % NS]);
-      }
-      if (!ok) {
-        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
-        *abort_flag = 1;
-      }
     } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+      // ---------------------------------------------------------- QK issuer
       // Descriptors are built once; a K step or a ring slot only moves the
       // start-address field (address >> 4), which never carries (shared
       // addresses stay below 256 KB).
       const uint64_t q_desc0 = smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
-      const uint64_t v_desc0 = smem_desc_sw128(sbase + C::OFF_V, C::TILE_BYTES, 1024);
-      constexpr uint64_t kTileStep = C::TILE_BYTES >> 4;
-      int nq = 0;      // Q tiles done with (last S issued)
-      int nitem = 0;   // items whose first PV was issued
+      int nq = 0;  // items started
+      int t = 0;   // global step
       bool ok = true;
-      // S = Q K(t)^T; j is the step within an item of n steps.
-      auto qk = [&](int j, int n, int t) {
-        const uint64_t kd = k_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
+      Item1 w;
+      for (int it = next_active(sched.first, w); ok && it < sched.last;
+           it = next_active(it + sched.step, w)) {
         const uint64_t qd = q_desc0 + static_cast<uint64_t>(nq % NQ) * kTileStep;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_bf16_ss(tmem, qd + k * 2, kd + k * 2, idesc_qk, k > 0 ? 1u : 0u);
-        mma_commit(s_full);
-        mma_commit(&k_done[t % NS]);
-        if (j + 1 == n) {
-          mma_commit(&q_empty[nq % NQ]);  // that Q slot may be refilled
-          ++nq;
-        }
-      };
-      int t = 0;  // global step of the current item's K/V tile 0
-      Item1 w, w2{};
-      int it = next_active(sched.first, w);
-      if (it < sched.last) {
-        ok = wait(&qk_ready[0], 0) && wait(&q_full[0], 0);
-        if (ok) {
-          tc_fence_after();
-          qk(0, w.n, 0);
-        }
-      }
-      while (ok && it < sched.last) {
-        const int it2 = next_active(it + sched.step, w2);
-        for (int j = 0; ok && j < w.n; ++j) {
-          const int tt = t + j;
-          // S for step tt + 1: the next K/V tile of this item or the first
-          // of the next item.
-          if (j + 1 < w.n) {
-            if (!wait(&qk_ready[(tt + 1) % NS], (tt + 1) / NS)) { ok = false; break; }
-            tc_fence_after();
-            qk(j + 1, w.n, tt + 1);
-          } else if (it2 < sched.last) {
-            if (!wait(&qk_ready[(tt + 1) % NS], (tt + 1) / NS) ||
-                !wait(&q_full[nq % NQ], nq / NQ)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            qk(0, w2.n, tt + 1);
-          }
-          // O (+)= P V for step tt.
-          if (!wait(&pv_ready[tt % NS], tt / NS) ||
-              (j == 0 && nitem > 0 && !wait(o_free, nitem - 1))) {
+        if (!wait(&q_full[nq % NQ], nq / NQ)) { ok = false; break; }
+        for (int j = 0; j < w.n; ++j, ++t) {
+          if (!wait(&k_full[t % NS], t / NS) || (t > 0 && !wait(s_read, t - 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t vd = v_desc0 + static_cast<uint64_t>(tt % NS) * kTileStep;
+          const uint64_t kd = k_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            mma_bf16_ts(tmem + C::O_COL, tmem + C::P_COL + k * 8, vd + static_cast<uint64_t>(k) * 128,
-                        idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&pv_done[tt % NS]);
-          if (j == 0) ++nitem;
-          if (j + 1 == w.n) mma_commit(o_done);
+          for (int k = 0; k < D / 16; ++k)
+            mma_bf16_ss(tmem, qd + k * 2, kd + k * 2, idesc_qk, k > 0 ? 1u : 0u);
+          mma_commit(s_full);
+          mma_commit(&k_done[t % NS]);
+          if constexpr (!kTmaStore)
+            if (j + 1 == w.n) mma_commit(&q_empty[nq % NQ]);  // that Q buffer may be refilled
         }
-        t += w.n;
-        it = it2;
-        w = w2;
+        ++nq;
       }
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
       }
-      int no_abort = 0;
       mma_commit(drain);
-      mbar_wait(drain, 0, &no_abort, kWaitLimitNs);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------------------------------------------------- PV issuer
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + C::OFF_V, C::TILE_BYTES, 1024);
+      int nitem = 0;
+      int t = 0;
+      bool ok = true;
+      Item1 w;
+      for (int it = next_active(sched.first, w); ok && it < sched.last;
+           it = next_active(it + sched.step, w)) {
+        for (int j = 0; j < w.n; ++j, ++t) {
+          if (!wait(&v_full[t % NS], t / NS) || !wait(p_ready, t) ||
+              (j == 0 && nitem > 0 && !wait(o_free, nitem - 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            mma_bf16_ts(tmem + C::O_COL, tmem + C::P_COL + k * 8, vd + static_cast<uint64_t>(k) * 128,
+                        idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&pv_done[t % NS]);
+          if (j + 1 == w.n) mma_commit(o_done);
+        }
+        ++nitem;
+      }
+      if (!ok) {
+        attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      mma_commit(drain);
+    }
+    if (warp == 1 || warp == 2) {
+      // Drain: all MMAs of both issuers are complete before teardown.
+      int no_abort = 0;
+      if (lane == 0) mbar_wait(drain, 0, &no_abort, kWaitLimitNs);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
     // ------------------------------------------------------------ softmax warps
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;  // row within the Q tile == TMEM lane
@@ -1392,9 +1405,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     const uint32_t s_addr = tmem + lane_off;
     const uint32_t p_addr = tmem + lane_off + C::P_COL;
     const uint32_t o_addr = tmem + lane_off + C::O_COL;
-    // Nothing was read before the first S: this warp's share of qk_ready(0).
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&qk_ready[0]);
     int t = 0;       // global step of the current item's K/V tile 0
     int nitem = 0;
     bool ok = true;
@@ -1431,15 +1441,15 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         // S is in registers: S(tt + 1) may overwrite it.
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&qk_ready[(tt + 1) % NS]);
+        if (lane == 0) mbar_arrive(s_read);
 
         const bool need_mask = kPacked ? tile_needs_mask(w.sq, w.qt, j, causal)
                                        : (j == n - 1) && (causal || (geo.Lk % BN) != 0);
         if (need_mask) {
-          const int kmax = row_kmax(w.sq, grow, causal);  // last visible key
+          // Element mask by compare-and-select (straight-line, no branches).
+          const int kv = row_kmax(w.sq, grow, causal) - j * BN;  // last visible column
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (j * BN + c > kmax) s[c] = -INFINITY;
+          for (int c = 0; c < BN; ++c) s[c] = mask_col(s[c], c, kv);
         }
         float mx[8];
 #pragma unroll
@@ -1506,7 +1516,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pv_ready[tt % NS]);
+        if (lane == 0) mbar_arrive(p_ready);
       }
       if (ok) ok = __all_sync(FULL, wait(o_done, nitem));
       if (!ok) break;
@@ -1518,23 +1528,37 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       tmem_ld32(o_addr + 32, r[1]);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(o_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (grow < w.sq.lq) {
-        __nv_bfloat16* orow = o + orow_index * D;
+      uint4 q4[8];
 #pragma unroll
-        for (int v8 = 0; v8 < 8; ++v8) {
-          const uint32_t* rv = &r[v8 >> 2][(v8 & 3) * 8];
-          uint4 q4;
-          q4.x = attn::pack_bf16x2(__uint_as_float(rv[0]) * inv, __uint_as_float(rv[1]) * inv);
-          q4.y = attn::pack_bf16x2(__uint_as_float(rv[2]) * inv, __uint_as_float(rv[3]) * inv);
-          q4.z = attn::pack_bf16x2(__uint_as_float(rv[4]) * inv, __uint_as_float(rv[5]) * inv);
-          q4.w = attn::pack_bf16x2(__uint_as_float(rv[6]) * inv, __uint_as_float(rv[7]) * inv);
-          *reinterpret_cast<uint4*>(orow + v8 * 8) = q4;
-        }
-        if (lse != nullptr)
-          lse[orow_index] = l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
+      for (int v8 = 0; v8 < 8; ++v8) {
+        const uint32_t* rv = &r[v8 >> 2][(v8 & 3) * 8];
+        q4[v8].x = attn::pack_bf16x2(__uint_as_float(rv[0]) * inv, __uint_as_float(rv[1]) * inv);
+        q4[v8].y = attn::pack_bf16x2(__uint_as_float(rv[2]) * inv, __uint_as_float(rv[3]) * inv);
+        q4[v8].z = attn::pack_bf16x2(__uint_as_float(rv[4]) * inv, __uint_as_float(rv[5]) * inv);
+        q4[v8].w = attn::pack_bf16x2(__uint_as_float(rv[6]) * inv, __uint_as_float(rv[7]) * inv);
       }
+      if constexpr (kTmaStore) {
+        // Row `row` of the tile into this item's Q buffer (its QK^T MMAs are
+        // complete), 16-byte chunk c at position c ^ (row % 8) of the
+        // 128-byte row: the map's swizzle.  Rows past L are clipped by the
+        // store, so every row is written.
+        uint8_t* buf = smem + C::OFF_Q + (nitem % NQ) * C::TILE_BYTES + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(buf + ((c ^ (row & 7)) << 4)) = q4[c];
+        fence_proxy_async_smem();  // visible to the TMA store
+        __syncwarp();
+        if (lane == 0) mbar_arrive(st_ready);
+      } else if (grow < w.sq.lq) {
+        uint4* orow = reinterpret_cast<uint4*>(o + orow_index * D);
+#pragma unroll
+        for (int v8 = 0; v8 < 8; ++v8) orow[v8] = q4[v8];
+      }
+      if (grow < w.sq.lq && lse != nullptr)
+        lse[orow_index] = l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
       ++nitem;
       t += n;
     }
@@ -1652,7 +1676,7 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
       return ATTN_ERR_CUDA;
     attr_set[dev] = true;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (q_div < 1 || (B * Hq) % q_div != 0) return ATTN_ERR_INVALID_ARG;
   bool maps_ok;
   if constexpr (kLayout == kPagedLayout)
@@ -1666,6 +1690,9 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   else
     maps_ok = make_map(&mq, q, D, geo.Lq, B * Hq / q_div) && make_map(&mk, k, D, geo.Lk, B * Hkv) &&
               make_map(&mv, v, D, geo.Lk, B * Hkv);
+  // The d = 64 dense kernel stores O tiles by TMA (the other layouts ignore mo).
+  if (maps_ok && kD64 && kLayout == kDenseLayout) maps_ok = make_map(&mo, o, D, geo.Lq, B * Hq);
+  else mo = mq;
   if (!maps_ok) return ATTN_ERR_CUDA;
   const int num_qt = (geo.Lq + BM - 1) / BM;
   const long long items = static_cast<long long>(B) * Hq * (kD64 ? num_qt : (num_qt + 1) / 2);
@@ -1677,7 +1704,7 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   const float scale_log2 = scale * attn::kLog2e;
   if constexpr (kD64) {
     prefill_bf16_d64_kernel<kLayout><<<grid, Cfg64::THREADS, smem_bytes, stream>>>(
-        mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, geo, causal,
+        mq, mk, mv, mo, static_cast<__nv_bfloat16*>(o), lse, B * Hq, Hq, Hkv, geo, causal,
         scale_log2, q_div, attn_host::device_status_ptr());
   } else {
     prefill_bf16_kernel<D, kLayout><<<grid, NUM_THREADS, smem_bytes, stream>>>(
