@@ -428,6 +428,42 @@ def prefill_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_k, sc
     return o, lse
 
 
+def prefill_bsr(q, k_blocks, v_blocks, kv_indptr, kv_indices, cu_seqlens_q, seq_lens_k, scale,
+                causal):
+    """Prefill against a KV cache addressed in block-sparse-row (BSR) form.
+
+    [Lecture 4] section 5.2: the "query rows x physical KV blocks" matrix of
+    a batch is block-sparse; in BSR form indices lists the non-zero blocks
+    (physical block ids) of every row end to end and row r's blocks are
+    indices[indptr[r] : indptr[r + 1]].  A page table is this matrix with
+    block size 16 (vLLM), a radix tree with block size 1 (SGLang); the
+    attention over the blocks gathered in order equals the attention over
+    the contiguous KV ("max difference 0").  Here row r is request r: its
+    keys are tokens 0 .. seq_lens_k[r] - 1, token t in block
+    indices[indptr[r] + t // block_size], slot t % block_size, with
+    k_blocks, v_blocks [num_blocks, block_size, Hkv, d].  Queries are packed
+    (cu_seqlens_q) and causal is aligned bottom-right, as in prefill_paged.
+
+    Returns O [total_q, Hq, d] and LSE [total_q, Hq].
+    """
+    q = _f64(q)
+    hq = q.shape[1]
+    hkv = k_blocks.shape[2]
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:2])
+    for b in range(len(cu_seqlens_q) - 1):
+        q0, q1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        lk = int(seq_lens_k[b])
+        row = np.asarray(kv_indices[int(kv_indptr[b]):int(kv_indptr[b + 1])])
+        for h in range(hq):
+            kh = kv_head_of(h, hq, hkv)
+            kk = paged_gather(k_blocks, row, lk, kh)
+            vv = paged_gather(v_blocks, row, lk, kh)
+            oo, ll, _, _ = attention_dense(q[q0:q1, h], kk, vv, scale, causal, lk - (q1 - q0))
+            o[q0:q1, h], lse[q0:q1, h] = oo, ll
+    return o, lse
+
+
 def decode_split_states(q_row, keys, values, scale, chunk):
     """Split-KV partial states of one query row (Flash-Decoding).
 

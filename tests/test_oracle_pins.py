@@ -763,3 +763,66 @@ def test_balanced_plan_lpt_bound_against_brute_force():
         # each CTA received its units from the longest down
         for c in cta_units:
             assert all(cost[a] >= cost[b] for a, b in zip(c, c[1:]))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bsr_prefill_lecture_5_2_example(causal):
+    """[Lecture 4] section 5.2: the three requests (19, 10, 29 tokens, block
+    size 4) in the page's BSR form (indptr [0, 5, 8, 16] and its indices)
+    give exactly the attention of the block-table form ('max difference 0')
+    and, within float64 rounding, torch's attention over the contiguous K/V."""
+    g = GOLD["lecture_bsr_page_tables"]
+    bs, lens = g["block_size"], g["seq_lens"]
+    indptr, indices = np.array(g["indptr"]), np.array(g["indices"])
+    rng = np.random.default_rng(21)
+    hq, hkv, d = 4, 2, 8
+    kb = rng.standard_normal((24, bs, hkv, d))
+    vb = rng.standard_normal((24, bs, hkv, d))
+    lq = [7, 10, 29]
+    cu = np.concatenate([[0], np.cumsum(lq)])
+    q = rng.standard_normal((int(cu[-1]), hq, d))
+    o, lse = orc.prefill_bsr(q, kb, vb, indptr, indices, cu, lens, 0.3, causal)
+    table = np.full((3, 8), -1)
+    for b, t in enumerate(g["tables"]):
+        table[b, :len(t)] = t
+    o_t, lse_t = orc.prefill_paged(q, kb, vb, table, cu, lens, 0.3, causal)
+    assert np.array_equal(o, o_t) and np.array_equal(lse, lse_t)
+    for b in range(3):
+        blocks = indices[indptr[b]:indptr[b + 1]]
+        k = kb[blocks].reshape(-1, hkv, d)[:lens[b]]
+        v = vb[blocks].reshape(-1, hkv, d)[:lens[b]]
+        mask = np.ones((lq[b], lens[b]), bool)
+        if causal:
+            mask = np.arange(lens[b])[None, :] <= np.arange(lq[b])[:, None] + lens[b] - lq[b]
+        qq = q[cu[b]:cu[b + 1]].transpose(1, 0, 2)
+        kk = np.repeat(k, hq // hkv, 1).transpose(1, 0, 2)
+        vv = np.repeat(v, hq // hkv, 1).transpose(1, 0, 2)
+        o_ref, lse_ref = _sdpa64_mask(qq, kk, vv, 0.3, mask)
+        assert np.abs(o[cu[b]:cu[b + 1]] - o_ref.transpose(1, 0, 2)).max() < 1e-12
+        assert np.abs(lse[cu[b]:cu[b + 1]] - lse_ref.T).max() < 1e-12
+
+
+def test_bsr_prefill_block_size_one():
+    """Block size 1 (the radix-tree layout, [Lecture 4] exercise 9(a)): every
+    token its own block, at a shuffled position of the pool; equals the
+    attention over the tokens in logical order (torch float64)."""
+    rng = np.random.default_rng(22)
+    lens, hq, hkv, d = [13, 1, 30], 2, 1, 8
+    pool = rng.permutation(sum(lens) + 5)
+    kb = rng.standard_normal((len(pool), 1, hkv, d))
+    vb = rng.standard_normal((len(pool), 1, hkv, d))
+    indptr = np.concatenate([[0], np.cumsum(lens)])
+    indices = pool[:sum(lens)]
+    lq = [4, 1, 30]
+    cu = np.concatenate([[0], np.cumsum(lq)])
+    q = rng.standard_normal((int(cu[-1]), hq, d))
+    o, lse = orc.prefill_bsr(q, kb, vb, indptr, indices, cu, lens, 0.35, True)
+    for b in range(3):
+        tok = indices[indptr[b]:indptr[b + 1]]
+        k, v = kb[tok, 0], vb[tok, 0]
+        mask = np.arange(lens[b])[None, :] <= np.arange(lq[b])[:, None] + lens[b] - lq[b]
+        qq = q[cu[b]:cu[b + 1]].transpose(1, 0, 2)
+        o_ref, lse_ref = _sdpa64_mask(qq, np.repeat(k, hq, 1).transpose(1, 0, 2),
+                                      np.repeat(v, hq, 1).transpose(1, 0, 2), 0.35, mask)
+        assert np.abs(o[cu[b]:cu[b + 1]] - o_ref.transpose(1, 0, 2)).max() < 1e-12
+        assert np.abs(lse[cu[b]:cu[b + 1]] - lse_ref.T).max() < 1e-12
