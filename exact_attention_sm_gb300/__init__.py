@@ -30,6 +30,8 @@ SIGNATURES = {
                              _I, _P]),
     "attn_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                 _I, _I, _I, _F, _I, _P]),
+    "attn_prefill_bsr": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                              _I, _I, _I, _F, _I, _P]),
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ,
                       _I, _P]),
@@ -158,9 +160,9 @@ def attn_prefill_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_
                        max_seqlen_q=None, max_seqlen_k=None, causal=False, scale=None, out=None,
                        lse=None, want_lse=True, stream=None):
     """Chunked prefill against a paged cache. q [total_q,Hq,d] bf16 packed by cu_seqlens_q
-    (int32 [B+1], device); k_pages/v_pages [num_pages,16,Hkv,d] bf16; block_table int32
-    [B,max_pages]; seq_lens_k int32 [B] (device). Causal is aligned bottom-right.
-    Returns (o [total_q,Hq,d], lse [total_q,Hq])."""
+    (int32 [B+1], device); k_pages/v_pages [num_pages,page_size,Hkv,d] bf16 (page_size a
+    power of two, 1..128); block_table int32 [B,max_pages]; seq_lens_k int32 [B] (device).
+    Causal is aligned bottom-right. Returns (o [total_q,Hq,d], lse [total_q,Hq])."""
     for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"), (block_table, "block_table"),
                  (cu_seqlens_q, "cu_seqlens_q"), (seq_lens_k, "seq_lens_k")):
         _need(t, n)
@@ -187,6 +189,44 @@ def attn_prefill_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_
                                   page_size, block_table.shape[1], num_pages, 1 if causal else 0,
                                   float(scale), _dtype_code(q), _stream(stream))
     _check(st, "attn_prefill_paged")
+    return out, lse
+
+
+def attn_prefill_bsr(q, k_blocks, v_blocks, kv_indptr, kv_indices, cu_seqlens_q, seq_lens_k,
+                     max_seqlen_q=None, max_seqlen_k=None, causal=False, scale=None, out=None,
+                     lse=None, want_lse=True, stream=None):
+    """Prefill against a KV cache in block-sparse-row form. q [total_q,Hq,d] bf16 packed by
+    cu_seqlens_q; k_blocks/v_blocks [num_blocks,block_size,Hkv,d] bf16; request b's blocks
+    are kv_indices[kv_indptr[b]:kv_indptr[b+1]] (int32, device); seq_lens_k int32 [B].
+    Returns (o [total_q,Hq,d], lse [total_q,Hq])."""
+    for t, n in ((q, "q"), (k_blocks, "k_blocks"), (v_blocks, "v_blocks"),
+                 (kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"),
+                 (cu_seqlens_q, "cu_seqlens_q"), (seq_lens_k, "seq_lens_k")):
+        _need(t, n)
+    for t in (kv_indptr, kv_indices, cu_seqlens_q, seq_lens_k):
+        if t.dtype != torch.int32:
+            raise TypeError("kv_indptr, kv_indices, cu_seqlens_q and seq_lens_k must be int32")
+    total_q, Hq, d = q.shape
+    num_blocks, block_size, Hkv, _ = k_blocks.shape
+    B = cu_seqlens_q.numel() - 1
+    if max_seqlen_q is None:
+        cq = cu_seqlens_q.cpu()
+        max_seqlen_q = int((cq[1:] - cq[:-1]).max()) if B > 0 else 1
+    if max_seqlen_k is None:
+        max_seqlen_k = int(seq_lens_k.max()) if B > 0 else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(total_q, Hq, dtype=torch.float32, device=q.device)
+    st = lib().attn_prefill_bsr(_ptr(q), _ptr(k_blocks), _ptr(v_blocks), _ptr(kv_indptr),
+                                _ptr(kv_indices), kv_indices.numel(), _ptr(cu_seqlens_q),
+                                _ptr(seq_lens_k), _ptr(out), _ptr(lse), B,
+                                max(1, int(max_seqlen_q)), int(max_seqlen_k), total_q, Hq, Hkv, d,
+                                block_size, num_blocks, 1 if causal else 0, float(scale),
+                                _dtype_code(q), _stream(stream))
+    _check(st, "attn_prefill_bsr")
     return out, lse
 
 

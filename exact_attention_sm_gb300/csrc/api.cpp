@@ -22,8 +22,9 @@ attn_status_t launch_prefill_f32(const float*, const float*, const float*, float
 attn_status_t launch_prefill_bf16(const void*, const void*, const void*, void*, float*, int, int,
                                   int, int, int, int, int, float, int, cudaStream_t);
 attn_status_t launch_prefill_bf16_paged(const void*, const void*, const void*, const int*,
-                                        const int*, const int*, void*, float*, int, int, int, int,
-                                        int, int, int, int, int, int, float, cudaStream_t);
+                                        const int*, int, int, const int*, const int*, void*, float*,
+                                        int, int, int, int, int, int, int, int, int, int, float,
+                                        cudaStream_t);
 attn_status_t launch_prefill_bf16_varlen(const void*, const void*, const void*, void*, float*,
                                          const int*, const int*, int, int, int, int, int, int, int,
                                          int, int, float, cudaStream_t);
@@ -303,9 +304,10 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void*
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if (page_size > 128 || (page_size & (page_size - 1)) != 0) return ATTN_ERR_UNSUPPORTED;
   if ((int64_t)max_seqlen_k > (int64_t)max_pages_per_seq * page_size) return ATTN_ERR_INVALID_ARG;
-  if ((int64_t)B * max_pages_per_seq > 0x7fffffffLL || num_pages == 0x7fffffff)
+  if ((int64_t)B * max_pages_per_seq > 0x7fffffffLL || num_pages == 0x7fffffff ||
+      (int64_t)num_pages * page_size > 0x7fffffffLL)
     return ATTN_ERR_UNSUPPORTED;
   if ((int64_t)B * Hq > (1 << 24) || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
@@ -314,9 +316,43 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void*
       (reinterpret_cast<uintptr_t>(seq_lens_k) & 3u) != 0)
     return ATTN_ERR_INVALID_ARG;
   return attn_host::launch_prefill_bf16_paged(
-      q, k_pages, v_pages, block_table, cu_seqlens_q, seq_lens_k, o, lse, B, max_seqlen_q,
-      std::max(max_seqlen_k, 1), total_q, Hq, Hkv, d, max_pages_per_seq, num_pages,
-      causal ? 1 : 0, scale, reinterpret_cast<cudaStream_t>(stream));
+      q, k_pages, v_pages, block_table, nullptr, 0, page_size, cu_seqlens_q, seq_lens_k, o, lse,
+      B, max_seqlen_q, std::max(max_seqlen_k, 1), total_q, Hq, Hkv, d, max_pages_per_seq,
+      num_pages, causal ? 1 : 0, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_prefill_bsr(const void* q, const void* k_blocks, const void* v_blocks,
+                               const int32_t* kv_indptr, const int32_t* kv_indices, int nnz,
+                               const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o,
+                               float* lse, int B, int max_seqlen_q, int max_seqlen_k, int total_q,
+                               int Hq, int Hkv, int d, int block_size, int num_blocks, int causal,
+                               float scale, attn_dtype_t dtype, attn_stream_t stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seqlen_q <= 0 || max_seqlen_k < 0 ||
+      total_q < 0 || nnz < 0 || num_blocks <= 0 || block_size <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (total_q == 0) return ATTN_OK;  // no query rows: nothing to write
+  if (!q || !k_blocks || !v_blocks || !kv_indptr || !cu_seqlens_q || !seq_lens_k || !o ||
+      (nnz > 0 && !kv_indices))
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (block_size > 128 || (block_size & (block_size - 1)) != 0) return ATTN_ERR_UNSUPPORTED;
+  if (num_blocks == 0x7fffffff || (int64_t)num_blocks * block_size > 0x7fffffffLL ||
+      (int64_t)max_seqlen_k > (int64_t)nnz * block_size)
+    return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hq > (1 << 24) || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_blocks) || !aligned16(v_blocks) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(kv_indptr) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(kv_indices) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(seq_lens_k) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  // With no blocks at all (nnz = 0) kv_indptr stands in for the unread indices.
+  return attn_host::launch_prefill_bf16_paged(
+      q, k_blocks, v_blocks, nnz > 0 ? kv_indices : kv_indptr, kv_indptr, nnz, block_size,
+      cu_seqlens_q, seq_lens_k, o, lse, B, max_seqlen_q, std::max(max_seqlen_k, 1), total_q, Hq,
+      Hkv, d, 0, num_blocks, causal ? 1 : 0, scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t attn_decode_sched_workspace_bytes(int B, int Hq, int Hkv, int d, int num_ctas) {

@@ -60,11 +60,16 @@ attn_status_t launch_prefill_f32(const float* q, const float* k, const float* v,
 attn_status_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                                   float scale, int q_div, cudaStream_t stream);
+// Packed queries against a paged KV cache: a sequence's blocks are row b of
+// block_table ([B, max_pages]) or, when kv_indptr is set, the block-sparse
+// row indices[kv_indptr[b] .. kv_indptr[b + 1]) (block_table = indices, nnz
+// entries); block_size is a power of two from 1 to 128.
 attn_status_t launch_prefill_bf16_paged(const void* q, const void* k_pages, const void* v_pages,
-                                        const int* block_table, const int* cu_q,
-                                        const int* seq_lens_k, void* o, float* lse, int B,
-                                        int max_q, int max_k, int total_q, int Hq, int Hkv, int d,
-                                        int max_pages, int num_pages, int causal, float scale,
+                                        const int* block_table, const int* kv_indptr, int nnz,
+                                        int block_size, const int* cu_q, const int* seq_lens_k,
+                                        void* o, float* lse, int B, int max_q, int max_k,
+                                        int total_q, int Hq, int Hkv, int d, int max_pages,
+                                        int num_pages, int causal, float scale,
                                         cudaStream_t stream);
 attn_status_t launch_prefill_bf16_varlen(const void* q, const void* k, const void* v, void* o,
                                          float* lse, const int* cu_q, const int* cu_k, int B,

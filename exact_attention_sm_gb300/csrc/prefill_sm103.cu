@@ -131,21 +131,31 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 // [total_k, Hkv, d]; Lq and Lk are then bounds on the lengths.
 // Paged K/V ([LLM book] 10.3.7 block-table addressing; "Lecture 4" 5.2):
 // the queries are packed as above, sequence b's keys are tokens 0 ..
-// seq_k[b]-1 of the cache [num_pages, 16, Hkv, d], token t in page
-// table[b * max_pages + t / 16], slot t % 16.
+// seq_k[b]-1 of the cache [num_pages, block, Hkv, d], token t in block
+// row[t / block], slot t % block, where row is the sequence's list of
+// physical blocks: table + b * max_pages (a block table), or, in the
+// block-sparse-row form of "Lecture 4" 5.2, indices + indptr[b] with
+// indptr[b + 1] - indptr[b] entries (table = indices, nnz entries).
 struct Geo {
   const int* cu_q;  // nullptr: dense
   const int* cu_k;
   int Lq, Lk, total_q, total_k;
-  const int* seq_k;  // paged layout only
+  const int* seq_k;  // paged layouts only
   const int* table;
   int max_pages, num_pages;
+  const int* indptr;  // block-sparse-row form (else nullptr: a [B, max_pages] table)
+  int nnz;            // entries of indices (block-sparse-row form)
+  int block_shift;    // tokens per block = 1 << block_shift
+  const void* k_raw;  // gathered layouts: the caches as plain pointers
+  const void* v_raw;
 };
 
 // Tensor layouts of one launch: dense [B, H, L, d]; packed sequences
-// (cu_seqlens); packed queries with K/V in a paged cache.
-constexpr int kDenseLayout = 0, kPackedLayout = 1, kPagedLayout = 2;
-constexpr int kPage = 16;  // tokens per cache page
+// (cu_seqlens); packed queries with K/V in a paged cache, blocks of 16 to
+// 128 tokens fetched by one TMA box each (kPagedLayout) or blocks of 1 to 8
+// tokens gathered row by row by the producer warp (kGatherLayout).
+constexpr int kDenseLayout = 0, kPackedLayout = 1, kPagedLayout = 2, kGatherLayout = 3;
+constexpr int kMaxPagesPerTile = 8;  // TMA blocks per 128-token tile (16-token blocks)
 
 struct Seq {
   int q_off, lq, k_off, lk;
@@ -167,8 +177,14 @@ __device__ __forceinline__ Seq seq_of(const Geo& g, int b, int* status) {
     return Seq{q0, q1 - q0, k0, k1 - k0};
   } else {
     const int q0 = g.cu_q[b], q1 = g.cu_q[b + 1], lk = g.seq_k[b];
+    // Blocks the sequence owns (block-sparse rows: checked against nnz).
+    long long nblk = g.max_pages;
+    if (g.indptr != nullptr) {
+      const int p0 = g.indptr[b], p1 = g.indptr[b + 1];
+      nblk = (p0 < 0 || p1 < p0 || p1 > g.nnz) ? -1 : p1 - p0;
+    }
     if (q0 < 0 || q1 < q0 || q1 > g.total_q || q1 - q0 > g.Lq || lk < 0 || lk > g.Lk ||
-        lk > g.max_pages * kPage) {
+        nblk < 0 || lk > (nblk << g.block_shift)) {
       attn::record_status(status, ATTN_ERR_BAD_INDEX);
       return Seq{0, 0, 0, 0};
     }
@@ -197,37 +213,46 @@ __device__ __forceinline__ bool tile_needs_mask(const Seq& sq, int qt, int j, in
   return j * BN + BN - 1 > row_kmax(sq, qt * BM, causal);
 }
 
-// Physical pages of one sequence's K/V tiles, looked up one tile ahead: the
-// block-table entries of tile j + 1 are requested when tile j is taken, so
-// their latency overlaps the wait for a free ring slot.  Pages past the
-// sequence's length are not looked up; they, and entries outside
-// [0, num_pages) (reported as ATTN_ERR_BAD_INDEX), take the page coordinate
-// num_pages, which lies outside the tensor: TMA writes zeros there and reads
-// nothing, and the complete-tx count is the full tile either way.
+// The row of physical blocks of sequence b.
+__device__ __forceinline__ const int* block_row(const Geo& g, int b) {
+  return g.indptr != nullptr ? g.table + g.indptr[b] : g.table + static_cast<size_t>(b) * g.max_pages;
+}
+
+// Physical blocks of one sequence's K/V tiles (blocks of 16 to 128 tokens,
+// np = 128 / block per tile), looked up one tile ahead: the entries of tile
+// j + 1 are requested when tile j is taken, so their latency overlaps the
+// wait for a free ring slot.  Blocks past the sequence's length are not
+// looked up; they, and entries outside [0, num_pages) (reported as
+// ATTN_ERR_BAD_INDEX), take the block coordinate num_pages, which lies
+// outside the tensor: TMA writes zeros there and reads nothing, and the
+// complete-tx count is the full tile either way.
 struct PageCursor {
-  static constexpr int NP = BN / kPage;  // pages per K/V tile
-  const int* row;                        // the sequence's block-table row
-  int lk, j;                             // length; tile whose entries `next` holds
+  static constexpr int NP = kMaxPagesPerTile;
+  const int* row;  // the sequence's blocks
+  int lk, j;       // length; tile whose entries `next` holds
+  int np, shift;   // blocks per tile; log2 of the block size
   int next[NP];
 
   __device__ __forceinline__ void fetch(const Geo& g) {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const int p = j * NP + i;
-      next[i] = p * kPage < lk ? row[p] : g.num_pages;
+      const int p = j * np + i;
+      next[i] = i < np && (p << shift) < lk ? row[p] : g.num_pages;
     }
   }
   __device__ __forceinline__ void begin(const Geo& g, int b, int len) {
-    row = g.table + static_cast<size_t>(b) * g.max_pages;
+    row = block_row(g, b);
     lk = len;
     j = 0;
+    shift = g.block_shift;
+    np = BN >> shift;
     fetch(g);
   }
-  // Pages of tile j (tiles are taken in order 0, 1, ...).
+  // Blocks of tile j (tiles are taken in order 0, 1, ...).
   __device__ __forceinline__ void take(int (&pg)[NP], const Geo& g, int* status) {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const bool needed = (j * NP + i) * kPage < lk;
+      const bool needed = i < np && ((j * np + i) << shift) < lk;
       pg[i] = next[i];
       if (needed && (pg[i] < 0 || pg[i] >= g.num_pages)) {
         attn::record_status(status, ATTN_ERR_BAD_INDEX);
@@ -240,29 +265,78 @@ struct PageCursor {
 };
 
 // One K or V tile from the paged cache: a 4-D TMA copy {64 columns, KV head,
-// 16 slots, page} per page and 64-column block, into the same swizzled rows
-// a dense tile occupies (each page is 16 rows, 2 KB per block, so the
-// 1024-byte swizzle atoms line up).
+// block slots, block} per block and 64-column block, into the same swizzled
+// rows a dense tile occupies (a block is 16 to 128 rows, 2 to 16 KB per
+// column block, so the 1024-byte swizzle atoms line up).
 template <int KB, int BLOCK_BYTES>
 __device__ __forceinline__ void tma_load_pages(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                               const int (&pg)[PageCursor::NP], int kvh) {
+                                               const int (&pg)[PageCursor::NP], int np, int shift,
+                                               int kvh) {
 #pragma unroll
-  for (int i = 0; i < PageCursor::NP; ++i)
+  for (int i = 0; i < PageCursor::NP; ++i) {
+    if (i >= np) break;
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb)
-      tma_load_4d(dst + kb * BLOCK_BYTES + i * kPage * 128, map, bar, kb * 64, kvh, 0, pg[i]);
+      tma_load_4d(dst + kb * BLOCK_BYTES + ((i * 128) << shift), map, bar, kb * 64, kvh, 0, pg[i]);
+  }
 }
 
-// Paged cache: the slots of a sequence's last page past its length may hold
+// Blocks of 1 to 8 tokens ("Lecture 4" 5.2's block size 4, the radix
+// tree's 1): one 128-row tile of K or V gathered row by row with 16-byte
+// cp.async copies by the 32 lanes of the producer warp (8 lanes per row,
+// 4 rows per instruction, so each instruction reads whole 128-byte rows),
+// written straight into the tile's 128-byte swizzle (chunk c of row r at
+// c ^ (r % 8)).  Rows past the sequence's length, and rows whose block is
+// outside [0, num_pages) (reported), are zero-filled.  Each lane then arms
+// `full` to arrive when its copies have landed (the barrier counts 32).
+template <int KB>
+__device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* base,
+                                            uint64_t* full, const Geo& g, const int* row, int lk,
+                                            int j, int kvh, int Hkv, int lane, int* status) {
+  constexpr int D = KB * 64;
+  const int chunk = lane & 7;
+  const uint32_t sdst = smem_u32(dst);
+#pragma unroll 8
+  for (int i = 0; i < BN / 4; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    const int t = j * BN + r;
+    int blk = -1;
+    if (t < lk) {
+      blk = row[t >> g.block_shift];
+      if (blk < 0 || blk >= g.num_pages) {
+        attn::record_status(status, ATTN_ERR_BAD_INDEX);
+        blk = -1;
+      }
+    }
+    const bool ok = blk >= 0;
+    const size_t src =
+        ok ? ((static_cast<size_t>(blk) << g.block_shift) + (t & ((1 << g.block_shift) - 1))) *
+                     static_cast<size_t>(Hkv) * D +
+                 static_cast<size_t>(kvh) * D
+           : 0;
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+      const uint32_t d_addr = sdst + kb * (BM * 128) + r * 128 + ((chunk ^ (r & 7)) << 4);
+      const __nv_bfloat16* s_ptr = base + src + kb * 64 + chunk * 8;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d_addr), "l"(s_ptr),
+                   "r"(ok ? 16 : 0)
+                   : "memory");
+    }
+  }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(full))
+               : "memory");
+}
+
+// Paged cache: the slots of a sequence's last block past its length may hold
 // anything, and P = 0 times a NaN there would still reach O through the PV
 // MMA.  Before P of the tile holding the last key is handed over, the softmax
 // thread of each such row clears it in the landed V tile (tile rows
-// [lk - j BN, round_up(lk, 16) - j BN)); pages wholly past the length were
-// zero-filled by TMA.
+// [lk - j BN, round_up(lk, block) - j BN)); blocks wholly past the length
+// were zero-filled by TMA.  (Gathered tiles are zero-filled past the length.)
 template <int KB, int BLOCK_BYTES>
-__device__ __forceinline__ void clear_v_tail(uint8_t* vtile, int row, int lk, int j) {
+__device__ __forceinline__ void clear_v_tail(uint8_t* vtile, int row, int lk, int j, int shift) {
   const int lo = lk - j * BN;
-  const int hi = min(BN, (lk + kPage - 1) / kPage * kPage - j * BN);
+  const int hi = min(BN, ((((lk - 1) >> shift) + 1) << shift) - j * BN);
   if (row >= lo && row < hi) {
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
@@ -275,9 +349,9 @@ __device__ __forceinline__ void clear_v_tail(uint8_t* vtile, int row, int lk, in
 }
 
 // Whether tile j of a sequence of lk keys holds its last key inside a
-// partial page (the case clear_v_tail handles).
-__device__ __forceinline__ bool has_v_tail(int lk, int j) {
-  return (lk % kPage) != 0 && (lk - 1) / BN == j;
+// partial block (the case clear_v_tail handles).
+__device__ __forceinline__ bool has_v_tail(int lk, int j, int shift) {
+  return (lk & ((1 << shift) - 1)) != 0 && (lk - 1) / BN == j;
 }
 
 struct Item {
@@ -514,6 +588,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int NS = C::NS, NSK = C::NSK;
   constexpr bool kPacked = kLayout != kDenseLayout;
   constexpr bool kPaged = kLayout == kPagedLayout;
+  constexpr bool kGather = kLayout == kGatherLayout;  // K/V rows gathered by warp 0
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -552,11 +627,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&o_free[x], 128);
     }
     for (int s = 0; s < NSK; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], kGather ? 32 : 1);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], kGather ? 32 : 1);
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(drain, 1);
@@ -598,10 +673,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
+    // (gathered layouts: the whole warp copies K/V rows; lane 0 alone issues
+    // the Q copies and the barrier bookkeeping of TMA)
+    if (kGather || lane == 0) {
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        if constexpr (!kGather) {
+          prefetch_tmap(&tm_k);
+          prefetch_tmap(&tm_v);
+        }
+      }
+      // A wait every lane takes (the lanes of a gathering warp stay together).
+      auto pwait = [&](uint64_t* bar, uint32_t parity) {
+        if constexpr (kGather)
+          return __all_sync(FULL, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
+        else
+          return mbar_wait(bar, parity, abort_flag, kWaitLimitNs);
+      };
       int g = 0;                // K/V tiles issued (ring position)
       int nq[2] = {0, 0};       // Q tiles issued per slot
       bool ok = true;
@@ -616,6 +704,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int kv_c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
         PageCursor pages;
         if constexpr (kPaged) pages.begin(geo, w.bh / Hq, w.sq.lk);
+        const int* brow = nullptr;  // gathered layouts: the sequence's blocks
+        if constexpr (kGather) brow = block_row(geo, w.bh / Hq);
         // K/V tile j of this item into the next ring slot.  The K and V halves
         // of a slot free separately: K after the slot's last QK^T, which the
         // MMA issuer commits one K/V tile before the slot's last PV, so K(j)
@@ -632,16 +722,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           };
           uint8_t* kdst = smem + C::OFF_K + sk * C::TILE_BYTES;
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
-          if (g >= NSK && !mbar_wait(&k_empty[sk], phk, abort_flag, kWaitLimitNs)) return false;
-          if constexpr (kPaged) {
+          if (g >= NSK && !pwait(&k_empty[sk], phk)) return false;
+          if constexpr (kGather) {
+            gather_tile<C::KB>(kdst, static_cast<const __nv_bfloat16*>(geo.k_raw), &k_full[sk], geo,
+                               brow, w.sq.lk, j, kv_c1, Hkv, lane, status);
+            if (g >= NS && !pwait(&v_empty[st], ph)) {
+              asm volatile("cp.async.wait_all;" ::: "memory");  // K(j) lands before giving up
+              return false;
+            }
+            gather_tile<C::KB>(vdst, static_cast<const __nv_bfloat16*>(geo.v_raw), &v_full[st], geo,
+                               brow, w.sq.lk, j, kv_c1, Hkv, lane, status);
+          } else if constexpr (kPaged) {
             int pg[PageCursor::NP];
             pages.take(pg, geo, status);  // tile j (tiles are issued in order)
             mbar_arrive_expect_tx(&k_full[sk], C::TILE_BYTES);
-            tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[sk], pg, kv_c1);
+            tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[sk], pg, pages.np,
+                                                  pages.shift, kv_c1);
             if (g >= NS && !mbar_wait(&v_empty[st], ph, abort_flag, kWaitLimitNs))
               return drain_k(sk);
             mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
-            tma_load_pages<C::KB, C::BLOCK_BYTES>(vdst, &tm_v, &v_full[st], pg, kv_c1);
+            tma_load_pages<C::KB, C::BLOCK_BYTES>(vdst, &tm_v, &v_full[st], pg, pages.np,
+                                                  pages.shift, kv_c1);
           } else {
             mbar_arrive_expect_tx(&k_full[sk], C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb)
@@ -663,25 +764,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = issue_kv(0);
         for (int x = 0; x < 2 && ok; ++x) {
           if (w.n[x] == 0) continue;
-          if (nq[x] > 0 && !mbar_wait(&q_empty[x], (nq[x] - 1) & 1, abort_flag, kWaitLimitNs)) {
+          if (nq[x] > 0 && !pwait(&q_empty[x], (nq[x] - 1) & 1)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q,
-                        &q_full[x], kb * 64, packed ? h : w.qt[x] * BM,
-                        packed ? w.sq.q_off + w.qt[x] * BM : w.bh / q_div);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&q_full[x], C::TILE_BYTES);
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_3d(smem + C::OFF_Q + x * C::TILE_BYTES + kb * C::BLOCK_BYTES, &tm_q,
+                          &q_full[x], kb * 64, packed ? h : w.qt[x] * BM,
+                          packed ? w.sq.q_off + w.qt[x] * BM : w.bh / q_div);
+          }
           ++nq[x];
         }
         for (int j = 1; ok && j < nmax; ++j) ok = issue_kv(j);
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
       }
       // Drain: every issued copy has landed before the CTA may exit (these
       // waits ignore the abort flag; TMA copies always complete).
+      if constexpr (kGather) asm volatile("cp.async.wait_all;" ::: "memory");
       int no_abort = 0;
       for (int x = 0; x < 2; ++x)
         if (nq[x] > 0) mbar_wait(&q_full[x], (nq[x] - 1) & 1, &no_abort, kWaitLimitNs);
@@ -741,6 +845,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (nmax == 0) continue;
         // First QK^T of each present tile.
         if (!mbar_wait(&k_full[g % NSK], (g / NSK) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        if constexpr (kGather) fence_proxy_async_smem();  // rows written by cp.async
         for (int x = 0; x < 2 && ok; ++x) {
           if (w.n[x] == 0) continue;
           if (!mbar_wait(&q_full[x], nitem[x] & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
@@ -762,11 +867,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             if (!v_ready && !mbar_wait(&v_full[st], ph, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            if constexpr (kGather) fence_proxy_async_smem();
             v_ready = true;
             tc_fence_after();
             issue_pv(x, st, j > 0);
             if (j + 1 < w.n[x]) {
               if (!k_ready && !mbar_wait(&k_full[st1], ph1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+              if constexpr (kGather) fence_proxy_async_smem();
               k_ready = true;
               tc_fence_after();
               issue_qk(x, st1, j + 2 == w.n[x]);
@@ -905,12 +1012,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if constexpr (kPaged) {
-          if (has_v_tail(w.sq.lk, j)) {
+          if (has_v_tail(w.sq.lk, j, geo.block_shift)) {
             const int gt = g_item + j;  // this K/V tile's ring position
             ok = __all_sync(FULL, mbar_wait(&v_full[gt % NS], (gt / NS) & 1, abort_flag,
                                             kWaitLimitNs));
             clear_v_tail<C::KB, C::BLOCK_BYTES>(smem + C::OFF_V + (gt % NS) * C::TILE_BYTES, row,
-                                                w.sq.lk, j);
+                                                w.sq.lk, j, geo.block_shift);
           }
         }
         tmem_st_wait();
@@ -1073,6 +1180,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   constexpr int D = C::D, NS = C::NS, NQ = C::NQ;
   constexpr bool kPacked = kLayout != kDenseLayout;
   constexpr bool kPaged = kLayout == kPagedLayout;
+  constexpr bool kGather = kLayout == kGatherLayout;   // K/V rows gathered by warp 0
   constexpr bool kTmaStore = kLayout == kDenseLayout;  // O tile through the Q buffer
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -1143,8 +1251,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       mbar_init(&q_empty[i], 1);
     }
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
+      mbar_init(&k_full[s], kGather ? 32 : 1);
+      mbar_init(&v_full[s], kGather ? 32 : 1);
       mbar_init(&k_done[s], 1);
       mbar_init(&pv_done[s], 1);
     }
@@ -1193,16 +1301,25 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   if (warp < 4) {
     // 128 x 72 + 128 x 184 registers = the 256 x 128 the CTA launched with.
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && (kGather || lane == 0)) {
       // ---------------------------------------------------------- TMA producer
       // K runs one tile ahead of V: a K slot frees when its QK^T is done
       // (k_done), a V slot when its PV is done (pv_done).
       // Issue order K(0), K(1), V(0), K(2), V(1), ...
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
+      // Gathered layouts: the whole warp copies the rows.
+      if constexpr (!kGather) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+      }
+      auto pwait = [&](uint64_t* bar, int parity) {
+        if constexpr (kGather) return __all_sync(FULL, wait(bar, parity));
+        else return wait(bar, parity);
+      };
       struct Cur {
         int it, j, n, c1, c2;  // tile j of n; TMA coordinates (rows, heads) of tile 0
         PageCursor pages;      // paged cache: this item's pages, one tile ahead
+        const int* brow;       // gathered layouts: the sequence's blocks
+        int lk;
       };
       auto enter = [&](Cur& c, int it) {
         Item1 w;
@@ -1215,6 +1332,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           c.c1 = packed ? h / group : 0;
           c.c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
           if constexpr (kPaged) c.pages.begin(geo, w.bh / Hq, w.sq.lk);
+          if constexpr (kGather) {
+            c.brow = block_row(geo, w.bh / Hq);
+            c.lk = w.sq.lk;
+          }
         }
       };
       auto next = [&](Cur& c) {
@@ -1228,32 +1349,44 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       bool ok = true;
       auto load_k = [&]() -> bool {
         const int st = tk % NS;
-        if (tk >= NS && !wait(&k_done[st], (tk / NS) + 1)) return false;
-        mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
-        if constexpr (kPaged) {
+        if (tk >= NS && !pwait(&k_done[st], (tk / NS) + 1)) return false;
+        if constexpr (kGather) {
+          gather_tile<1>(smem + C::OFF_K + st * C::TILE_BYTES,
+                         static_cast<const __nv_bfloat16*>(geo.k_raw), &k_full[st], geo, ck.brow,
+                         ck.lk, ck.j, ck.c1, Hkv, lane, status);
+        } else if constexpr (kPaged) {
+          mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
           int pg[PageCursor::NP];
           ck.pages.take(pg, geo, status);
           tma_load_pages<1, C::TILE_BYTES>(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k,
-                                           &k_full[st], pg, ck.c1);
-        } else
+                                           &k_full[st], pg, ck.pages.np, ck.pages.shift, ck.c1);
+        } else {
+          mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
           tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k, &k_full[st], 0,
                       packed ? ck.c1 : ck.j * BN, packed ? ck.c2 + ck.j * BN : ck.c2);
+        }
         ++tk;
         next(ck);
         return true;
       };
       auto load_v = [&]() -> bool {
         const int st = tv % NS;
-        if (tv >= NS && !wait(&pv_done[st], (tv / NS) + 1)) return false;
-        mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
-        if constexpr (kPaged) {
+        if (tv >= NS && !pwait(&pv_done[st], (tv / NS) + 1)) return false;
+        if constexpr (kGather) {
+          gather_tile<1>(smem + C::OFF_V + st * C::TILE_BYTES,
+                         static_cast<const __nv_bfloat16*>(geo.v_raw), &v_full[st], geo, cv.brow,
+                         cv.lk, cv.j, cv.c1, Hkv, lane, status);
+        } else if constexpr (kPaged) {
+          mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
           int pg[PageCursor::NP];
           cv.pages.take(pg, geo, status);
           tma_load_pages<1, C::TILE_BYTES>(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v,
-                                           &v_full[st], pg, cv.c1);
-        } else
+                                           &v_full[st], pg, cv.pages.np, cv.pages.shift, cv.c1);
+        } else {
+          mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
           tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v, &v_full[st], 0,
                       packed ? cv.c1 : cv.j * BN, packed ? cv.c2 + cv.j * BN : cv.c2);
+        }
         ++tv;
         next(cv);
         return true;
@@ -1263,12 +1396,13 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         if (ck.it < sched.last) ok = load_k();
         if (ok) ok = load_v();
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
       }
       // Drain: every issued copy has landed before the CTA may exit (k_full
-      // and v_full count TMA bytes only; copies always complete).
+      // and v_full count TMA bytes or cp.async arrivals; copies always complete).
+      if constexpr (kGather) asm volatile("cp.async.wait_all;" ::: "memory");
       int no_abort = 0;
       for (int u = tk > NS ? tk - NS : 0; u < tk; ++u)
         mbar_wait(&k_full[u % NS], (u / NS) & 1, &no_abort, kWaitLimitNs);
@@ -1342,6 +1476,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
             ok = false;
             break;
           }
+          if constexpr (kGather) fence_proxy_async_smem();  // rows written by cp.async
           tc_fence_after();
           const uint64_t kd = k_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
 #pragma unroll
@@ -1374,6 +1509,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
             ok = false;
             break;
           }
+          if constexpr (kGather) fence_proxy_async_smem();
           tc_fence_after();
           const uint64_t vd = v_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
 #pragma unroll
@@ -1507,10 +1643,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         tmem_st32(p_addr, pk[0]);
         tmem_st32(p_addr + 32, pk[1]);
         if constexpr (kPaged) {
-          if (has_v_tail(w.sq.lk, j)) {
+          if (has_v_tail(w.sq.lk, j, geo.block_shift)) {
             ok = __all_sync(FULL, wait(&v_full[tt % NS], tt / NS));
             clear_v_tail<1, C::TILE_BYTES>(smem + C::OFF_V + (tt % NS) * C::TILE_BYTES, row,
-                                           w.sq.lk, j);
+                                           w.sq.lk, j, geo.block_shift);
           }
         }
         tmem_st_wait();
@@ -1612,19 +1748,19 @@ bool make_map_packed(CUtensorMap* m, const void* base, int D, int H, int total) 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Paged cache [num_pages, 16 slots, Hkv, d] bf16 viewed as {d, Hkv, 16,
-// num_pages}; box {64, 1, 16, 1}: one page of one KV head, 64 columns, in
-// the tile's 128-byte swizzle.  The page coordinate num_pages (past the
-// tensor) reads as zeros.
-bool make_map_pages(CUtensorMap* m, const void* base, int D, int Hkv, int num_pages) {
+// Paged cache [num_pages, block slots, Hkv, d] bf16 viewed as {d, Hkv,
+// block, num_pages}; box {64, 1, block, 1}: one block of one KV head, 64
+// columns, in the tile's 128-byte swizzle.  The block coordinate num_pages
+// (past the tensor) reads as zeros.
+bool make_map_pages(CUtensorMap* m, const void* base, int D, int Hkv, int block, int num_pages) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
-                              static_cast<cuuint64_t>(kPage), static_cast<cuuint64_t>(num_pages)};
+                              static_cast<cuuint64_t>(block), static_cast<cuuint64_t>(num_pages)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(Hkv) * D * 2,
-                                 static_cast<cuuint64_t>(kPage) * Hkv * D * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kPage), 1};
+                                 static_cast<cuuint64_t>(block) * Hkv * D * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(block), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1681,8 +1817,13 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   bool maps_ok;
   if constexpr (kLayout == kPagedLayout)
     maps_ok = make_map_packed(&mq, q, D, Hq, geo.total_q) &&
-              make_map_pages(&mk, k, D, Hkv, geo.num_pages) &&
-              make_map_pages(&mv, v, D, Hkv, geo.num_pages);
+              make_map_pages(&mk, k, D, Hkv, 1 << geo.block_shift, geo.num_pages) &&
+              make_map_pages(&mv, v, D, Hkv, 1 << geo.block_shift, geo.num_pages);
+  else if constexpr (kLayout == kGatherLayout) {  // K/V rows gathered from plain pointers
+    maps_ok = make_map_packed(&mq, q, D, Hq, geo.total_q);
+    mk = mq;
+    mv = mq;
+  }
   else if constexpr (kLayout == kPackedLayout)
     maps_ok = make_map_packed(&mq, q, D, Hq, geo.total_q) &&
               make_map_packed(&mk, k, D, Hkv, geo.total_k) &&
@@ -1721,7 +1862,7 @@ namespace attn_host {
 attn_status_t launch_prefill_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
                                   int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                                   float scale, int q_div, cudaStream_t stream) {
-  const Geo geo{nullptr, nullptr, Lq, Lk, 0, 0, nullptr, nullptr, 0, 0};
+  const Geo geo{nullptr, nullptr, Lq, Lk, 0, 0, nullptr, nullptr, 0, 0, nullptr, 0, 4, nullptr, nullptr};
   if (d == 64) return launch<64, kDenseLayout>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
   if (d == 128)
     return launch<128, kDenseLayout>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, q_div, stream);
@@ -1733,7 +1874,8 @@ attn_status_t launch_prefill_bf16_varlen(const void* q, const void* k, const voi
                                          int max_q, int max_k, int total_q, int total_k, int Hq,
                                          int Hkv, int d, int causal, float scale,
                                          cudaStream_t stream) {
-  const Geo geo{cu_q, cu_k, max_q, max_k, total_q, total_k, nullptr, nullptr, 0, 0};
+  const Geo geo{cu_q, cu_k, max_q, max_k, total_q, total_k, nullptr, nullptr, 0, 0,
+                nullptr, 0, 4, nullptr, nullptr};
   if (d == 64)
     return launch<64, kPackedLayout>(q, k, v, o, lse, B, Hq, Hkv, geo, causal, scale, 1, stream);
   if (d == 128)
@@ -1742,19 +1884,29 @@ attn_status_t launch_prefill_bf16_varlen(const void* q, const void* k, const voi
 }
 
 attn_status_t launch_prefill_bf16_paged(const void* q, const void* k_pages, const void* v_pages,
-                                        const int* block_table, const int* cu_q,
-                                        const int* seq_lens_k, void* o, float* lse, int B,
-                                        int max_q, int max_k, int total_q, int Hq, int Hkv, int d,
-                                        int max_pages, int num_pages, int causal, float scale,
+                                        const int* block_table, const int* kv_indptr, int nnz,
+                                        int block_size, const int* cu_q, const int* seq_lens_k,
+                                        void* o, float* lse, int B, int max_q, int max_k,
+                                        int total_q, int Hq, int Hkv, int d, int max_pages,
+                                        int num_pages, int causal, float scale,
                                         cudaStream_t stream) {
+  int shift = 0;
+  while ((1 << shift) < block_size) ++shift;
+  if ((1 << shift) != block_size || shift > 7) return ATTN_ERR_UNSUPPORTED;
   const Geo geo{cu_q, nullptr, max_q, max_k, total_q, 0, seq_lens_k, block_table, max_pages,
-                num_pages};
+                num_pages, kv_indptr, nnz, shift, k_pages, v_pages};
+  // Blocks of 16 tokens or more: one TMA box per block; smaller: row gathers.
+  const bool tma = block_size >= 16;
   if (d == 64)
-    return launch<64, kPagedLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal, scale, 1,
-                                    stream);
+    return tma ? launch<64, kPagedLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal,
+                                          scale, 1, stream)
+               : launch<64, kGatherLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal,
+                                           scale, 1, stream);
   if (d == 128)
-    return launch<128, kPagedLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal, scale,
-                                     1, stream);
+    return tma ? launch<128, kPagedLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal,
+                                           scale, 1, stream)
+               : launch<128, kGatherLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal,
+                                            scale, 1, stream);
   return ATTN_ERR_UNSUPPORTED;
 }
 

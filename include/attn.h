@@ -316,22 +316,26 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
  *   q [total_q, Hq, d] bf16 packed as in attn_fwd_varlen with
  *   cu_seqlens_q [B + 1] (DEVICE int32); o [total_q, Hq, d] bf16; lse
  *   [total_q, Hq] fp32 or NULL.
- *   k_pages, v_pages [num_pages, 16, Hkv, d] bf16 (the decode cache layout);
- *   block_table [B, max_pages_per_seq] int32 and seq_lens_k [B] int32, both
- *   on the device: sequence b's keys are tokens 0 .. seq_lens_k[b]-1, token
- *   t in page block_table[b][t / 16], slot t % 16.  Entries at or past
- *   ceil(seq_lens_k[b] / 16) are never read.
+ *   k_pages, v_pages [num_pages, page_size, Hkv, d] bf16 (the decode cache
+ *   layout at page_size 16); block_table [B, max_pages_per_seq] int32 and
+ *   seq_lens_k [B] int32, both on the device: sequence b's keys are tokens
+ *   0 .. seq_lens_k[b]-1, token t in page block_table[b][t / page_size],
+ *   slot t % page_size.  Entries at or past ceil(seq_lens_k[b] / page_size)
+ *   are never read.
  *   max_seqlen_q / max_seqlen_k bound the lengths (max_seqlen_k <=
- *   max_pages_per_seq * 16).
+ *   max_pages_per_seq * page_size).
+ *   page_size: a power of two from 1 to 128.  Pages of 16 tokens or more go
+ *   to shared memory as one TMA copy each; smaller pages are gathered row by
+ *   row (slower: more, smaller copies).
  *
  * Causal is aligned bottom-right as in attn_fwd_varlen: the chunk's queries
  * are the last Lq of the sequence's Lk tokens (their K/V already appended).
  * Slots of a sequence's last page past its length may hold anything: they
- * never reach the result.  d in {64, 128}, page_size 16, bf16.  total_q = 0
- * returns ATTN_OK without a launch.  Errors: ATTN_ERR_INVALID_ARG for NULLs,
- * bad sizes or misalignment; ATTN_ERR_UNSUPPORTED for other d, page sizes
- * or dtypes.  On the device, a cu_seqlens_q entry or length out of bounds,
- * or a needed block-table entry outside [0, num_pages), is reported as
+ * never reach the result.  d in {64, 128}, bf16.  total_q = 0 returns
+ * ATTN_OK without a launch.  Errors: ATTN_ERR_INVALID_ARG for NULLs, bad
+ * sizes or misalignment; ATTN_ERR_UNSUPPORTED for other d, page sizes or
+ * dtypes.  On the device, a cu_seqlens_q entry or length out of bounds, or a
+ * needed block-table entry outside [0, num_pages), is reported as
  * ATTN_ERR_BAD_INDEX (the sequence is skipped, or the page reads as zeros and
  * that sequence's rows are not meaningful); nothing outside the tensors is
  * read or written.
@@ -342,6 +346,40 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void*
                                  int max_seqlen_q, int max_seqlen_k, int total_q, int Hq, int Hkv,
                                  int d, int page_size, int max_pages_per_seq, int num_pages,
                                  int causal, float scale, attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_prefill_bsr - prefill against a KV cache addressed in block-sparse
+ * row (BSR) form ("Lecture 4" section 5.2, "block-sparse format: unifying
+ * KV layouts"): the batch's "query rows x physical KV blocks" matrix is
+ * block-sparse; kv_indices lists the non-zero blocks (physical block ids) of
+ * every request end to end and request b's blocks, in logical order, are
+ * kv_indices[kv_indptr[b] .. kv_indptr[b + 1]).  A vLLM page table is this
+ * form with block_size 16, SGLang's radix tree with block_size 1 (the
+ * lecture's exercise 9 (a)).
+ *
+ *   q [total_q, Hq, d] bf16 packed with cu_seqlens_q [B + 1]; o, lse as in
+ *   attn_prefill_paged.
+ *   k_blocks, v_blocks [num_blocks, block_size, Hkv, d] bf16.
+ *   kv_indptr [B + 1], kv_indices [nnz], seq_lens_k [B]: int32 on the
+ *   device.  Request b's keys are tokens 0 .. seq_lens_k[b]-1, token t in
+ *   block kv_indices[kv_indptr[b] + t / block_size], slot t % block_size;
+ *   kv_indptr[b + 1] - kv_indptr[b] >= ceil(seq_lens_k[b] / block_size).
+ *   block_size: a power of two from 1 to 128 (16 and above: one TMA copy per
+ *   block; below: row gathers into the same shared-memory tiles).
+ *   Decode is the case of one query per request.
+ *
+ * Causal is aligned bottom-right (the request's queries are its last Lq
+ * tokens).  d in {64, 128}, bf16.  Errors as attn_prefill_paged; on the
+ * device, kv_indptr entries outside [0, nnz] or decreasing, too few blocks
+ * for a length, and needed block ids outside [0, num_blocks) are reported as
+ * ATTN_ERR_BAD_INDEX and never dereferenced.
+ */
+attn_status_t attn_prefill_bsr(const void* q, const void* k_blocks, const void* v_blocks,
+                               const int32_t* kv_indptr, const int32_t* kv_indices, int nnz,
+                               const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, void* o,
+                               float* lse, int B, int max_seqlen_q, int max_seqlen_k, int total_q,
+                               int Hq, int Hkv, int d, int block_size, int num_blocks, int causal,
+                               float scale, attn_dtype_t dtype, attn_stream_t stream);
 
 /*
  * Cascade (shared-prefix) decode ([Lecture 4] 4.4 "cascade attention" and

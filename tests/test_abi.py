@@ -235,9 +235,44 @@ def test_prefill_paged_rejects_on_host():
     assert paged(kp=MISALIGNED) == 1
     assert paged(table=ctypes.c_void_p(0x10002)) == 1
     assert paged(d=96) == 2
-    assert paged(page=32) == 2
+    assert paged(page=24) == 2                # pages are a power of two ...
+    assert paged(page=256) == 2               # ... of at most 128 tokens
+    assert paged(page=4, mk=17) == 1          # longer than max_pages * 4
     assert paged(dtype=ea.ATTN_F32) == 2
     assert paged(tq=0, q=None, o=None) == 0   # no query rows: no launch
+
+
+def bsr(**kw):
+    args = dict(q=FAKE, kb=FAKE, vb=FAKE, indptr=FAKE, indices=FAKE, nnz=16, cq=FAKE, sk=FAKE,
+                o=FAKE, lse=None, B=3, mq=29, mk=29, tq=46, Hq=4, Hkv=2, d=64, block=4,
+                num_blocks=24, causal=1, scale=0.1, dtype=ea.ATTN_BF16)
+    args.update(kw)
+    a = args
+    return ea.lib().attn_prefill_bsr(a["q"], a["kb"], a["vb"], a["indptr"], a["indices"], a["nnz"],
+                                     a["cq"], a["sk"], a["o"], a["lse"], a["B"], a["mq"], a["mk"],
+                                     a["tq"], a["Hq"], a["Hkv"], a["d"], a["block"],
+                                     a["num_blocks"], a["causal"], a["scale"], a["dtype"], None)
+
+
+def test_prefill_bsr_rejects_on_host():
+    """[Lecture 4] 5.2 block-sparse rows: argument checks before any launch."""
+    assert bsr(q=None) == 1
+    assert bsr(indptr=None) == 1
+    assert bsr(indices=None) == 1             # blocks listed but no indices
+    assert bsr(sk=None) == 1
+    assert bsr(B=0) == 1
+    assert bsr(Hkv=3) == 1
+    assert bsr(nnz=-1) == 1
+    assert bsr(num_blocks=0) == 1
+    assert bsr(scale=float("inf")) == 1
+    assert bsr(kb=MISALIGNED) == 1
+    assert bsr(indices=ctypes.c_void_p(0x10002)) == 1
+    assert bsr(d=96) == 2
+    assert bsr(block=3) == 2
+    assert bsr(block=256) == 2
+    assert bsr(mk=65) == 2                    # longer than all 16 blocks of 4 tokens together
+    assert bsr(dtype=ea.ATTN_F32) == 2
+    assert bsr(tq=0, q=None, o=None) == 0     # no query rows: no launch
 
 
 def bwd(**kw):
