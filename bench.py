@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import math
 import os
@@ -61,6 +62,10 @@ WORKLOADS = {
     # tokens attend to its whole cached context (lengths U[1024, 8192], seed 4).
     "prefill-paged-chunk512-llama": dict(kind="paged", B=16, Hq=32, Hkv=8, chunk=512, d=128,
                                          lo=1024, hi=8192, causal=True, dtype="bf16"),
+    # The same chunks against a cache in block-sparse-row form with 4-token
+    # blocks (Lecture 4 section 5.2's block size; rows gathered, not TMA boxes).
+    "prefill-bsr-block4-llama": dict(kind="paged", B=16, Hq=32, Hkv=8, chunk=512, d=128,
+                                     lo=1024, hi=8192, causal=True, dtype="bf16", block=4),
     # Training: the backward pass of the GPT-2-medium-shaped causal attention
     # (the forward's O and LSE precomputed; dO random).
     "gpt2-medium-backward": dict(kind="backward", B=64, Hq=16, Hkv=16, L=1024, d=64, causal=True,
@@ -90,9 +95,11 @@ def describe(name):
         return (f"{name}: {w['B']} packed sequences, lengths U[1,{w['max_len']}] seed 3, "
                 f"Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} causal (bottom-right) bf16 + LSE")
     if w["kind"] == "paged":
+        form = (f"block-sparse rows of {w['block']}-token blocks" if "block" in w
+                else "16-token shuffled pages")
         return (f"{name}: {w['B']} requests, cached context U[{w['lo']},{w['hi']}] seed 4, the last "
                 f"{w['chunk']} tokens of each as packed queries, Hq={w['Hq']} Hkv={w['Hkv']} "
-                f"d={w['d']} causal (bottom-right) bf16 + LSE, 16-token shuffled pages")
+                f"d={w['d']} causal (bottom-right) bf16 + LSE, {form}")
     if w["kind"] == "cascade":
         return (f"{name}: B={w['B']} Hq={w['Hq']} Hkv={w['Hkv']} d={w['d']} bf16, shared prefix "
                 f"{w['prefix']} + {w['suffix']} unique tokens per request (16-token shuffled pages)")
@@ -317,13 +324,25 @@ def make_step(name, torch, ea, inputs):
     if w["kind"] == "paged":
         lens_k = inputs.decode_lengths_uniform(w["B"], w["lo"], w["hi"], seed=4)
         lens_q = [min(w["chunk"], n) for n in lens_k]
-        _, kp, vp, table, sl = inputs.decode_inputs(lens_k, w["Hq"], w["Hkv"], w["d"], seed=0,
-                                                    device="cuda")
+        bs = w.get("block", 16)
+        _, kp, vp, table, sl = inputs.decode_inputs(lens_k, w["Hq"], w["Hkv"], w["d"], page_size=bs,
+                                                    seed=0, device="cuda")
         q, _, _, cq, _ = inputs.varlen_inputs(lens_q, lens_q, w["Hq"], w["Hkv"], w["d"], seed=1,
                                               device="cuda")
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[0], w["Hq"], dtype=torch.float32, device="cuda")
         mq, mk = max(lens_q), max(lens_k)
+        if "block" in w:  # block-sparse rows: the table's used entries end to end
+            counts = [-(-n // bs) for n in lens_k]
+            tab = table.cpu()
+            indices = torch.cat([tab[b, :c] for b, c in enumerate(counts)]).cuda()
+            indptr = torch.tensor([0] + list(itertools.accumulate(counts)), dtype=torch.int32,
+                                  device="cuda")
+
+            def step():
+                ea.attn_prefill_bsr(q, kp, vp, indptr, indices, cq, sl, mq, mk, causal=True, out=o,
+                                    lse=lse)
+            return step, 1, paged_flops(w, lens_q, lens_k), "flops", None
 
         def step():
             ea.attn_prefill_paged(q, kp, vp, table, cq, sl, mq, mk, causal=True, out=o, lse=lse)

@@ -151,11 +151,10 @@ struct Geo {
 };
 
 // Tensor layouts of one launch: dense [B, H, L, d]; packed sequences
-// (cu_seqlens); packed queries with K/V in a paged cache, blocks of 16 to
-// 128 tokens fetched by one TMA box each (kPagedLayout) or blocks of 1 to 8
-// tokens gathered row by row by the producer warp (kGatherLayout).
+// (cu_seqlens); packed queries with K/V in a paged cache, 16-token pages
+// fetched by one TMA box each (kPagedLayout) or blocks of any other size
+// gathered row by row by the producer warp (kGatherLayout).
 constexpr int kDenseLayout = 0, kPackedLayout = 1, kPagedLayout = 2, kGatherLayout = 3;
-constexpr int kMaxPagesPerTile = 8;  // TMA blocks per 128-token tile (16-token blocks)
 
 struct Seq {
   int q_off, lq, k_off, lk;
@@ -218,41 +217,41 @@ __device__ __forceinline__ const int* block_row(const Geo& g, int b) {
   return g.indptr != nullptr ? g.table + g.indptr[b] : g.table + static_cast<size_t>(b) * g.max_pages;
 }
 
-// Physical blocks of one sequence's K/V tiles (blocks of 16 to 128 tokens,
-// np = 128 / block per tile), looked up one tile ahead: the entries of tile
-// j + 1 are requested when tile j is taken, so their latency overlaps the
-// wait for a free ring slot.  Blocks past the sequence's length are not
-// looked up; they, and entries outside [0, num_pages) (reported as
-// ATTN_ERR_BAD_INDEX), take the block coordinate num_pages, which lies
+// Physical pages of one sequence's K/V tiles (16-token pages), looked up
+// one tile ahead: the entries of tile j + 1 are requested when tile j is
+// taken, so their latency overlaps the wait for a free ring slot (the ids
+// are only used a tile later: the producer is a single thread on the
+// critical path of every K/V tile).  Pages past the sequence's length are
+// not looked up; they, and entries outside [0, num_pages) (reported as
+// ATTN_ERR_BAD_INDEX), take the page coordinate num_pages, which lies
 // outside the tensor: TMA writes zeros there and reads nothing, and the
-// complete-tx count is the full tile either way.
+// complete-tx count is the full tile either way.  Other block sizes take
+// the gathered layout below.
+constexpr int kPage = 16;  // tokens per TMA page
 struct PageCursor {
-  static constexpr int NP = kMaxPagesPerTile;
-  const int* row;  // the sequence's blocks
-  int lk, j;       // length; tile whose entries `next` holds
-  int np, shift;   // blocks per tile; log2 of the block size
+  static constexpr int NP = BN / kPage;  // pages per K/V tile
+  const int* row;                        // the sequence's pages
+  int lk, j;                             // length; tile whose entries `next` holds
   int next[NP];
 
   __device__ __forceinline__ void fetch(const Geo& g) {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const int p = j * np + i;
-      next[i] = i < np && (p << shift) < lk ? row[p] : g.num_pages;
+      const int p = j * NP + i;
+      next[i] = p * kPage < lk ? row[p] : g.num_pages;
     }
   }
   __device__ __forceinline__ void begin(const Geo& g, int b, int len) {
     row = block_row(g, b);
     lk = len;
     j = 0;
-    shift = g.block_shift;
-    np = BN >> shift;
     fetch(g);
   }
-  // Blocks of tile j (tiles are taken in order 0, 1, ...).
+  // Pages of tile j (tiles are taken in order 0, 1, ...).
   __device__ __forceinline__ void take(int (&pg)[NP], const Geo& g, int* status) {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      const bool needed = i < np && ((j * np + i) << shift) < lk;
+      const bool needed = (j * NP + i) * kPage < lk;
       pg[i] = next[i];
       if (needed && (pg[i] < 0 || pg[i] >= g.num_pages)) {
         attn::record_status(status, ATTN_ERR_BAD_INDEX);
@@ -265,52 +264,82 @@ struct PageCursor {
 };
 
 // One K or V tile from the paged cache: a 4-D TMA copy {64 columns, KV head,
-// block slots, block} per block and 64-column block, into the same swizzled
-// rows a dense tile occupies (a block is 16 to 128 rows, 2 to 16 KB per
-// column block, so the 1024-byte swizzle atoms line up).
+// 16 slots, page} per page and 64-column block, into the same swizzled rows
+// a dense tile occupies (each page is 16 rows, 2 KB per block, so the
+// 1024-byte swizzle atoms line up).
 template <int KB, int BLOCK_BYTES>
 __device__ __forceinline__ void tma_load_pages(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                               const int (&pg)[PageCursor::NP], int np, int shift,
-                                               int kvh) {
+                                               const int (&pg)[PageCursor::NP], int kvh) {
 #pragma unroll
-  for (int i = 0; i < PageCursor::NP; ++i) {
-    if (i >= np) break;
+  for (int i = 0; i < PageCursor::NP; ++i)
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb)
-      tma_load_4d(dst + kb * BLOCK_BYTES + ((i * 128) << shift), map, bar, kb * 64, kvh, 0, pg[i]);
-  }
+      tma_load_4d(dst + kb * BLOCK_BYTES + i * kPage * 128, map, bar, kb * 64, kvh, 0, pg[i]);
 }
 
-// Blocks of 1 to 8 tokens ("Lecture 4" 5.2's block size 4, the radix
-// tree's 1): one 128-row tile of K or V gathered row by row with 16-byte
-// cp.async copies by the 32 lanes of the producer warp (8 lanes per row,
-// 4 rows per instruction, so each instruction reads whole 128-byte rows),
-// written straight into the tile's 128-byte swizzle (chunk c of row r at
-// c ^ (r % 8)).  Rows past the sequence's length, and rows whose block is
+// Blocks of other sizes ("Lecture 4" 5.2's block size 4, the radix tree's
+// 1, or 32 to 128) are gathered row by row.  GatherCursor holds the block ids of
+// one sequence's next 128-token tile, np = 128 / block of them, entry
+// k * 32 + lane in register ids[k] of that lane; they are loaded one tile
+// ahead (coalesced), so their latency overlaps the current tile's copies.
+// Ids past the sequence's length are -1.
+struct GatherCursor {
+  const int* row;  // the sequence's blocks
+  int lk, j, shift, np;
+  int ids[4];      // tile j's block ids (np <= 128 = 4 x 32)
+
+  __device__ __forceinline__ void fetch(int lane) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = k * 32 + lane, p = j * np + e;
+      ids[k] = e < np && (p << shift) < lk ? row[p] : -1;
+    }
+  }
+  __device__ __forceinline__ void begin(const Geo& g, int b, int len, int lane) {
+    row = block_row(g, b);
+    lk = len;
+    j = 0;
+    shift = g.block_shift;
+    np = BN >> shift;
+    fetch(lane);
+  }
+  __device__ __forceinline__ void advance(int lane) {
+    ++j;
+    fetch(lane);
+  }
+};
+
+// One 128-row tile of K or V (tile c.j of the cursor's sequence) gathered
+// with 16-byte cp.async copies by the 32 lanes of the producer warp: 8 lanes
+// per row and 4 rows per instruction, so each instruction reads whole
+// 128-byte rows; rows go straight into the tile's 128-byte swizzle (chunk c
+// of row r at c ^ (r % 8)).  Row r's block id comes from lane (r / block) %
+// 32 by a shuffle (for a given instruction every lane wants the same ids
+// register).  Rows past the sequence's length, and rows whose block is
 // outside [0, num_pages) (reported), are zero-filled.  Each lane then arms
 // `full` to arrive when its copies have landed (the barrier counts 32).
 template <int KB>
 __device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* base,
-                                            uint64_t* full, const Geo& g, const int* row, int lk,
-                                            int j, int kvh, int Hkv, int lane, int* status) {
+                                            uint64_t* full, const Geo& g, const GatherCursor& c,
+                                            int kvh, int Hkv, int lane, int* status) {
   constexpr int D = KB * 64;
   const int chunk = lane & 7;
   const uint32_t sdst = smem_u32(dst);
 #pragma unroll 8
   for (int i = 0; i < BN / 4; ++i) {
     const int r = 4 * i + (lane >> 3);
-    const int t = j * BN + r;
-    int blk = -1;
-    if (t < lk) {
-      blk = row[t >> g.block_shift];
-      if (blk < 0 || blk >= g.num_pages) {
-        attn::record_status(status, ATTN_ERR_BAD_INDEX);
-        blk = -1;
-      }
+    const int idx = r >> c.shift;  // entry of the tile's ids
+    const int k = (4 * i >> c.shift) >> 5;  // the same for every lane
+    const int src_reg = k == 0 ? c.ids[0] : k == 1 ? c.ids[1] : k == 2 ? c.ids[2] : c.ids[3];
+    int blk = __shfl_sync(0xffffffffu, src_reg, idx & 31);
+    const int t = c.j * BN + r;
+    if (t < c.lk && (blk < 0 || blk >= g.num_pages)) {
+      attn::record_status(status, ATTN_ERR_BAD_INDEX);
+      blk = -1;
     }
-    const bool ok = blk >= 0;
+    const bool ok = t < c.lk && blk >= 0;
     const size_t src =
-        ok ? ((static_cast<size_t>(blk) << g.block_shift) + (t & ((1 << g.block_shift) - 1))) *
+        ok ? ((static_cast<size_t>(blk) << c.shift) + (t & ((1 << c.shift) - 1))) *
                      static_cast<size_t>(Hkv) * D +
                  static_cast<size_t>(kvh) * D
            : 0;
@@ -704,8 +733,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int kv_c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
         PageCursor pages;
         if constexpr (kPaged) pages.begin(geo, w.bh / Hq, w.sq.lk);
-        const int* brow = nullptr;  // gathered layouts: the sequence's blocks
-        if constexpr (kGather) brow = block_row(geo, w.bh / Hq);
+        GatherCursor gc;  // gathered layouts: the item's block ids, one tile ahead
+        if constexpr (kGather) gc.begin(geo, w.bh / Hq, w.sq.lk, lane);
         // K/V tile j of this item into the next ring slot.  The K and V halves
         // of a slot free separately: K after the slot's last QK^T, which the
         // MMA issuer commits one K/V tile before the slot's last PV, so K(j)
@@ -723,26 +752,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* kdst = smem + C::OFF_K + sk * C::TILE_BYTES;
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
           if (g >= NSK && !pwait(&k_empty[sk], phk)) return false;
-          if constexpr (kGather) {
+          if constexpr (kGather) {  // tile j of the item (the cursor's tile)
             gather_tile<C::KB>(kdst, static_cast<const __nv_bfloat16*>(geo.k_raw), &k_full[sk], geo,
-                               brow, w.sq.lk, j, kv_c1, Hkv, lane, status);
+                               gc, kv_c1, Hkv, lane, status);
             if (g >= NS && !pwait(&v_empty[st], ph)) {
               asm volatile("cp.async.wait_all;" ::: "memory");  // K(j) lands before giving up
               return false;
             }
             gather_tile<C::KB>(vdst, static_cast<const __nv_bfloat16*>(geo.v_raw), &v_full[st], geo,
-                               brow, w.sq.lk, j, kv_c1, Hkv, lane, status);
+                               gc, kv_c1, Hkv, lane, status);
+            gc.advance(lane);
           } else if constexpr (kPaged) {
             int pg[PageCursor::NP];
             pages.take(pg, geo, status);  // tile j (tiles are issued in order)
             mbar_arrive_expect_tx(&k_full[sk], C::TILE_BYTES);
-            tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[sk], pg, pages.np,
-                                                  pages.shift, kv_c1);
+            tma_load_pages<C::KB, C::BLOCK_BYTES>(kdst, &tm_k, &k_full[sk], pg, kv_c1);
             if (g >= NS && !mbar_wait(&v_empty[st], ph, abort_flag, kWaitLimitNs))
               return drain_k(sk);
             mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
-            tma_load_pages<C::KB, C::BLOCK_BYTES>(vdst, &tm_v, &v_full[st], pg, pages.np,
-                                                  pages.shift, kv_c1);
+            tma_load_pages<C::KB, C::BLOCK_BYTES>(vdst, &tm_v, &v_full[st], pg, kv_c1);
           } else {
             mbar_arrive_expect_tx(&k_full[sk], C::TILE_BYTES);
             for (int kb = 0; kb < C::KB; ++kb)
@@ -1318,8 +1346,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       struct Cur {
         int it, j, n, c1, c2;  // tile j of n; TMA coordinates (rows, heads) of tile 0
         PageCursor pages;      // paged cache: this item's pages, one tile ahead
-        const int* brow;       // gathered layouts: the sequence's blocks
-        int lk;
+        GatherCursor gath;     // gathered layouts: this item's block ids, one tile ahead
       };
       auto enter = [&](Cur& c, int it) {
         Item1 w;
@@ -1332,10 +1359,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           c.c1 = packed ? h / group : 0;
           c.c2 = packed ? w.sq.k_off : (w.bh / Hq) * Hkv + h / group;
           if constexpr (kPaged) c.pages.begin(geo, w.bh / Hq, w.sq.lk);
-          if constexpr (kGather) {
-            c.brow = block_row(geo, w.bh / Hq);
-            c.lk = w.sq.lk;
-          }
+          if constexpr (kGather) c.gath.begin(geo, w.bh / Hq, w.sq.lk, lane);
         }
       };
       auto next = [&](Cur& c) {
@@ -1352,14 +1376,15 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         if (tk >= NS && !pwait(&k_done[st], (tk / NS) + 1)) return false;
         if constexpr (kGather) {
           gather_tile<1>(smem + C::OFF_K + st * C::TILE_BYTES,
-                         static_cast<const __nv_bfloat16*>(geo.k_raw), &k_full[st], geo, ck.brow,
-                         ck.lk, ck.j, ck.c1, Hkv, lane, status);
+                         static_cast<const __nv_bfloat16*>(geo.k_raw), &k_full[st], geo, ck.gath,
+                         ck.c1, Hkv, lane, status);
+          ck.gath.advance(lane);
         } else if constexpr (kPaged) {
           mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
           int pg[PageCursor::NP];
           ck.pages.take(pg, geo, status);
           tma_load_pages<1, C::TILE_BYTES>(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k,
-                                           &k_full[st], pg, ck.pages.np, ck.pages.shift, ck.c1);
+                                           &k_full[st], pg, ck.c1);
         } else {
           mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
           tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES, &tm_k, &k_full[st], 0,
@@ -1374,14 +1399,15 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         if (tv >= NS && !pwait(&pv_done[st], (tv / NS) + 1)) return false;
         if constexpr (kGather) {
           gather_tile<1>(smem + C::OFF_V + st * C::TILE_BYTES,
-                         static_cast<const __nv_bfloat16*>(geo.v_raw), &v_full[st], geo, cv.brow,
-                         cv.lk, cv.j, cv.c1, Hkv, lane, status);
+                         static_cast<const __nv_bfloat16*>(geo.v_raw), &v_full[st], geo, cv.gath,
+                         cv.c1, Hkv, lane, status);
+          cv.gath.advance(lane);
         } else if constexpr (kPaged) {
           mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
           int pg[PageCursor::NP];
           cv.pages.take(pg, geo, status);
           tma_load_pages<1, C::TILE_BYTES>(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v,
-                                           &v_full[st], pg, cv.pages.np, cv.pages.shift, cv.c1);
+                                           &v_full[st], pg, cv.c1);
         } else {
           mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
           tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES, &tm_v, &v_full[st], 0,
@@ -1815,10 +1841,10 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   CUtensorMap mq, mk, mv, mo;
   if (q_div < 1 || (B * Hq) % q_div != 0) return ATTN_ERR_INVALID_ARG;
   bool maps_ok;
-  if constexpr (kLayout == kPagedLayout)
+  if constexpr (kLayout == kPagedLayout)  // 16-token pages
     maps_ok = make_map_packed(&mq, q, D, Hq, geo.total_q) &&
-              make_map_pages(&mk, k, D, Hkv, 1 << geo.block_shift, geo.num_pages) &&
-              make_map_pages(&mv, v, D, Hkv, 1 << geo.block_shift, geo.num_pages);
+              make_map_pages(&mk, k, D, Hkv, kPage, geo.num_pages) &&
+              make_map_pages(&mv, v, D, Hkv, kPage, geo.num_pages);
   else if constexpr (kLayout == kGatherLayout) {  // K/V rows gathered from plain pointers
     maps_ok = make_map_packed(&mq, q, D, Hq, geo.total_q);
     mk = mq;
@@ -1893,10 +1919,10 @@ attn_status_t launch_prefill_bf16_paged(const void* q, const void* k_pages, cons
   int shift = 0;
   while ((1 << shift) < block_size) ++shift;
   if ((1 << shift) != block_size || shift > 7) return ATTN_ERR_UNSUPPORTED;
+  // 16-token pages: one TMA copy per page; other block sizes: row gathers.
+  const bool tma = block_size == 16;
   const Geo geo{cu_q, nullptr, max_q, max_k, total_q, 0, seq_lens_k, block_table, max_pages,
                 num_pages, kv_indptr, nnz, shift, k_pages, v_pages};
-  // Blocks of 16 tokens or more: one TMA box per block; smaller: row gathers.
-  const bool tma = block_size >= 16;
   if (d == 64)
     return tma ? launch<64, kPagedLayout>(q, k_pages, v_pages, o, lse, B, Hq, Hkv, geo, causal,
                                           scale, 1, stream)

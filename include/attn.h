@@ -324,9 +324,9 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
  *   are never read.
  *   max_seqlen_q / max_seqlen_k bound the lengths (max_seqlen_k <=
  *   max_pages_per_seq * page_size).
- *   page_size: a power of two from 1 to 128.  Pages of 16 tokens or more go
- *   to shared memory as one TMA copy each; smaller pages are gathered row by
- *   row (slower: more, smaller copies).
+ *   page_size: a power of two from 1 to 128.  16-token pages go to shared
+ *   memory as one TMA copy each; other sizes are gathered row by row
+ *   (slower: many 16-byte copies).
  *
  * Causal is aligned bottom-right as in attn_fwd_varlen: the chunk's queries
  * are the last Lq of the sequence's Lk tokens (their K/V already appended).
@@ -364,8 +364,8 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_pages, const void*
  *   device.  Request b's keys are tokens 0 .. seq_lens_k[b]-1, token t in
  *   block kv_indices[kv_indptr[b] + t / block_size], slot t % block_size;
  *   kv_indptr[b + 1] - kv_indptr[b] >= ceil(seq_lens_k[b] / block_size).
- *   block_size: a power of two from 1 to 128 (16 and above: one TMA copy per
- *   block; below: row gathers into the same shared-memory tiles).
+ *   block_size: a power of two from 1 to 128 (16: one TMA copy per block;
+ *   other sizes: row gathers into the same shared-memory tiles).
  *   Decode is the case of one query per request.
  *
  * Causal is aligned bottom-right (the request's queries are its last Lq

@@ -2,9 +2,9 @@
 5.2), and against block tables of page sizes other than 16, on the GPU
 against the float64 oracle (bf16 tolerances).
 
-Blocks of 16 tokens and more reach shared memory as one TMA copy each;
-smaller blocks (the section's block size 4, the radix tree's block size 1)
-are gathered row by row.  Both paths must give the oracle's result."""
+16-token blocks reach shared memory as one TMA copy each; other block
+sizes (the section's block size 4, the radix tree's block size 1, 32 to
+128) are gathered row by row.  Both paths must give the oracle's result."""
 import json
 import math
 import os
@@ -124,7 +124,7 @@ def test_block_size_one_whole_sequences(d):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("block", [16, 32, 64, 128])
 def test_large_blocks(d, block):
-    """Block sizes 16 to 128 (one TMA copy per block), ragged tails with NaN."""
+    """Block sizes 16 (TMA copies) and 32 to 128 (row gathers), ragged tails with NaN."""
     run_bsr([200, 3, 64], [700, 3, 250], d, block, True, seed=block, poison=True)
 
 
