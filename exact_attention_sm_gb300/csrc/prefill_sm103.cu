@@ -316,12 +316,12 @@ struct GatherCursor {
 // of row r at c ^ (r % 8)).  Row r's block id comes from lane (r / block) %
 // 32 by a shuffle (for a given instruction every lane wants the same ids
 // register).  Rows past the sequence's length, and rows whose block is
-// outside [0, num_pages) (reported), are zero-filled.  Each lane then arms
-// `full` to arrive when its copies have landed (the barrier counts 32).
+// outside [0, num_pages) (reported), are zero-filled.  The copies form one
+// cp.async group; GatherRetire publishes the tile once they have landed.
 template <int KB>
 __device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* base,
-                                            uint64_t* full, const Geo& g, const GatherCursor& c,
-                                            int kvh, int Hkv, int lane, int* status) {
+                                            const Geo& g, const GatherCursor& c, int kvh, int Hkv,
+                                            int lane, int* status) {
   constexpr int D = KB * 64;
   const int chunk = lane & 7;
   const uint32_t sdst = smem_u32(dst);
@@ -352,9 +352,37 @@ __device__ __forceinline__ void gather_tile(uint8_t* dst, const __nv_bfloat16* b
                    : "memory");
     }
   }
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(full))
-               : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
+
+// Publishes gathered tiles to the tensor core one tile late: after tile t's
+// group is committed, tile t - 1's copies are waited for (wait_group 1),
+// made visible to the async proxy (fence.proxy.async by every writing lane)
+// and its full barrier arrived on (count 1).  flush() publishes the last
+// one; the producer calls it before any wait that is not already satisfied,
+// so a consumer never waits on a tile the producer is holding back.
+struct GatherRetire {
+  uint64_t* pend = nullptr;
+  __device__ __forceinline__ void publish(int lane) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pend);
+  }
+  __device__ __forceinline__ void committed(uint64_t* full, int lane) {
+    if (pend != nullptr) {
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      publish(lane);
+    }
+    pend = full;
+  }
+  __device__ __forceinline__ void flush(int lane) {
+    if (pend != nullptr) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      publish(lane);
+      pend = nullptr;
+    }
+  }
+};
 
 // Paged cache: the slots of a sequence's last block past its length may hold
 // anything, and P = 0 times a NaN there would still reach O through the PV
@@ -656,11 +684,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&o_free[x], 128);
     }
     for (int s = 0; s < NSK; ++s) {
-      mbar_init(&k_full[s], kGather ? 32 : 1);
+      mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&v_full[s], kGather ? 32 : 1);
+      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(drain, 1);
@@ -712,12 +740,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           prefetch_tmap(&tm_v);
         }
       }
-      // A wait every lane takes (the lanes of a gathering warp stay together).
-      auto pwait = [&](uint64_t* bar, uint32_t parity) {
-        if constexpr (kGather)
+      // A wait every lane takes (the lanes of a gathering warp stay together;
+      // a gathered tile held back is published before the warp blocks).
+      GatherRetire retire;
+      auto pwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if constexpr (kGather) {
+          if (__all_sync(FULL, mbar_test_wait(bar, parity))) return true;
+          retire.flush(lane);
           return __all_sync(FULL, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
-        else
+        } else {
           return mbar_wait(bar, parity, abort_flag, kWaitLimitNs);
+        }
       };
       int g = 0;                // K/V tiles issued (ring position)
       int nq[2] = {0, 0};       // Q tiles issued per slot
@@ -753,14 +786,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
           if (g >= NSK && !pwait(&k_empty[sk], phk)) return false;
           if constexpr (kGather) {  // tile j of the item (the cursor's tile)
-            gather_tile<C::KB>(kdst, static_cast<const __nv_bfloat16*>(geo.k_raw), &k_full[sk], geo,
-                               gc, kv_c1, Hkv, lane, status);
+            gather_tile<C::KB>(kdst, static_cast<const __nv_bfloat16*>(geo.k_raw), geo, gc, kv_c1,
+                               Hkv, lane, status);
+            retire.committed(&k_full[sk], lane);
             if (g >= NS && !pwait(&v_empty[st], ph)) {
-              asm volatile("cp.async.wait_all;" ::: "memory");  // K(j) lands before giving up
+              retire.flush(lane);  // K(j) lands before giving up
               return false;
             }
-            gather_tile<C::KB>(vdst, static_cast<const __nv_bfloat16*>(geo.v_raw), &v_full[st], geo,
-                               gc, kv_c1, Hkv, lane, status);
+            gather_tile<C::KB>(vdst, static_cast<const __nv_bfloat16*>(geo.v_raw), geo, gc, kv_c1,
+                               Hkv, lane, status);
+            retire.committed(&v_full[st], lane);
             gc.advance(lane);
           } else if constexpr (kPaged) {
             int pg[PageCursor::NP];
@@ -813,7 +848,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // Drain: every issued copy has landed before the CTA may exit (these
       // waits ignore the abort flag; TMA copies always complete).
-      if constexpr (kGather) asm volatile("cp.async.wait_all;" ::: "memory");
+      if constexpr (kGather) retire.flush(lane);
       int no_abort = 0;
       for (int x = 0; x < 2; ++x)
         if (nq[x] > 0) mbar_wait(&q_full[x], (nq[x] - 1) & 1, &no_abort, kWaitLimitNs);
@@ -873,7 +908,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (nmax == 0) continue;
         // First QK^T of each present tile.
         if (!mbar_wait(&k_full[g % NSK], (g / NSK) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        if constexpr (kGather) fence_proxy_async_smem();  // rows written by cp.async
         for (int x = 0; x < 2 && ok; ++x) {
           if (w.n[x] == 0) continue;
           if (!mbar_wait(&q_full[x], nitem[x] & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
@@ -895,13 +929,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             if (!v_ready && !mbar_wait(&v_full[st], ph, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            if constexpr (kGather) fence_proxy_async_smem();
             v_ready = true;
             tc_fence_after();
             issue_pv(x, st, j > 0);
             if (j + 1 < w.n[x]) {
               if (!k_ready && !mbar_wait(&k_full[st1], ph1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-              if constexpr (kGather) fence_proxy_async_smem();
               k_ready = true;
               tc_fence_after();
               issue_qk(x, st1, j + 2 == w.n[x]);
@@ -1279,8 +1311,8 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       mbar_init(&q_empty[i], 1);
     }
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&k_full[s], kGather ? 32 : 1);
-      mbar_init(&v_full[s], kGather ? 32 : 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
       mbar_init(&k_done[s], 1);
       mbar_init(&pv_done[s], 1);
     }
@@ -1339,9 +1371,15 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
       }
-      auto pwait = [&](uint64_t* bar, int parity) {
-        if constexpr (kGather) return __all_sync(FULL, wait(bar, parity));
-        else return wait(bar, parity);
+      GatherRetire retire;  // gathered tiles are published one tile late
+      auto pwait = [&](uint64_t* bar, int parity) -> bool {
+        if constexpr (kGather) {
+          if (__all_sync(FULL, mbar_test_wait(bar, static_cast<uint32_t>(parity) & 1u))) return true;
+          retire.flush(lane);
+          return __all_sync(FULL, wait(bar, parity));
+        } else {
+          return wait(bar, parity);
+        }
       };
       struct Cur {
         int it, j, n, c1, c2;  // tile j of n; TMA coordinates (rows, heads) of tile 0
@@ -1376,8 +1414,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         if (tk >= NS && !pwait(&k_done[st], (tk / NS) + 1)) return false;
         if constexpr (kGather) {
           gather_tile<1>(smem + C::OFF_K + st * C::TILE_BYTES,
-                         static_cast<const __nv_bfloat16*>(geo.k_raw), &k_full[st], geo, ck.gath,
-                         ck.c1, Hkv, lane, status);
+                         static_cast<const __nv_bfloat16*>(geo.k_raw), geo, ck.gath, ck.c1, Hkv,
+                         lane, status);
+          retire.committed(&k_full[st], lane);
           ck.gath.advance(lane);
         } else if constexpr (kPaged) {
           mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
@@ -1399,8 +1438,9 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         if (tv >= NS && !pwait(&pv_done[st], (tv / NS) + 1)) return false;
         if constexpr (kGather) {
           gather_tile<1>(smem + C::OFF_V + st * C::TILE_BYTES,
-                         static_cast<const __nv_bfloat16*>(geo.v_raw), &v_full[st], geo, cv.gath,
-                         cv.c1, Hkv, lane, status);
+                         static_cast<const __nv_bfloat16*>(geo.v_raw), geo, cv.gath, cv.c1, Hkv,
+                         lane, status);
+          retire.committed(&v_full[st], lane);
           cv.gath.advance(lane);
         } else if constexpr (kPaged) {
           mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
@@ -1428,7 +1468,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       }
       // Drain: every issued copy has landed before the CTA may exit (k_full
       // and v_full count TMA bytes or cp.async arrivals; copies always complete).
-      if constexpr (kGather) asm volatile("cp.async.wait_all;" ::: "memory");
+      if constexpr (kGather) retire.flush(lane);
       int no_abort = 0;
       for (int u = tk > NS ? tk - NS : 0; u < tk; ++u)
         mbar_wait(&k_full[u % NS], (u / NS) & 1, &no_abort, kWaitLimitNs);
@@ -1444,7 +1484,7 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
       int nq = 0;
       bool ok = true;
       Item1 w;
-      int back_bh[NQ], back_qt[NQ];  // dense: the item whose O a buffer holds
+      int back_bh[NQ] = {}, back_qt[NQ] = {};  // dense: the item whose O a buffer holds
       auto store_o = [&](int i) -> bool {  // O tile of the nq-th item i (dense)
         const int qs = i % NQ;
         if (!wait(st_ready, i)) return false;
@@ -1502,7 +1542,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
             ok = false;
             break;
           }
-          if constexpr (kGather) fence_proxy_async_smem();  // rows written by cp.async
           tc_fence_after();
           const uint64_t kd = k_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
 #pragma unroll
@@ -1535,7 +1574,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
             ok = false;
             break;
           }
-          if constexpr (kGather) fence_proxy_async_smem();
           tc_fence_after();
           const uint64_t vd = v_desc0 + static_cast<uint64_t>(t % NS) * kTileStep;
 #pragma unroll
