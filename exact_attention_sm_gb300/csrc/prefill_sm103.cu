@@ -1148,7 +1148,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //              S(t-1) (s_read); commits s_full and k_done.
 //   PV issuer: PV(t) once V(t) has landed (v_full) and the softmax wrote P(t)
 //              (p_ready); commits pv_done (V slot free, P and O may be
-//              rewritten) and, after an item's last PV, o_done.
+//              rewritten; after an item's last PV, its O is final).
 // Epilogue (dense layout): the softmax threads write O / l as bf16 rows into
 // the item's Q buffer (its last QK^T is done) in the tensor map's 128-byte
 // swizzle, and the Q producer stores the tile with one TMA copy before it
@@ -1225,6 +1225,42 @@ __device__ __forceinline__ Item1 decode_item1(int it, bool grouped, int BH, int 
   w.n = kv > 0 ? kv : 0;
   w.zero = kv == 0;
   return w;
+}
+
+// The epilogue of one d = 64 row: O / l as bf16 and the LSE.  Dense layout:
+// the row goes into the item's Q buffer `stage` (its QK^T MMAs are
+// complete), 16-byte chunk c at position c ^ (row % 8) of the 128-byte row
+// (the O map's swizzle; rows past L are clipped by the TMA store, so every
+// row is written) and each warp arrives on st_ready.  Other layouts store
+// the row directly.
+template <bool kTmaStore>
+__device__ __forceinline__ void finish_row(const uint32_t (&r)[2][32], float l, float m_s,
+                                           bool live, size_t orow, __nv_bfloat16* o, float* lse,
+                                           uint8_t* stage, int row, int lane, uint64_t* st_ready) {
+  constexpr int D = Cfg64::D;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint4 q4[8];
+#pragma unroll
+  for (int v8 = 0; v8 < 8; ++v8) {
+    const uint32_t* rv = &r[v8 >> 2][(v8 & 3) * 8];
+    q4[v8].x = attn::pack_bf16x2(__uint_as_float(rv[0]) * inv, __uint_as_float(rv[1]) * inv);
+    q4[v8].y = attn::pack_bf16x2(__uint_as_float(rv[2]) * inv, __uint_as_float(rv[3]) * inv);
+    q4[v8].z = attn::pack_bf16x2(__uint_as_float(rv[4]) * inv, __uint_as_float(rv[5]) * inv);
+    q4[v8].w = attn::pack_bf16x2(__uint_as_float(rv[6]) * inv, __uint_as_float(rv[7]) * inv);
+  }
+  if constexpr (kTmaStore) {
+    uint8_t* buf = stage + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(buf + ((c ^ (row & 7)) << 4)) = q4[c];
+    fence_proxy_async_smem();  // visible to the TMA store
+    __syncwarp();
+    if (lane == 0) mbar_arrive(st_ready);
+  } else if (live) {
+    uint4* orow_p = reinterpret_cast<uint4*>(o + orow * D);
+#pragma unroll
+    for (int v8 = 0; v8 < 8; ++v8) orow_p[v8] = q4[v8];
+  }
+  if (live && lse != nullptr) lse[orow] = l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
 }
 
 template <int kLayout>
@@ -1581,7 +1617,6 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
             mma_bf16_ts(tmem + C::O_COL, tmem + C::P_COL + k * 8, vd + static_cast<uint64_t>(k) * 128,
                         idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(&pv_done[t % NS]);
-          if (j + 1 == w.n) mma_commit(o_done);
         }
         ++nitem;
       }
@@ -1599,6 +1634,12 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
     // ------------------------------------------------------------ softmax warps
+    // An item's epilogue (O / l and the LSE) is deferred into the next
+    // item's first step: that step computes its P while the previous item's
+    // last PV completes (pv_done of the step before), hands P to the tensor
+    // core, then reads the finished O, releases it (o_free: the new item's
+    // first PV waits for it) and normalises and stores the old rows, so the
+    // wait for the last PV and the stores overlap the new item's MMAs.
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;  // row within the Q tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -1608,6 +1649,11 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
     int t = 0;       // global step of the current item's K/V tile 0
     int nitem = 0;
     bool ok = true;
+    // The item whose O is still in TMEM (its epilogue pending).
+    bool pend_on = false, pend_live = false;
+    float pend_m = 0.f, pend_l = 0.f;
+    size_t pend_orow = 0;
+    int pend_slot = 0;
     for (int it = sched.first; ok && it < sched.last; it += sched.step) {
       const Item1 w = item_at(it);
       const int n = w.n;
@@ -1685,9 +1731,10 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
           pk[c >> 6][(c >> 1) & 31] = attn::pack_bf16x2(e.x, e.y);
         }
         const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
-        const float2 r = fadd2(r01, r23);
-        l = l * alpha + (r.x + r.y);
-        // PV of the previous step has read P and updated O.
+        const float2 r2 = fadd2(r01, r23);
+        l = l * alpha + (r2.x + r2.y);
+        // PV of the previous step (at j = 0: the previous item's last PV)
+        // has read P and updated O.
         if (tt > 0) {
           ok = __all_sync(FULL, wait(&pv_done[(tt - 1) % NS], (tt - 1) / NS));
           if (!ok) break;
@@ -1717,50 +1764,45 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_ready);
+        if (j == 0 && pend_on) {
+          // The previous item's last PV completed before this step's wait on
+          // pv_done: read its O, release it (this item's first PV may then
+          // overwrite it) and finish its rows.
+          uint32_t r[2][32];
+          tmem_ld32(o_addr, r[0]);
+          tmem_ld32(o_addr + 32, r[1]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free);
+          finish_row<kTmaStore>(r, pend_l, pend_m, pend_live, pend_orow, o, lse,
+                                smem + C::OFF_Q + pend_slot * C::TILE_BYTES, row, lane,
+                                st_ready);
+          pend_on = false;
+        }
       }
-      if (ok) ok = __all_sync(FULL, wait(o_done, nitem));
       if (!ok) break;
-      tc_fence_after();
-      // O to registers, then release O at once: the next item's first PV may
-      // overwrite it while this thread normalises and stores.
-      uint32_t r[2][32];
-      tmem_ld32(o_addr, r[0]);
-      tmem_ld32(o_addr + 32, r[1]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4 q4[8];
-#pragma unroll
-      for (int v8 = 0; v8 < 8; ++v8) {
-        const uint32_t* rv = &r[v8 >> 2][(v8 & 3) * 8];
-        q4[v8].x = attn::pack_bf16x2(__uint_as_float(rv[0]) * inv, __uint_as_float(rv[1]) * inv);
-        q4[v8].y = attn::pack_bf16x2(__uint_as_float(rv[2]) * inv, __uint_as_float(rv[3]) * inv);
-        q4[v8].z = attn::pack_bf16x2(__uint_as_float(rv[4]) * inv, __uint_as_float(rv[5]) * inv);
-        q4[v8].w = attn::pack_bf16x2(__uint_as_float(rv[6]) * inv, __uint_as_float(rv[7]) * inv);
-      }
-      if constexpr (kTmaStore) {
-        // Row `row` of the tile into this item's Q buffer (its QK^T MMAs are
-        // complete), 16-byte chunk c at position c ^ (row % 8) of the
-        // 128-byte row: the map's swizzle.  Rows past L are clipped by the
-        // store, so every row is written.
-        uint8_t* buf = smem + C::OFF_Q + (nitem % NQ) * C::TILE_BYTES + row * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(buf + ((c ^ (row & 7)) << 4)) = q4[c];
-        fence_proxy_async_smem();  // visible to the TMA store
-        __syncwarp();
-        if (lane == 0) mbar_arrive(st_ready);
-      } else if (grow < w.sq.lq) {
-        uint4* orow = reinterpret_cast<uint4*>(o + orow_index * D);
-#pragma unroll
-        for (int v8 = 0; v8 < 8; ++v8) orow[v8] = q4[v8];
-      }
-      if (grow < w.sq.lq && lse != nullptr)
-        lse[orow_index] = l > 0.f ? (m_s + log2f(l)) * attn::kLn2 : -INFINITY;
+      pend_on = true;
+      pend_m = m_s;
+      pend_l = l;
+      pend_orow = orow_index;
+      pend_live = grow < w.sq.lq;
+      pend_slot = nitem % NQ;
       ++nitem;
       t += n;
+    }
+    // The last item: its final PV, then its epilogue.
+    if (ok && pend_on) {
+      ok = __all_sync(FULL, wait(&pv_done[(t - 1) % NS], (t - 1) / NS));
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[2][32];
+        tmem_ld32(o_addr, r[0]);
+        tmem_ld32(o_addr + 32, r[1]);
+        tmem_ld_wait();
+        finish_row<kTmaStore>(r, pend_l, pend_m, pend_live, pend_orow, o, lse,
+                              smem + C::OFF_Q + pend_slot * C::TILE_BYTES, row, lane, st_ready);
+      }
     }
     if (!ok) {
       if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
