@@ -431,7 +431,8 @@ attn_status_t attn_decode_paged_balanced(const void* q, const void* k_pages, con
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Lq) {
   if (B <= 0 || Hq <= 0 || Lq <= 0) return 0;
-  return round_up(static_cast<size_t>(B) * Hq * Lq * sizeof(float), kAlign);
+  // D (one float per query row), then the kernels' two work counters.
+  return round_up(static_cast<size_t>(B) * Hq * Lq * sizeof(float), kAlign) + kAlign;
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,

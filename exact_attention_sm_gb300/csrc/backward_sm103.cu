@@ -11,7 +11,7 @@
 // Three kernels, no atomics (every gradient element is written by exactly
 // one CTA, sums run in a fixed order, so results are bitwise reproducible):
 //   bwd_rowdot_kernel   D = rowsum(dO * O) per query row (fp32).
-//   bwd_dkdv_kernel     one CTA per (request, KV head, key tile j): K_j, V_j
+//   bwd_dkdv_kernel     work item (request, KV head, key tile j): K_j, V_j
 //                       stay in shared memory while the Q tiles of every
 //                       query head of the group stream past; per Q tile four
 //                       tcgen05 MMAs with the 128 keys as the M dimension:
@@ -20,7 +20,7 @@
 //                         dV  += P^T dO_i            (P^T bf16 from TMEM)
 //                         dK  += dS^T Q_i            (dS^T bf16 from TMEM)
 //                       so neither P nor dS is ever transposed.
-//   bwd_dq_kernel       one CTA per (request, query head, Q tile i): Q_i and
+//   bwd_dq_kernel       work item (request, query head, Q tile i): Q_i and
 //                       dO_i stay while the K/V tiles stream past; per K/V
 //                       tile three MMAs with the queries as M:
 //                         S = Q_i K_j^T,  dP = dO_i V_j^T,  dQ += dS K_j.
@@ -28,11 +28,20 @@
 // against a single kernel that adds dQ with atomics; in exchange the result
 // does not depend on the order in which CTAs finish.
 //
-// Roles (both MMA kernels, 256 threads, one CTA per SM): warp 0 lane 0 loads
-// tiles with TMA, warp 1 lane 0 issues the MMAs, warps 4-7 (one thread per
-// TMEM lane, i.e. per key row in bwd_dkdv and per query row in bwd_dq) do
-// the elementwise work.  Every wait is bounded (ATTN_ERR_DEVICE_TIMEOUT, CTA
-// abort, drain, TMEM freed), as in the forward kernels.
+// Both MMA kernels run one persistent CTA per SM (384 threads) that takes
+// work items from a counter, heaviest first, and loads the next item's
+// tiles while it works on the current one.  Roles: warps 0 and 2 (lane 0)
+// load tiles with TMA, warp 1 lane 0 issues the MMAs, warps 4-11 do the
+// elementwise work in two groups of four, one per half of the tile pair
+// (the 64-query halves of S^T in bwd_dkdv, the 64-key halves of S in
+// bwd_dq); in a group one thread owns one TMEM lane (a key row in bwd_dkdv,
+// a query row in bwd_dq).  S and dP are whole 128 x 128 products (N = 128
+// per instruction), and every hand-off between the issuer and the groups is
+// one barrier, so the single issuing thread stalls the tensor core as
+// little as possible; S of the next tile pair goes into a second TMEM
+// buffer while the groups work on this one (bwd_dq, and bwd_dkdv at
+// d = 64).  Every wait is bounded (ATTN_ERR_DEVICE_TIMEOUT, CTA abort,
+// drain, TMEM freed), as in the forward kernels.
 #include <cuda.h>
 
 #include <algorithm>
@@ -46,9 +55,10 @@ namespace {
 using namespace sm103;
 
 constexpr int T = 128;               // rows of a Q or K/V tile (MMA M and N)
-constexpr int THREADS = 256;         // 8 warps
+constexpr int THREADS = 384;         // 12 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 50000000ull;
 constexpr unsigned FULL = 0xffffffffu;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -83,9 +93,11 @@ struct BwdCfg {
   static constexpr int BLOCK_BYTES = T * 128;   // one 128-row block
   static constexpr int TILE_BYTES = T * D * 2;  // one bf16 tile
   // TMEM columns: S (or S^T) 0..127, dP (or dP^T) 128..255, then the fp32
-  // accumulators.  P^T / dS^T (bf16 pairs) overwrite the first 64 columns
-  // of S^T / dP^T.
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, ACC0_COL = 256, ACC1_COL = 256 + D;
+  // accumulators, and a second S buffer at 384..511 where the accumulators
+  // leave room.  P^T / dS^T / dS (bf16 pairs) of a 64-column half overwrite
+  // the first 32 columns of that half.
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, ACC0_COL = 256, ACC1_COL = 256 + D,
+                            S1_COL = 384;
 };
 
 // Instruction descriptor: kind::f16, bf16 A/B, fp32 D, M = 128.
@@ -94,23 +106,23 @@ __host__ __device__ constexpr uint32_t idesc(int N, bool b_mn_major) {
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(T >> 4) << 24);
 }
 
-// A tile is processed in two halves of H = 64 rows (queries in bwd_dkdv,
-// keys in bwd_dq): the elementwise warps start on the first half while the
-// tensor core computes the second.  Half h of a K-major or MN-major tile
-// starts 64 rows (8 KB, eight whole swizzle atoms) into each column block.
+// The elementwise groups split a tile pair into two halves of H = 64 rows
+// (queries in bwd_dkdv, keys in bwd_dq).  Half h of a K-major or MN-major
+// tile starts 64 rows (8 KB, eight whole swizzle atoms) into each column
+// block.
 constexpr int H = T / 2;
 constexpr uint64_t kHalfStep = (H * 128) >> 4;  // descriptor start-address step of a half
 
-// D(tmem, 128 x H fp32) = A B^T for the 128-row K-major tile A and half of
-// the K-major tile B ([rows][D] bf16, 128-byte swizzle, KB column blocks of
-// BLOCK_BYTES): one MMA per 16 columns of D.
+// D(tmem, 128 x 128 fp32) = A B^T for the 128-row K-major tiles A and B:
+// one MMA per 16 columns of D (N = 128: a wider product per instruction
+// keeps the tensor core busier than two N = 64 halves).
 template <int D>
-__device__ __forceinline__ void mma_kmajor_half(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+__device__ __forceinline__ void mma_kmajor_full(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
   constexpr uint64_t kBlk = BwdCfg<D>::BLOCK_BYTES >> 4;
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint64_t off = (k >> 2) * kBlk + (k & 3) * 2;
-    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc(H, false), k > 0 ? 1u : 0u);
+    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc(T, false), k > 0 ? 1u : 0u);
   }
 }
 
@@ -128,9 +140,12 @@ __device__ __forceinline__ void mma_tmem_a_half(uint32_t d_tmem, uint32_t a_tmem
 
 // D = rowsum(dO * O) for every query row: one warp per row, fp32 sums of the
 // bf16 products in a fixed lane order.
+// Block 0 also zeroes the two work counters of the MMA kernels that follow
+// on the same stream.
 __global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
                                   const __nv_bfloat16* __restrict__ d_o, float* __restrict__ dd,
-                                  long long rows, int d) {
+                                  long long rows, int d, int* work) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) work[threadIdx.x] = 0;
   const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -148,35 +163,48 @@ __global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
 }
 
 }  // namespace
-
 namespace {
 
-// Shared-memory layout of both MMA kernels: six bf16 tiles, then two stages
-// of 128 fp32 per-query values (LSE and D) used by bwd_dkdv, then barriers.
+// Stage counts and shared-memory layout of both MMA kernels.  Each kernel
+// holds two operand tiles for a whole work item (K, V in bwd_dkdv; Q, dO in
+// bwd_dq) in NF slots, so the next item's pair loads during this one at
+// d = 64, and streams the other two (Q, dO; K, V) through an NS-stage ring
+// deep enough to cover the load latency.  Then two stages of 128 fp32
+// per-query values (LSE and D, bwd_dkdv), the item ring, the barriers.
+// Two producer threads load the tiles, one the first and one the second
+// tile of every pair: the copies one thread issues complete one after
+// another (about 24 bytes per clock from L2), so one thread alone would not
+// keep up with the tensor core at d = 64.  Producer 0 arms each pair's
+// barrier for both tiles; producer 1's copy only completes bytes on it.
 template <int D>
 struct BwdSmem {
   using C = BwdCfg<D>;
-  // 6 tiles at t * TILE_BYTES
-  static constexpr int OFF_VEC = 6 * C::TILE_BYTES;
+  static constexpr int NF = D == 64 ? 2 : 1;
+  static constexpr int NS = D == 64 ? 4 : 2;
+  static constexpr int TILES = 2 * NF + 2 * NS;
+  static constexpr int OFF_VEC = TILES * C::TILE_BYTES;
   static constexpr int OFF_BAR = OFF_VEC + 4 * T * 4;
-  static constexpr int USED = OFF_BAR + 256 + 1024;  // barriers + alignment slack
-  // d = 64 would fit two CTAs per SM; each CTA takes all 512 TMEM columns,
-  // so the request is padded to keep one CTA per SM.
-  static constexpr int BYTES = USED > 120 * 1024 ? USED : 120 * 1024;
+  static constexpr int BYTES = OFF_BAR + 512 + 1024;  // barriers, item ring, alignment slack
 };
+static_assert(BwdSmem<64>::BYTES <= 227 * 1024 && BwdSmem<128>::BYTES <= 227 * 1024,
+              "shared memory of one CTA");
+
+constexpr int kItemRing = 8;  // published work items in flight
 
 struct BwdBars {
-  uint64_t* kv_full;   // [2]
-  uint64_t* kv_empty;  // [2]
-  uint64_t* q_full;    // [2]
-  uint64_t* q_empty;   // [2]
-  uint64_t* s_full;    // [2] per half: S (S^T) of the half is in TMEM
-  uint64_t* dp_full;   // [2] per half: dP (dP^T)
-  uint64_t* p_ready;   // [2] per half: P^T written (bwd_dkdv)
-  uint64_t* ds_ready;  // [2] per half: dS (dS^T) written
-  uint64_t* acc_done;
+  uint64_t* hold_full;    // [NF] the item's held pair has landed
+  uint64_t* hold_empty;   // [NF] the item's products are done with it
+  uint64_t* ring_full;    // [NS] a streamed pair has landed
+  uint64_t* ring_empty;   // [NS] the products are done with it
+  uint64_t* s_full;       // [2 S buffers]: S (S^T) is in TMEM
+  uint64_t* dp_full;      // dP (dP^T) is in TMEM
+  uint64_t* p_ready;      // [2 iteration parities]: P^T written (bwd_dkdv)
+  uint64_t* ds_ready;     // dS (dS^T) written
+  uint64_t* acc_done;     // the item's accumulators are final
   uint64_t* drain;
-  uint64_t* vec_full;  // [2] per-query values staged by the elementwise warps
+  uint64_t* vec_full;     // [2] per-query values staged by the elementwise warps
+  uint64_t* item_full;    // [kItemRing] item id published
+  int* items;             // [kItemRing]
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -184,40 +212,51 @@ struct BwdBars {
 __device__ __forceinline__ BwdBars carve_bars(uint8_t* base) {
   uint64_t* b = reinterpret_cast<uint64_t*>(base);
   BwdBars r;
-  r.kv_full = b;
-  r.kv_empty = b + 2;
-  r.q_full = b + 4;
-  r.q_empty = b + 6;
-  r.s_full = b + 8;
-  r.dp_full = b + 10;
-  r.p_ready = b + 12;
-  r.ds_ready = b + 14;
-  r.acc_done = b + 16;
-  r.drain = b + 17;
-  r.vec_full = b + 18;
-  r.tmem_slot = reinterpret_cast<uint32_t*>(b + 20);
+  r.hold_full = b;
+  r.hold_empty = b + 2;
+  r.ring_full = b + 4;
+  r.ring_empty = b + 8;
+  r.s_full = b + 12;
+  r.dp_full = b + 14;
+  r.p_ready = b + 15;
+  r.ds_ready = b + 17;
+  r.acc_done = b + 18;
+  r.drain = b + 19;
+  r.vec_full = b + 20;
+  r.item_full = b + 22;
+  r.items = reinterpret_cast<int*>(b + 22 + kItemRing);
+  r.tmem_slot = reinterpret_cast<uint32_t*>(r.items + kItemRing);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
   return r;
 }
+static_assert((22 + kItemRing) * 8 + kItemRing * 4 + 8 <= 512, "barrier area");
+static_assert(BwdSmem<64>::NF <= 2 && BwdSmem<64>::NS <= 4 && BwdSmem<128>::NF <= 2 &&
+                  BwdSmem<128>::NS <= 4,
+              "barrier counts");
 
 // Barrier set-up, the pending-timeout check and the TMEM allocation shared
 // by both kernels.  Returns false when the CTA must skip its work.
+template <int NF, int NS>
 __device__ __forceinline__ bool bwd_prologue(const BwdBars& bb, int* status) {
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bb.kv_full[s], 1);
-      mbar_init(&bb.kv_empty[s], 1);
-      mbar_init(&bb.q_full[s], 1);
-      mbar_init(&bb.q_empty[s], 1);
-      mbar_init(&bb.s_full[s], 1);
-      mbar_init(&bb.dp_full[s], 1);
-      mbar_init(&bb.p_ready[s], 4);   // one arrival per elementwise warp
-      mbar_init(&bb.ds_ready[s], 4);
+    for (int s = 0; s < NF; ++s) {
+      mbar_init(&bb.hold_full[s], 1);
+      mbar_init(&bb.hold_empty[s], 1);
     }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bb.ring_full[s], 1);
+      mbar_init(&bb.ring_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bb.s_full[s], 1);
+      mbar_init(&bb.p_ready[s], 8);   // one arrival per elementwise warp
+      mbar_init(&bb.vec_full[s], 8);
+    }
+    mbar_init(bb.dp_full, 1);
+    mbar_init(bb.ds_ready, 8);
+    for (int s = 0; s < kItemRing; ++s) mbar_init(&bb.item_full[s], 1);
     mbar_init(bb.acc_done, 1);
     mbar_init(bb.drain, 1);
-    mbar_init(&bb.vec_full[0], 4);
-    mbar_init(&bb.vec_full[1], 4);
     *bb.abort_flag = (status != nullptr &&
                       *reinterpret_cast<volatile int*>(status) == ATTN_ERR_DEVICE_TIMEOUT) ? 2 : 0;
     fence_mbar_init();
@@ -244,13 +283,13 @@ __device__ __forceinline__ void bwd_epilogue(const BwdBars& bb) {
   }
 }
 
-// Writes one 128-column-or-less fp32 TMEM row (D columns from `col`) times
-// `mul` as bf16 to global memory (16-byte stores).
-template <int D>
-__device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, __nv_bfloat16* dst,
-                                               bool live) {
+// Writes NC x 32 fp32 columns of this thread's TMEM lane (from `taddr`)
+// times `mul` as bf16 to global memory (16-byte stores).
+template <int NC>
+__device__ __forceinline__ void store_cols_bf16(uint32_t taddr, float mul, __nv_bfloat16* dst,
+                                                bool live) {
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = 0; c < NC; ++c) {
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
@@ -268,13 +307,88 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, __nv_b
   }
 }
 
+// -inf where column c lies past kv (c > kv) / before lo (c < lo), else x:
+// a compare and a select, no branch.
+__device__ __forceinline__ float neg_inf_if_gt(float x, int c, int kv) {
+  float r;
+  asm("{\n\t.reg .pred q;\n\tsetp.gt.s32 q, %2, %3;\n\tselp.f32 %0, 0fFF800000, %1, q;\n\t}"
+      : "=f"(r)
+      : "f"(x), "r"(c), "r"(kv));
+  return r;
+}
+__device__ __forceinline__ float neg_inf_if_lt(float x, int c, int lo) {
+  float r;
+  asm("{\n\t.reg .pred q;\n\tsetp.lt.s32 q, %2, %3;\n\tselp.f32 %0, 0fFF800000, %1, q;\n\t}"
+      : "=f"(r)
+      : "f"(x), "r"(c), "r"(lo));
+  return r;
+}
+
+// Work items of both kernels, in the order the CTAs claim them: the heads in
+// groups of kHeadGroup; within a group tile index t = 0 (the heaviest under
+// the causal rule) of every head first, then t = 1, ...  The items running
+// at the same time then re-read the same few heads' streamed tiles (Q and dO
+// in bwd_dkdv, K and V in bwd_dq) from L2, and the lightest come last.
+constexpr int kHeadGroup = 32;
+__device__ __forceinline__ void item_order(int x, int nt, int heads, int& t, int& head) {
+  const int per_group = kHeadGroup * nt;
+  const int g0 = (x / per_group) * kHeadGroup;
+  const int rem = x % per_group;
+  const int gsz = min(kHeadGroup, heads - g0);
+  t = rem / gsz;
+  head = g0 + rem % gsz;
+}
+
+// Persistent CTAs take items from a counter in the workspace (zeroed by
+// bwd_rowdot_kernel, which runs first on the same stream): the producer
+// claims one item ahead and publishes each id in the item ring (-1: none
+// left); the issuer and the elementwise warps read the ids in order.  A
+// slot is rewritten only kItemRing items later, after the held-pair and ring
+// barriers have forced every reader past it.
+__device__ __forceinline__ void publish_item(const BwdBars& bb, int k, int x) {
+  bb.items[k % kItemRing] = x;
+  mbar_arrive(&bb.item_full[k % kItemRing]);  // release: the id is visible to the waiters
+}
+
+// dK, dV item: key tile j of KV head bhk; iteration n runs over (query head
+// of the group, Q tile i) with the Q tiles that can see tile j: all of them,
+// or i >= j under the causal (square) rule.
+struct KvItem {
+  int j, bhk, b, hk, i0, per_head, n_iter;
+};
+__device__ __forceinline__ KvItem kv_item(int x, int nk, int nq, int B, int Hq, int Hkv,
+                                          int causal) {
+  KvItem w;
+  item_order(x, nk, B * Hkv, w.j, w.bhk);
+  w.b = w.bhk / Hkv;
+  w.hk = w.bhk % Hkv;
+  w.i0 = causal ? w.j : 0;
+  w.per_head = nq - w.i0;
+  w.n_iter = (Hq / Hkv) * w.per_head;
+  return w;
+}
+
+// dQ item: Q tile i of query head bhq (the last Q tiles, heaviest under the
+// causal rule, first) against the n_iter K/V tiles it sees.
+struct QItem {
+  int i, bhq, bhk, n_iter;
+};
+__device__ __forceinline__ QItem q_item(int x, int nk, int nq, int B, int Hq, int Hkv,
+                                        int causal) {
+  QItem w;
+  int t;
+  item_order(x, nq, B * Hq, t, w.bhq);
+  w.i = nq - 1 - t;
+  w.bhk = (w.bhq / Hq) * Hkv + (w.bhq % Hq) / (Hq / Hkv);
+  w.n_iter = causal ? min(nk, w.i + 1) : nk;
+  return w;
+}
+
 }  // namespace
 
 namespace {
 
-// dK, dV of one key tile j of one (request, KV head).  Iteration n runs over
-// (query head of the group, Q tile i) with the Q tiles that can see tile j:
-// all of them, or i >= j under the causal (square) rule.
+// dK, dV of key tiles (persistent CTAs, one item after another).
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -283,119 +397,177 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                     const float* __restrict__ dd, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int B, int Hq, int Hkv, int Lq, int Lk,
-                    int causal, float scale, int* status) {
+                    int causal, float scale, int* work, int* status) {
   using C = BwdCfg<D>;
   using L = BwdSmem<D>;
+  constexpr int NF = L::NF, NS = L::NS;
+  // Two S^T buffers where TMEM has room (d = 64): S^T of the next Q tile is
+  // computed while the elementwise warps still work on this one.  At d = 128
+  // the accumulators take columns 256..511 and S^T(n + 1) waits for the dV
+  // products that read P^T(n) from S^T(n)'s columns.
+  constexpr bool kTwoS = C::ACC1_COL + D <= C::S1_COL;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const uint32_t sbase = smem_u32(smem);
   const BwdBars bb = carve_bars(smem + L::OFF_BAR);
-  float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);  // [2 stages][LSE*log2e | D][128]
+  float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);  // [2 stages][-LSE*log2e | -D][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (Lk + T - 1) / T, nq = (Lq + T - 1) / T;
-  const int BHkv = B * Hkv;
-  // Heaviest first under the causal rule: all key tiles 0, then tiles 1, ...
-  const int j = static_cast<int>(blockIdx.x) / BHkv;
-  const int bhk = static_cast<int>(blockIdx.x) % BHkv;
-  const int b = bhk / Hkv, hk = bhk % Hkv;
+  const int num_items = nk * B * Hkv;
   const int g = Hq / Hkv;
-  const int i0 = causal ? j : 0;                 // first Q tile that sees key tile j
-  const int per_head = nq - i0;
-  const int n_iter = g * per_head;               // >= 1
-  if (j >= nk) return;
-  if (!bwd_prologue(bb, status)) return;
+  if (!bwd_prologue<NF, NS>(bb, status)) return;
   const uint32_t tmem = *bb.tmem_slot;
-  // Tile slots: K, V, Q[2], dO[2].
-  constexpr int TK = 0, TV = 1, TQ = 2, TDO = 4;
+  // Tiles: K, V of held slot f at 2f, 2f + 1; Q, dO of ring stage s at
+  // 2 NF + 2s, 2 NF + 2s + 1.
   auto tile = [&](int t) { return smem + t * C::TILE_BYTES; };
+  auto taddr = [&](int t) { return sbase + static_cast<uint32_t>(t * C::TILE_BYTES); };
   auto wait = [&](uint64_t* bar, int phase_count) {
     return mbar_wait(bar, static_cast<uint32_t>(phase_count) & 1u, bb.abort_flag, kWaitLimitNs);
   };
+  auto ring_wait = [&](int n) { return wait(&bb.ring_full[n % NS], n / NS); };
+  auto read_item = [&](int k, KvItem& w) -> int {  // 1: item, 0: none left, -1: wait failed
+    if (!wait(&bb.item_full[k % kItemRing], k / kItemRing)) return -1;
+    const int x = *reinterpret_cast<volatile int*>(&bb.items[k % kItemRing]);
+    if (x < 0) return 0;
+    w = kv_item(x, nk, nq, B, Hq, Hkv, causal);
+    return 1;
+  };
+  // S^T(n) (n counts the CTA's iterations over all its items): its TMEM
+  // columns, its barrier for half hh and that barrier's phase.
+  auto s_col = [&](int n) -> uint32_t { return (kTwoS && (n & 1)) ? C::S1_COL : C::S_COL; };
+  auto s_bar = [&](int n) { return &bb.s_full[kTwoS ? (n & 1) : 0]; };
+  auto s_phase = [&](int n) { return kTwoS ? (n >> 1) : n; };
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
     if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(&bb.kv_full[0], 2 * C::TILE_BYTES);
-      for (int kb = 0; kb < C::KB; ++kb) {
-        tma_load_3d(tile(TK) + kb * C::BLOCK_BYTES, &tm_k, &bb.kv_full[0], kb * 64, j * T, bhk);
-        tma_load_3d(tile(TV) + kb * C::BLOCK_BYTES, &tm_v, &bb.kv_full[0], kb * 64, j * T, bhk);
-      }
+      // ------------------------------------------------------------ TMA producers
+      // Producer 0 (warp 0) claims and publishes the items and loads K and
+      // Q; producer 1 (warp 2) reads the published ids and loads V and dO.
+      const int role = warp >> 1;
+      prefetch_tmap(role ? &tm_v : &tm_k);
+      prefetch_tmap(role ? &tm_do : &tm_q);
       bool ok = true;
-      int issued = 0;
-      for (int n = 0; n < n_iter; ++n) {
-        const int st = n & 1;
-        if (n >= 2 && !wait(&bb.q_empty[st], (n >> 1) - 1)) { ok = false; break; }
-        const int bhq = b * Hq + hk * g + n / per_head;
-        const int i = i0 + n % per_head;
-        mbar_arrive_expect_tx(&bb.q_full[st], 2 * C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(tile(TQ + st) + kb * C::BLOCK_BYTES, &tm_q, &bb.q_full[st], kb * 64, i * T, bhq);
-          tma_load_3d(tile(TDO + st) + kb * C::BLOCK_BYTES, &tm_do, &bb.q_full[st], kb * 64, i * T,
-                      bhq);
+      int k = 0, it = 0;
+      int x = role ? 0 : atomicAdd(&work[0], 1);
+      for (;; ++k) {
+        KvItem w;
+        if (role == 0) {
+          const int cur = x < num_items ? x : -1;
+          if (cur >= 0) x = atomicAdd(&work[0], 1);  // the next claim's latency overlaps this item
+          publish_item(bb, k, cur);
+          if (cur < 0) break;
+          w = kv_item(cur, nk, nq, B, Hq, Hkv, causal);
+        } else {
+          const int got = read_item(k, w);
+          if (got < 0) { ok = false; break; }
+          if (got == 0) break;
         }
-        issued = n + 1;
+        const int f = k % NF;
+        if (k >= NF && !wait(&bb.hold_empty[f], k / NF - 1)) { ok = false; break; }
+        uint64_t* hb = &bb.hold_full[f];
+        if (role == 0) mbar_arrive_expect_tx(hb, 2 * C::TILE_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(tile(2 * f + role) + kb * C::BLOCK_BYTES, role ? &tm_v : &tm_k, hb, kb * 64,
+                      w.j * T, w.bhk);
+        for (int n = 0; n < w.n_iter; ++n, ++it) {
+          const int st = it % NS;
+          if (it >= NS && !wait(&bb.ring_empty[st], it / NS - 1)) { ok = false; break; }
+          const int bhq = w.b * Hq + w.hk * g + n / w.per_head;
+          const int i = w.i0 + n % w.per_head;
+          uint64_t* rb = &bb.ring_full[st];
+          if (role == 0) mbar_arrive_expect_tx(rb, 2 * C::TILE_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(tile(2 * NF + 2 * st + role) + kb * C::BLOCK_BYTES, role ? &tm_do : &tm_q, rb,
+                        kb * 64, i * T, bhq);
+        }
+        if (!ok) { ++k; break; }
       }
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
         *bb.abort_flag = 1;
       }
-      // Drain: every issued copy has landed before the CTA may exit.
+      // Drain: every copy this thread issued (k items' held tiles, `it`
+      // ring tiles) has landed before the CTA may exit.  After an abort the
+      // other producer may not have armed a barrier: the short limit then
+      // ends the wait (a copy lands within microseconds).
       int no_abort = 0;
-      mbar_wait(&bb.kv_full[0], 0, &no_abort, kWaitLimitNs);
-      for (int n = issued > 2 ? issued - 2 : 0; n < issued; ++n)
-        mbar_wait(&bb.q_full[n & 1], (n >> 1) & 1, &no_abort, kWaitLimitNs);
+      for (int kk = k > NF ? k - NF : 0; kk < k; ++kk)
+        mbar_wait(&bb.hold_full[kk % NF], (kk / NF) & 1, &no_abort, kDrainLimitNs);
+      for (int n = it > NS ? it - NS : 0; n < it; ++n)
+        mbar_wait(&bb.ring_full[n % NS], (n / NS) & 1, &no_abort, kDrainLimitNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint64_t k_desc = smem_desc_sw128(sbase + TK * C::TILE_BYTES, 16, 1024);
-      const uint64_t v_desc = smem_desc_sw128(sbase + TV * C::TILE_BYTES, 16, 1024);
-      bool ok = wait(&bb.kv_full[0], 0);
-      for (int n = 0; ok && n < n_iter; ++n) {
-        const int st = n & 1;
-        const uint32_t q_addr = sbase + (TQ + st) * C::TILE_BYTES;
-        const uint32_t do_addr = sbase + (TDO + st) * C::TILE_BYTES;
-        if (!wait(&bb.q_full[st], n >> 1)) { ok = false; break; }
+      bool ok = true;
+      int it = 0;
+      for (int k = 0; ok; ++k) {
+        KvItem w;
+        const int got = read_item(k, w);
+        if (got <= 0) { ok = got == 0; break; }
+        const int f = k % NF;
+        const uint64_t k_desc = smem_desc_sw128(taddr(2 * f), 16, 1024);
+        const uint64_t v_desc = smem_desc_sw128(taddr(2 * f + 1), 16, 1024);
+        // S^T(n) = K Q_n^T (keys as rows, queries as columns).
+        auto issue_s = [&](int n) {
+          const uint64_t q_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS)), 16, 1024);
+          mma_kmajor_full<D>(tmem + s_col(n), k_desc, q_k);
+          mma_commit(s_bar(n));
+        };
+        // dP^T(n) = V dO_n^T.
+        auto issue_dp = [&](int n) {
+          const uint64_t do_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS) + 1), 16, 1024);
+          mma_kmajor_full<D>(tmem + C::DP_COL, v_desc, do_k);
+          mma_commit(bb.dp_full);
+        };
+        if (!wait(&bb.hold_full[f], k / NF) || !ring_wait(it)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        // S^T = K Q^T, then dP^T = V dO^T (keys as rows), query half by half:
-        // columns h * 64.. of S^T and dP^T.
-        const uint64_t q_k = smem_desc_sw128(q_addr, 16, 1024);
-        const uint64_t do_k = smem_desc_sw128(do_addr, 16, 1024);
-        for (int hh = 0; hh < 2; ++hh) {
-          mma_kmajor_half<D>(tmem + C::S_COL + hh * H, k_desc, q_k + hh * kHalfStep);
-          mma_commit(&bb.s_full[hh]);
-        }
-        for (int hh = 0; hh < 2; ++hh) {
-          mma_kmajor_half<D>(tmem + C::DP_COL + hh * H, v_desc, do_k + hh * kHalfStep);
-          mma_commit(&bb.dp_full[hh]);
-        }
-        // dV += P^T dO, half by half as P^T arrives (P^T of half h in
-        // columns h * 32.. as bf16 pairs; dO rows h * 64..).
-        const uint64_t do_mn = smem_desc_sw128(do_addr, C::BLOCK_BYTES, 1024);
-        const uint64_t q_mn = smem_desc_sw128(q_addr, C::BLOCK_BYTES, 1024);
-        for (int hh = 0; ok && hh < 2; ++hh) {
-          if (!wait(&bb.p_ready[hh], n)) { ok = false; break; }
+        issue_s(it);
+        issue_dp(it);
+        for (int n = 0; ok && n < w.n_iter; ++n, ++it) {
+          const int st = it % NS;
+          const bool more = n + 1 < w.n_iter;
+          if (kTwoS && more) {
+            if (!ring_wait(it + 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(it + 1);
+          }
+          // dV += P^T dO_n once both groups have written P^T (bf16 pairs in
+          // the first 32 columns of each query half's S^T columns; dO rows
+          // h * 64..).  The first product of an item overwrites the
+          // accumulator: both groups have stored the previous item's
+          // gradients before their P^T(n) arrival.
+          const uint64_t q_mn = smem_desc_sw128(taddr(2 * NF + 2 * st), C::BLOCK_BYTES, 1024);
+          const uint64_t do_mn = smem_desc_sw128(taddr(2 * NF + 2 * st + 1), C::BLOCK_BYTES, 1024);
+          if (!wait(&bb.p_ready[it & 1], it >> 1)) { ok = false; break; }
           tc_fence_after();
-          mma_tmem_a_half<D>(tmem + C::ACC1_COL, tmem + C::S_COL + hh * (H / 2),
-                             do_mn + hh * kHalfStep, n > 0 || hh > 0);
-        }
-        // dK += dS^T Q, half by half as dS^T arrives.
-        for (int hh = 0; ok && hh < 2; ++hh) {
-          if (!wait(&bb.ds_ready[hh], n)) { ok = false; break; }
+          for (int hh = 0; hh < 2; ++hh)
+            mma_tmem_a_half<D>(tmem + C::ACC1_COL, tmem + s_col(it) + hh * H,
+                               do_mn + hh * kHalfStep, n > 0 || hh > 0);
+          if (!kTwoS && more) {
+            if (!ring_wait(it + 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(it + 1);  // over P^T(n), after the dV products that read it
+          }
+          // dK += dS^T Q_n once both groups have written dS^T, then dP^T(n + 1)
+          // over the dP^T columns those products read.
+          if (!wait(bb.ds_ready, it)) { ok = false; break; }
           tc_fence_after();
-          mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + C::DP_COL + hh * (H / 2),
-                             q_mn + hh * kHalfStep, n > 0 || hh > 0);
+          for (int hh = 0; hh < 2; ++hh)
+            mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + C::DP_COL + hh * H,
+                               q_mn + hh * kHalfStep, n > 0 || hh > 0);
+          if (more) issue_dp(it + 1);
+          mma_commit(&bb.ring_empty[st]);  // Q and dO of this stage may be refilled
         }
         if (!ok) break;
-        mma_commit(&bb.q_empty[st]);  // Q and dO of this stage may be refilled
+        mma_commit(bb.acc_done);
+        mma_commit(&bb.hold_empty[f]);     // K and V of this slot may be refilled
       }
-      if (ok) mma_commit(bb.acc_done);
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
         *bb.abort_flag = 1;
@@ -406,136 +578,147 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ elementwise
+    // Two groups of four warps: group hh works on query half hh of every
+    // tile pair, each thread on key row c (its TMEM lane).
+    const int half = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int c = quad * 32 + lane;               // key row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float scale_log2 = scale * attn::kLog2e;
-    const int kk = j * T + c;                      // this thread's key
-    // Per-query values of iteration n for query column c (this thread
-    // stages one of the 128), negated for the packed FMAs: -LSE in the log2
-    // domain (-inf where the query row does not exist or sees no key, so
-    // that P = 0) and -D.
-    auto fetch = [&](int n, float& l2, float& dv_) {
-      l2 = -INFINITY;
-      dv_ = 0.f;
-      if (n < n_iter) {
-        const int bhq = b * Hq + hk * g + n / per_head;
-        const int row = (i0 + n % per_head) * T + c;
-        if (row < Lq) {
-          const float x = lse[static_cast<size_t>(bhq) * Lq + row];
-          if (x != -INFINITY) l2 = -x * attn::kLog2e;
-          dv_ = -dd[static_cast<size_t>(bhq) * Lq + row];
-        }
-      }
+    // Per-query values of iteration n of item w for query column c, negated
+    // for the packed FMAs: group 0 stages -LSE in the log2 domain (-inf
+    // where the query row does not exist or sees no key, so that P = 0),
+    // group 1 -D.
+    auto fetch = [&](const KvItem& w, int n) -> float {
+      const int bhq = w.b * Hq + w.hk * g + n / w.per_head;
+      const int row = (w.i0 + n % w.per_head) * T + c;
+      if (row >= Lq) return half == 0 ? -INFINITY : 0.f;
+      const size_t at = static_cast<size_t>(bhq) * Lq + row;
+      if (half != 0) return -dd[at];
+      const float x = lse[at];
+      return x == -INFINITY ? -INFINITY : -x * attn::kLog2e;
     };
-    float pre_l2, pre_d;
-    fetch(0, pre_l2, pre_d);
-    bool ok = true;
-    for (int n = 0; n < n_iter; ++n) {
-      const int st = n & 1;
-      float* l2s = vec + st * 2 * T;
-      float* ds_ = l2s + T;
-      // Every warp writes its 32 values, then waits for the other three
-      // (an mbarrier, so the wait stays bounded).  A warp's arrival for n
-      // follows its last read of stage n - 1, so once all four have arrived
-      // for n, stage (n + 1) & 1 may be overwritten.
-      l2s[c] = pre_l2;
-      ds_[c] = pre_d;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bb.vec_full[st]);
-      ok = __all_sync(FULL, wait(&bb.vec_full[st], n >> 1));
-      if (!ok) break;
-      fetch(n + 1, pre_l2, pre_d);
-      const int i = i0 + n % per_head;
-      const bool diag = causal && i == j;          // keys past the query are masked here
-      // P^T row c, query half by half: P[r] = 2^(S^T[c][r] scale log2e -
-      // LSE_r log2e) as bf16 pairs, written to columns h * 32.. (over S^T
-      // columns this thread has already read).
-      uint32_t pw[64];
-      for (int hh = 0; ok && hh < 2; ++hh) {
-        ok = __all_sync(FULL, wait(&bb.s_full[hh], n));
+    KvItem w, nxt;
+    int got = __shfl_sync(FULL, read_item(0, w), 0);
+    bool ok = got >= 0;
+    float pre = got > 0 ? fetch(w, 0) : 0.f;
+    int it = 0;
+    for (int k = 0; ok && got > 0; ++k) {
+      int got_next = 0;
+      for (int n = 0; n < w.n_iter; ++n, ++it) {
+        const int st = it & 1;
+        float* l2s = vec + st * 2 * T;
+        float* ds_ = l2s + T;
+        // Every warp writes its 32 values, then waits for the other seven
+        // (an mbarrier, so the wait stays bounded).  A warp's arrival for
+        // it follows its last read of stage it - 1, so once all eight have
+        // arrived for it, stage (it + 1) & 1 may be overwritten.
+        (half == 0 ? l2s : ds_)[c] = pre;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bb.vec_full[st]);
+        ok = __all_sync(FULL, wait(&bb.vec_full[st], it >> 1));
+        if (!ok) break;
+        if (n + 1 < w.n_iter) {
+          pre = fetch(w, n + 1);
+        } else {                                   // the next item's first values
+          got_next = read_item(k + 1, nxt);
+          ok = __all_sync(FULL, got_next >= 0);
+          if (!ok) break;
+          pre = got_next > 0 ? fetch(nxt, 0) : 0.f;
+        }
+        const int i = w.i0 + n % w.per_head;
+        // P^T row c over this group's query half: P[r] = 2^(S^T[c][r] scale
+        // log2e - LSE_r log2e), 0 for queries before key c on the diagonal
+        // tile; bf16 pairs over the half's first 32 S^T columns.
+        ok = __all_sync(FULL, wait(s_bar(it), s_phase(it)));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[2][32];
-        tmem_ld32(tmem + lane_off + C::S_COL + hh * H, sr[0]);
-        tmem_ld32(tmem + lane_off + C::S_COL + hh * H + 32, sr[1]);
-        tmem_ld_wait();
-        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const uint32_t s_addr = tmem + lane_off + s_col(it) + half * H;
+        uint32_t pw[H / 2];
+        {
+          uint32_t sr[2][32];
+          tmem_ld32(s_addr, sr[0]);
+          tmem_ld32(s_addr + 32, sr[1]);
+          tmem_ld_wait();
+          float x[H];
+          const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
-        for (int e = 0; e < H; e += 4) {
-          const int r = hh * H + e;
-          const float4 nl = *reinterpret_cast<const float4*>(&l2s[r]);
-          float2 pa = ffma2(make_float2(__uint_as_float(sr[e >> 5][e & 31]),
-                                        __uint_as_float(sr[e >> 5][(e & 31) + 1])),
-                            sc2, make_float2(nl.x, nl.y));
-          float2 pb = ffma2(make_float2(__uint_as_float(sr[e >> 5][(e & 31) + 2]),
-                                        __uint_as_float(sr[e >> 5][(e & 31) + 3])),
-                            sc2, make_float2(nl.z, nl.w));
-          pa.x = ex2(pa.x);
-          pa.y = ex2(pa.y);
-          pb.x = ex2(pb.x);
-          pb.y = ex2(pb.y);
-          if (diag) {
-            if (kk > i * T + r) pa.x = 0.f;
-            if (kk > i * T + r + 1) pa.y = 0.f;
-            if (kk > i * T + r + 2) pb.x = 0.f;
-            if (kk > i * T + r + 3) pb.y = 0.f;
+          for (int e = 0; e < H; e += 4) {
+            const float4 nl = *reinterpret_cast<const float4*>(&l2s[half * H + e]);
+            const float2 xa = ffma2(make_float2(__uint_as_float(sr[e >> 5][e & 31]),
+                                                __uint_as_float(sr[e >> 5][(e & 31) + 1])),
+                                    sc2, make_float2(nl.x, nl.y));
+            const float2 xb = ffma2(make_float2(__uint_as_float(sr[e >> 5][(e & 31) + 2]),
+                                                __uint_as_float(sr[e >> 5][(e & 31) + 3])),
+                                    sc2, make_float2(nl.z, nl.w));
+            x[e] = xa.x;
+            x[e + 1] = xa.y;
+            x[e + 2] = xb.x;
+            x[e + 3] = xb.y;
           }
-          pw[r >> 1] = attn::pack_bf16x2(pa.x, pa.y);
-          pw[(r >> 1) + 1] = attn::pack_bf16x2(pb.x, pb.y);
+          if (causal && i == w.j) {                // query i T + half H + e < key j T + c
+            const int lo = c - half * H;
+#pragma unroll
+            for (int e = 0; e < H; ++e) x[e] = neg_inf_if_lt(x[e], e, lo);
+          }
+#pragma unroll
+          for (int e = 0; e < H; e += 2) pw[e >> 1] = attn::pack_bf16x2(ex2(x[e]), ex2(x[e + 1]));
         }
-        tmem_st32(tmem + lane_off + C::S_COL + hh * (H / 2),
-                  *reinterpret_cast<uint32_t(*)[32]>(&pw[hh * 32]));
+        tmem_st32(s_addr, pw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bb.p_ready[hh]);
-      }
-      if (!ok) break;
-      // dS^T row c: dS[r] = P[r] (dP^T[c][r] - D_r), with P as handed to the
-      // MMA, written over dP^T columns this thread has already read.
-      for (int hh = 0; ok && hh < 2; ++hh) {
-        ok = __all_sync(FULL, wait(&bb.dp_full[hh], n));
+        if (lane == 0) mbar_arrive(&bb.p_ready[st]);
+        // dS^T row c: dS[r] = P[r] (dP^T[c][r] - D_r), with P as handed to
+        // the MMA, over the half's first 32 dP^T columns (already read).
+        ok = __all_sync(FULL, wait(bb.dp_full, it));
         if (!ok) break;
         tc_fence_after();
+        const uint32_t dp_addr = tmem + lane_off + C::DP_COL + half * H;
         uint32_t dr[2][32];
-        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H, dr[0]);
-        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H + 32, dr[1]);
+        tmem_ld32(dp_addr, dr[0]);
+        tmem_ld32(dp_addr + 32, dr[1]);
         tmem_ld_wait();
-        uint32_t sw[32];
+        uint32_t sw[H / 2];
         const float2 zero2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < H; e += 4) {
-          const int r = hh * H + e;
-          const float4 nd = *reinterpret_cast<const float4*>(&ds_[r]);
+          const float4 nd = *reinterpret_cast<const float4*>(&ds_[half * H + e]);
           const float2 xa = fadd2(make_float2(__uint_as_float(dr[e >> 5][e & 31]),
                                               __uint_as_float(dr[e >> 5][(e & 31) + 1])),
                                   make_float2(nd.x, nd.y));
           const float2 xb = fadd2(make_float2(__uint_as_float(dr[e >> 5][(e & 31) + 2]),
                                               __uint_as_float(dr[e >> 5][(e & 31) + 3])),
                                   make_float2(nd.z, nd.w));
-          const uint32_t p0 = pw[r >> 1], p1 = pw[(r >> 1) + 1];
+          const uint32_t p0 = pw[e >> 1], p1 = pw[(e >> 1) + 1];
           const float2 sa = ffma2(make_float2(attn::bf16_lo(p0), attn::bf16_hi(p0)), xa, zero2);
           const float2 sb = ffma2(make_float2(attn::bf16_lo(p1), attn::bf16_hi(p1)), xb, zero2);
           sw[e >> 1] = attn::pack_bf16x2(sa.x, sa.y);
           sw[(e >> 1) + 1] = attn::pack_bf16x2(sb.x, sb.y);
         }
-        tmem_st32(tmem + lane_off + C::DP_COL + hh * (H / 2), sw);
+        tmem_st32(dp_addr, sw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bb.ds_ready[hh]);
+        if (lane == 0) mbar_arrive(bb.ds_ready);
       }
       if (!ok) break;
-    }
-    if (ok) ok = __all_sync(FULL, wait(bb.acc_done, 0));
-    if (ok) {
+      // The item's gradients: group 0 writes dV row j T + c, group 1 dK.
+      ok = __all_sync(FULL, wait(bb.acc_done, k));
+      if (!ok) break;
       tc_fence_after();
+      const int kk = w.j * T + c;
       const bool live = kk < Lk;
-      const size_t out_row = (static_cast<size_t>(bhk) * Lk + (live ? kk : 0)) * D;
-      store_row_bf16<D>(tmem + lane_off + C::ACC0_COL, scale, dk + out_row, live);
-      store_row_bf16<D>(tmem + lane_off + C::ACC1_COL, 1.f, dv + out_row, live);
-    } else {
+      const size_t out_row = (static_cast<size_t>(w.bhk) * Lk + (live ? kk : 0)) * D;
+      if (half == 0)
+        store_cols_bf16<D / 32>(tmem + lane_off + C::ACC1_COL, 1.f, dv + out_row, live);
+      else
+        store_cols_bf16<D / 32>(tmem + lane_off + C::ACC0_COL, scale, dk + out_row, live);
+      tc_fence_before();
+      w = nxt;
+      got = got_next;
+    }
+    if (!ok) {
       if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
       *bb.abort_flag = 1;
     }
@@ -547,8 +730,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 namespace {
 
-// dQ of one Q tile i of one (request, query head): the K/V tiles it sees
-// stream through a two-stage ring.
+// dQ of Q tiles (persistent CTAs, one item after another): the K/V tiles an
+// item sees stream through the ring.
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -556,9 +739,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                   const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
                   const float* __restrict__ dd, __nv_bfloat16* __restrict__ dq, int B, int Hq,
-                  int Hkv, int Lq, int Lk, int causal, float scale, int* status) {
+                  int Hkv, int Lq, int Lk, int causal, float scale, int* work, int* status) {
   using C = BwdCfg<D>;
   using L = BwdSmem<D>;
+  constexpr int NF = L::NF, NS = L::NS;
+  // Two S buffers (the accumulator takes D columns from 256): S of the next
+  // K/V tile is computed while the elementwise warps work on this one.
+  static_assert(C::ACC0_COL + D <= C::S1_COL, "TMEM columns");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -567,91 +754,135 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (Lk + T - 1) / T, nq = (Lq + T - 1) / T;
-  const int BHq = B * Hq;
-  // Heaviest first under the causal rule: the last Q tiles of every head first.
-  const int i = nq - 1 - static_cast<int>(blockIdx.x) / BHq;
-  const int bhq = static_cast<int>(blockIdx.x) % BHq;
-  const int b = bhq / Hq, h = bhq % Hq;
-  const int bhk = b * Hkv + h / (Hq / Hkv);
-  const int n_iter = causal ? min(nk, i + 1) : nk;  // K/V tiles this Q tile sees
-  if (i < 0) return;
-  if (!bwd_prologue(bb, status)) return;
+  const int num_items = nq * B * Hq;
+  if (!bwd_prologue<NF, NS>(bb, status)) return;
   const uint32_t tmem = *bb.tmem_slot;
-  // Tile slots: Q, dO, K[2], V[2].
-  constexpr int TQ = 0, TDO = 1, TK = 2, TV = 4;
-  auto tile = [&](int t) { return smem + t * C::TILE_BYTES; };
+  // Tiles: Q, dO of held slot f at 2f, 2f + 1; K, V of ring stage s at
+  // 2 NF + 2s, 2 NF + 2s + 1.
+  auto tile = [&](int tt) { return smem + tt * C::TILE_BYTES; };
+  auto taddr = [&](int tt) { return sbase + static_cast<uint32_t>(tt * C::TILE_BYTES); };
   auto wait = [&](uint64_t* bar, int phase_count) {
     return mbar_wait(bar, static_cast<uint32_t>(phase_count) & 1u, bb.abort_flag, kWaitLimitNs);
   };
+  auto ring_wait = [&](int n) { return wait(&bb.ring_full[n % NS], n / NS); };
+  auto read_item = [&](int k, QItem& w) -> int {  // 1: item, 0: none left, -1: wait failed
+    if (!wait(&bb.item_full[k % kItemRing], k / kItemRing)) return -1;
+    const int x = *reinterpret_cast<volatile int*>(&bb.items[k % kItemRing]);
+    if (x < 0) return 0;
+    w = q_item(x, nk, nq, B, Hq, Hkv, causal);
+    return 1;
+  };
+  auto s_col = [&](int it) -> uint32_t { return (it & 1) ? C::S1_COL : C::S_COL; };
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
     if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(&bb.q_full[0], 2 * C::TILE_BYTES);
-      for (int kb = 0; kb < C::KB; ++kb) {
-        tma_load_3d(tile(TQ) + kb * C::BLOCK_BYTES, &tm_q, &bb.q_full[0], kb * 64, i * T, bhq);
-        tma_load_3d(tile(TDO) + kb * C::BLOCK_BYTES, &tm_do, &bb.q_full[0], kb * 64, i * T, bhq);
-      }
+      // ------------------------------------------------------------ TMA producers
+      // Producer 0 (warp 0) claims and publishes the items and loads Q and
+      // K; producer 1 (warp 2) reads the published ids and loads dO and V.
+      const int role = warp >> 1;
+      prefetch_tmap(role ? &tm_do : &tm_q);
+      prefetch_tmap(role ? &tm_v : &tm_k);
       bool ok = true;
-      int issued = 0;
-      for (int jt = 0; jt < n_iter; ++jt) {
-        const int st = jt & 1;
-        if (jt >= 2 && !wait(&bb.kv_empty[st], (jt >> 1) - 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bb.kv_full[st], 2 * C::TILE_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb) {
-          tma_load_3d(tile(TK + st) + kb * C::BLOCK_BYTES, &tm_k, &bb.kv_full[st], kb * 64, jt * T, bhk);
-          tma_load_3d(tile(TV + st) + kb * C::BLOCK_BYTES, &tm_v, &bb.kv_full[st], kb * 64, jt * T, bhk);
+      int k = 0, it = 0;
+      int x = role ? 0 : atomicAdd(&work[1], 1);
+      for (;; ++k) {
+        QItem w;
+        if (role == 0) {
+          const int cur = x < num_items ? x : -1;
+          if (cur >= 0) x = atomicAdd(&work[1], 1);
+          publish_item(bb, k, cur);
+          if (cur < 0) break;
+          w = q_item(cur, nk, nq, B, Hq, Hkv, causal);
+        } else {
+          const int got = read_item(k, w);
+          if (got < 0) { ok = false; break; }
+          if (got == 0) break;
         }
-        issued = jt + 1;
+        const int f = k % NF;
+        if (k >= NF && !wait(&bb.hold_empty[f], k / NF - 1)) { ok = false; break; }
+        uint64_t* hb = &bb.hold_full[f];
+        if (role == 0) mbar_arrive_expect_tx(hb, 2 * C::TILE_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(tile(2 * f + role) + kb * C::BLOCK_BYTES, role ? &tm_do : &tm_q, hb, kb * 64,
+                      w.i * T, w.bhq);
+        for (int jt = 0; jt < w.n_iter; ++jt, ++it) {
+          const int st = it % NS;
+          if (it >= NS && !wait(&bb.ring_empty[st], it / NS - 1)) { ok = false; break; }
+          uint64_t* rb = &bb.ring_full[st];
+          if (role == 0) mbar_arrive_expect_tx(rb, 2 * C::TILE_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(tile(2 * NF + 2 * st + role) + kb * C::BLOCK_BYTES, role ? &tm_v : &tm_k, rb,
+                        kb * 64, jt * T, w.bhk);
+        }
+        if (!ok) { ++k; break; }
       }
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
         *bb.abort_flag = 1;
       }
       int no_abort = 0;
-      mbar_wait(&bb.q_full[0], 0, &no_abort, kWaitLimitNs);
-      for (int jt = issued > 2 ? issued - 2 : 0; jt < issued; ++jt)
-        mbar_wait(&bb.kv_full[jt & 1], (jt >> 1) & 1, &no_abort, kWaitLimitNs);
+      for (int kk = k > NF ? k - NF : 0; kk < k; ++kk)
+        mbar_wait(&bb.hold_full[kk % NF], (kk / NF) & 1, &no_abort, kDrainLimitNs);
+      for (int n = it > NS ? it - NS : 0; n < it; ++n)
+        mbar_wait(&bb.ring_full[n % NS], (n / NS) & 1, &no_abort, kDrainLimitNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint64_t q_desc = smem_desc_sw128(sbase + TQ * C::TILE_BYTES, 16, 1024);
-      const uint64_t do_desc = smem_desc_sw128(sbase + TDO * C::TILE_BYTES, 16, 1024);
-      bool ok = wait(&bb.q_full[0], 0);
-      for (int jt = 0; ok && jt < n_iter; ++jt) {
-        const int st = jt & 1;
-        const uint32_t k_addr = sbase + (TK + st) * C::TILE_BYTES;
-        const uint32_t v_addr = sbase + (TV + st) * C::TILE_BYTES;
-        if (!wait(&bb.kv_full[st], jt >> 1)) { ok = false; break; }
-        tc_fence_after();
-        // S = Q K^T and dP = dO V^T (queries as rows), key half by half:
-        // columns h * 64.. of S and dP.
-        const uint64_t k_k = smem_desc_sw128(k_addr, 16, 1024);
-        const uint64_t v_k = smem_desc_sw128(v_addr, 16, 1024);
-        for (int hh = 0; hh < 2; ++hh) {
-          mma_kmajor_half<D>(tmem + C::S_COL + hh * H, q_desc, k_k + hh * kHalfStep);
-          mma_commit(&bb.s_full[hh]);
-          mma_kmajor_half<D>(tmem + C::DP_COL + hh * H, do_desc, v_k + hh * kHalfStep);
-          mma_commit(&bb.dp_full[hh]);
+      bool ok = true;
+      int it = 0;
+      for (int k = 0; ok; ++k) {
+        QItem w;
+        const int got = read_item(k, w);
+        if (got <= 0) { ok = got == 0; break; }
+        const int f = k % NF;
+        const uint64_t q_desc = smem_desc_sw128(taddr(2 * f), 16, 1024);
+        const uint64_t do_desc = smem_desc_sw128(taddr(2 * f + 1), 16, 1024);
+        // S(it) = Q K^T (queries as rows, keys as columns).
+        auto issue_s = [&](int n) {
+          const uint64_t k_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS)), 16, 1024);
+          mma_kmajor_full<D>(tmem + s_col(n), q_desc, k_k);
+          mma_commit(&bb.s_full[n & 1]);
+        };
+        // dP(it) = dO V^T.
+        auto issue_dp = [&](int n) {
+          const uint64_t v_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS) + 1), 16, 1024);
+          mma_kmajor_full<D>(tmem + C::DP_COL, do_desc, v_k);
+          mma_commit(bb.dp_full);
+        };
+        if (!wait(&bb.hold_full[f], k / NF) || !ring_wait(it)) {
+          ok = false;
+          break;
         }
-        // dQ += dS K, half by half as dS arrives (dS of half h in columns
-        // DP_COL + h * 32.. as bf16 pairs; K rows h * 64..).
-        const uint64_t k_mn = smem_desc_sw128(k_addr, C::BLOCK_BYTES, 1024);
-        for (int hh = 0; ok && hh < 2; ++hh) {
-          if (!wait(&bb.ds_ready[hh], jt)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(it);
+        issue_dp(it);
+        for (int jt = 0; ok && jt < w.n_iter; ++jt, ++it) {
+          const int st = it % NS;
+          const bool more = jt + 1 < w.n_iter;
+          if (more) {
+            if (!ring_wait(it + 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(it + 1);
+          }
+          // dQ += dS K once both groups have written dS (bf16 pairs in
+          // columns DP_COL + h * 64.. for key half h; K rows h * 64..), then
+          // dP of the next tile over the columns those products read.  The
+          // item's first product overwrites the accumulator: group 0, which
+          // alone stores dQ, has done so before its dS arrival.
+          const uint64_t k_mn = smem_desc_sw128(taddr(2 * NF + 2 * st), C::BLOCK_BYTES, 1024);
+          if (!wait(bb.ds_ready, it)) { ok = false; break; }
           tc_fence_after();
-          mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + C::DP_COL + hh * (H / 2),
-                             k_mn + hh * kHalfStep, jt > 0 || hh > 0);
+          for (int hh = 0; hh < 2; ++hh)
+            mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + C::DP_COL + hh * H,
+                               k_mn + hh * kHalfStep, jt > 0 || hh > 0);
+          if (more) issue_dp(it + 1);
+          mma_commit(&bb.ring_empty[st]);  // K and V of this stage may be refilled
         }
         if (!ok) break;
-        mma_commit(&bb.kv_empty[st]);  // K and V of this stage may be refilled
+        mma_commit(bb.acc_done);
+        mma_commit(&bb.hold_empty[f]);     // Q and dO of this slot may be refilled
       }
-      if (ok) mma_commit(bb.acc_done);
       if (!ok) {
         attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
         *bb.abort_flag = 1;
@@ -662,68 +893,107 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ elementwise
+    // Two groups of four warps: group hh works on key half hh of every K/V
+    // tile, each thread on query row r (its TMEM lane).
+    const int half = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float scale_log2 = scale * attn::kLog2e;
-    const int qrow = i * T + r;
-    const bool live = qrow < Lq;
-    float l2 = INFINITY, drow = 0.f;             // +inf: a row that does not exist has P = 0
-    if (live) {
-      const float x = lse[static_cast<size_t>(bhq) * Lq + qrow];
-      if (x != -INFINITY) l2 = x * attn::kLog2e;
-      drow = dd[static_cast<size_t>(bhq) * Lq + qrow];
-    }
-    bool ok = true;
-    for (int jt = 0; ok && jt < n_iter; ++jt) {
-      // Keys past Lk, and past the query under the causal rule, get P = 0.
+    const float2 sc2 = make_float2(scale_log2, scale_log2);
+    const float2 zero2 = make_float2(0.f, 0.f);
+    // -LSE log2e (-inf where the row does not exist or sees no key: P = 0)
+    // and -D of this thread's query row in item w.
+    auto fetch = [&](const QItem& w, float& nl, float& nd) {
+      const int qrow = w.i * T + r;
+      nl = -INFINITY;
+      nd = 0.f;
+      if (qrow < Lq) {
+        const float x = lse[static_cast<size_t>(w.bhq) * Lq + qrow];
+        if (x != -INFINITY) nl = -x * attn::kLog2e;
+        nd = -dd[static_cast<size_t>(w.bhq) * Lq + qrow];
+      }
+    };
+    QItem w, nxt;
+    int got = __shfl_sync(FULL, read_item(0, w), 0);
+    bool ok = got >= 0;
+    float pre_l = 0.f, pre_d = 0.f;
+    if (got > 0) fetch(w, pre_l, pre_d);
+    int it = 0;
+    for (int k = 0; ok && got > 0; ++k) {
+      const float2 nl2 = make_float2(pre_l, pre_l), nd2 = make_float2(pre_d, pre_d);
+      const int qrow = w.i * T + r;
+      // Keys past Lk, and past the query under the causal rule, get P = 0;
+      // only the diagonal tile and a ragged last tile hold any.
       const int kmax = causal ? min(Lk - 1, qrow) : Lk - 1;
-      for (int hh = 0; ok && hh < 2; ++hh) {
-        ok = __all_sync(FULL, wait(&bb.s_full[hh], jt)) &&
-             __all_sync(FULL, wait(&bb.dp_full[hh], jt));
+      int got_next = 0;
+      for (int jt = 0; jt < w.n_iter; ++jt, ++it) {
+        if (jt + 1 == w.n_iter) {                  // the next item's row values
+          got_next = read_item(k + 1, nxt);
+          ok = __all_sync(FULL, got_next >= 0);
+          if (!ok) break;
+          if (got_next > 0) fetch(nxt, pre_l, pre_d);
+        }
+        const bool need_mask = (causal && jt == w.i) || (jt + 1) * T > Lk;
+        ok = __all_sync(FULL, wait(&bb.s_full[it & 1], it >> 1)) &&
+             __all_sync(FULL, wait(bb.dp_full, it));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[2][32], dr[2][32];
-        tmem_ld32(tmem + lane_off + C::S_COL + hh * H, sr[0]);
-        tmem_ld32(tmem + lane_off + C::S_COL + hh * H + 32, sr[1]);
-        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H, dr[0]);
-        tmem_ld32(tmem + lane_off + C::DP_COL + hh * H + 32, dr[1]);
-        tmem_ld_wait();
-        uint32_t sw[32];
-        const float2 sc2 = make_float2(scale_log2, scale_log2);
-        const float2 nl2 = make_float2(-l2, -l2), nd2 = make_float2(-drow, -drow);
-        const float2 zero2 = make_float2(0.f, 0.f);
+        const uint32_t s_addr = tmem + lane_off + s_col(it) + half * H;
+        const uint32_t dp_addr = tmem + lane_off + C::DP_COL + half * H;
+        // dS over 32 keys at a time, written 16 pair columns at a time over
+        // dP columns this thread has already read.
 #pragma unroll
-        for (int e = 0; e < H; e += 2) {
-          const int key = jt * T + hh * H + e;
-          float2 p = ffma2(make_float2(__uint_as_float(sr[e >> 5][e & 31]),
-                                       __uint_as_float(sr[e >> 5][(e & 31) + 1])),
-                           sc2, nl2);
-          p.x = key > kmax ? 0.f : ex2(p.x);
-          p.y = key + 1 > kmax ? 0.f : ex2(p.y);
-          // P is rounded to bf16 as in the forward's P V product and in bwd_dkdv.
-          const uint32_t pw = attn::pack_bf16x2(p.x, p.y);
-          const float2 x = fadd2(make_float2(__uint_as_float(dr[e >> 5][e & 31]),
-                                             __uint_as_float(dr[e >> 5][(e & 31) + 1])),
-                                 nd2);
-          const float2 ds2 = ffma2(make_float2(attn::bf16_lo(pw), attn::bf16_hi(pw)), x, zero2);
-          sw[e >> 1] = attn::pack_bf16x2(ds2.x, ds2.y);
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(s_addr + ch * 32, sr);
+          tmem_ld32(dp_addr + ch * 32, dr);
+          tmem_ld_wait();
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 p = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                   sc2, nl2);
+            x[e] = p.x;
+            x[e + 1] = p.y;
+          }
+          if (need_mask) {
+            const int kv = kmax - (jt * T + half * H + ch * 32);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = neg_inf_if_gt(x[e], e, kv);
+          }
+          uint32_t sw[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            // P is rounded to bf16 as in the forward's P V product and in bwd_dkdv.
+            const uint32_t pw = attn::pack_bf16x2(ex2(x[e]), ex2(x[e + 1]));
+            const float2 xd = fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                    nd2);
+            const float2 ds2 = ffma2(make_float2(attn::bf16_lo(pw), attn::bf16_hi(pw)), xd, zero2);
+            sw[e >> 1] = attn::pack_bf16x2(ds2.x, ds2.y);
+          }
+          tmem_st16(dp_addr + ch * 16, sw);
         }
-        // Over dP columns this thread has already read (half 1 lands on
-        // half 0's dP columns).
-        tmem_st32(tmem + lane_off + C::DP_COL + hh * (H / 2), sw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bb.ds_ready[hh]);
+        if (lane == 0) mbar_arrive(bb.ds_ready);
       }
+      if (!ok) break;
+      if (half == 0) {
+        // Group 0 writes dQ row qrow (all D columns).
+        ok = __all_sync(FULL, wait(bb.acc_done, k));
+        if (!ok) break;
+        tc_fence_after();
+        const bool live = qrow < Lq;
+        const size_t out_row = (static_cast<size_t>(w.bhq) * Lq + (live ? qrow : 0)) * D;
+        store_cols_bf16<D / 32>(tmem + lane_off + C::ACC0_COL, scale, dq + out_row, live);
+        tc_fence_before();
+      }
+      w = nxt;
+      got = got_next;
     }
-    if (ok) ok = __all_sync(FULL, wait(bb.acc_done, 0));
-    if (ok) {
-      tc_fence_after();
-      const size_t out_row = (static_cast<size_t>(bhq) * Lq + (live ? qrow : 0)) * D;
-      store_row_bf16<D>(tmem + lane_off + C::ACC0_COL, scale, dq + out_row, live);
-    } else {
+    if (!ok) {
       if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
       *bb.abort_flag = 1;
     }
@@ -779,14 +1049,20 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   if ((rows + 7) / 8 > 0x7fffffffLL || dq_ctas > 0x7fffffffLL || dkdv_ctas > 0x7fffffffLL)
     return ATTN_ERR_UNSUPPORTED;
   int* status = attn_host::device_status_ptr();
+  // The two work counters follow D in the workspace (at the next 256-byte boundary).
+  int* work = reinterpret_cast<int*>(reinterpret_cast<char*>(dd) +
+                                     ((static_cast<size_t>(rows) * sizeof(float) + 255) & ~size_t{255}));
+  const long long sms = attn_host::num_sms();
+  if (sms <= 0) return ATTN_ERR_CUDA;
   bwd_rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), dd, rows, D);
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>(dkdv_ctas), THREADS, L::BYTES, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), dd, rows, D,
+      work);
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>(std::min(dkdv_ctas, sms)), THREADS, L::BYTES, stream>>>(
       mq, mk, mv, mdo, lse, dd, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-      B, Hq, Hkv, Lq, Lk, causal, scale, status);
-  bwd_dq_kernel<D><<<static_cast<unsigned>(dq_ctas), THREADS, L::BYTES, stream>>>(
+      B, Hq, Hkv, Lq, Lk, causal, scale, work, status);
+  bwd_dq_kernel<D><<<static_cast<unsigned>(std::min(dq_ctas, sms)), THREADS, L::BYTES, stream>>>(
       mq, mk, mv, mdo, lse, dd, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv, Lq, Lk, causal,
-      scale, status);
+      scale, work, status);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

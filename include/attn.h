@@ -293,7 +293,10 @@ attn_status_t attn_decode_paged_balanced(const void* q, const void* k_pages, con
  *   q, o, d_o, dq  [B, Hq, Lq, d] bf16     k, v, dk, dv  [B, Hkv, Lk, d] bf16
  *   lse            [B, Hq, Lq] fp32 (natural log, as attn_fwd writes it)
  *   workspace      attn_bwd_workspace_bytes(B, Hq, Lq) bytes, 256-byte
- *                  aligned (holds D); device memory owned by the caller.
+ *                  aligned (holds D and the kernels' work counters, which
+ *                  the call resets); device memory owned by the caller.
+ *                  Calls that may run at the same time need separate
+ *                  workspaces.
  *   causal requires Lq == Lk (square rule, as attn_fwd).
  * d in {64, 128}, bf16 only.  Errors: ATTN_ERR_INVALID_ARG for NULLs, bad
  * sizes or misalignment; ATTN_ERR_UNSUPPORTED for other d or dtypes or

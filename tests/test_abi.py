@@ -287,7 +287,7 @@ def bwd(**kw):
 
 
 def test_bwd_rejects_on_host():
-    assert ea.lib().attn_bwd_workspace_bytes(2, 4, 100) == 3328   # 800 floats -> 256-byte multiple
+    assert ea.lib().attn_bwd_workspace_bytes(2, 4, 100) == 3584   # 800 floats -> 256-byte multiple, + counters
     assert bwd(q=None) == 1
     assert bwd(dv=None) == 1
     assert bwd(Hkv=3) == 1
