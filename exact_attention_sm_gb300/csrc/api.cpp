@@ -431,8 +431,10 @@ attn_status_t attn_decode_paged_balanced(const void* q, const void* k_pages, con
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Lq) {
   if (B <= 0 || Hq <= 0 || Lq <= 0) return 0;
-  // D (one float per query row), then the kernels' two work counters.
-  return round_up(static_cast<size_t>(B) * Hq * Lq * sizeof(float), kAlign) + kAlign;
+  // -LSE log2e and -D (one float per query row, rows padded to whole
+  // 128-row tiles), then the kernels' two work counters.
+  const size_t rows_pad = static_cast<size_t>(B) * Hq * ((static_cast<size_t>(Lq) + 127) / 128) * 128;
+  return 2 * round_up(rows_pad * sizeof(float), kAlign) + kAlign;
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,

@@ -10,7 +10,8 @@
 //
 // Three kernels, no atomics (every gradient element is written by exactly
 // one CTA, sums run in a fixed order, so results are bitwise reproducible):
-//   bwd_rowdot_kernel   D = rowsum(dO * O) per query row (fp32).
+//   bwd_rowdot_kernel   D = rowsum(dO * O) per query row (fp32), written as
+//                       -D next to -LSE log2e, both padded to whole Q tiles.
 //   bwd_dkdv_kernel     work item (request, KV head, key tile j): K_j, V_j
 //                       stay in shared memory while the Q tiles of every
 //                       query head of the group stream past; per Q tile four
@@ -140,15 +141,29 @@ __device__ __forceinline__ void mma_tmem_a_half(uint32_t d_tmem, uint32_t a_tmem
 
 // D = rowsum(dO * O) for every query row: one warp per row, fp32 sums of the
 // bf16 products in a fixed lane order.
-// Block 0 also zeroes the two work counters of the MMA kernels that follow
-// on the same stream.
+// One warp per query row of the padded [B Hq][nq 128] layout: nd = -D and
+// nl = -LSE log2e (-inf where the row does not exist or sees no key, so that
+// P = 0; nd = 0 there).  Block 0 also zeroes the two work counters of the MMA
+// kernels that follow on the same stream.
 __global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
-                                  const __nv_bfloat16* __restrict__ d_o, float* __restrict__ dd,
-                                  long long rows, int d, int* work) {
+                                  const __nv_bfloat16* __restrict__ d_o,
+                                  const float* __restrict__ lse, float* __restrict__ nl,
+                                  float* __restrict__ nd, long long heads, int Lq, int Lq_pad,
+                                  int d, int* work) {
   if (blockIdx.x == 0 && threadIdx.x < 2) work[threadIdx.x] = 0;
-  const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long long rp = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+  if (rp >= heads * Lq_pad) return;
+  const long long h = rp / Lq_pad;
+  const int row = static_cast<int>(rp - h * Lq_pad);
+  if (row >= Lq) {
+    if (lane == 0) {
+      nl[rp] = -INFINITY;
+      nd[rp] = 0.f;
+    }
+    return;
+  }
+  const long long r = h * Lq + row;
   const uint32_t* op = reinterpret_cast<const uint32_t*>(o + r * d);
   const uint32_t* gp = reinterpret_cast<const uint32_t*>(d_o + r * d);
   float acc = 0.f;
@@ -159,7 +174,11 @@ __global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(FULL, acc, off);
-  if (lane == 0) dd[r] = acc;
+  if (lane == 0) {
+    const float x = lse[r];
+    nl[rp] = x == -INFINITY ? -INFINITY : -x * attn::kLog2e;
+    nd[rp] = -acc;
+  }
 }
 
 }  // namespace
@@ -169,8 +188,8 @@ namespace {
 // holds two operand tiles for a whole work item (K, V in bwd_dkdv; Q, dO in
 // bwd_dq) in NF slots, so the next item's pair loads during this one at
 // d = 64, and streams the other two (Q, dO; K, V) through an NS-stage ring
-// deep enough to cover the load latency.  Then two stages of 128 fp32
-// per-query values (LSE and D, bwd_dkdv), the item ring, the barriers.
+// deep enough to cover the load latency.  Then the ring's per-query values
+// (-LSE log2e and -D of the Q tile, bwd_dkdv), the item ring, the barriers.
 // Two producer threads load the tiles, one the first and one the second
 // tile of every pair: the copies one thread issues complete one after
 // another (about 24 bytes per clock from L2), so one thread alone would not
@@ -182,8 +201,8 @@ struct BwdSmem {
   static constexpr int NF = D == 64 ? 2 : 1;
   static constexpr int NS = D == 64 ? 4 : 2;
   static constexpr int TILES = 2 * NF + 2 * NS;
-  static constexpr int OFF_VEC = TILES * C::TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_VEC + 4 * T * 4;
+  static constexpr int OFF_VEC = TILES * C::TILE_BYTES;  // [NS][-LSE log2e | -D][128] fp32
+  static constexpr int OFF_BAR = OFF_VEC + NS * 2 * T * 4;
   static constexpr int BYTES = OFF_BAR + 512 + 1024;  // barriers, item ring, alignment slack
 };
 static_assert(BwdSmem<64>::BYTES <= 227 * 1024 && BwdSmem<128>::BYTES <= 227 * 1024,
@@ -202,7 +221,6 @@ struct BwdBars {
   uint64_t* ds_ready;     // dS (dS^T) written
   uint64_t* acc_done;     // the item's accumulators are final
   uint64_t* drain;
-  uint64_t* vec_full;     // [2] per-query values staged by the elementwise warps
   uint64_t* item_full;    // [kItemRing] item id published
   int* items;             // [kItemRing]
   uint32_t* tmem_slot;
@@ -222,7 +240,6 @@ __device__ __forceinline__ BwdBars carve_bars(uint8_t* base) {
   r.ds_ready = b + 17;
   r.acc_done = b + 18;
   r.drain = b + 19;
-  r.vec_full = b + 20;
   r.item_full = b + 22;
   r.items = reinterpret_cast<int*>(b + 22 + kItemRing);
   r.tmem_slot = reinterpret_cast<uint32_t*>(r.items + kItemRing);
@@ -250,7 +267,6 @@ __device__ __forceinline__ bool bwd_prologue(const BwdBars& bb, int* status) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bb.s_full[s], 1);
       mbar_init(&bb.p_ready[s], 8);   // one arrival per elementwise warp
-      mbar_init(&bb.vec_full[s], 8);
     }
     mbar_init(bb.dp_full, 1);
     mbar_init(bb.ds_ready, 8);
@@ -394,8 +410,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
-                    const float* __restrict__ dd, __nv_bfloat16* __restrict__ dk,
+                    const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ nlse,
+                    const float* __restrict__ nd, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int B, int Hq, int Hkv, int Lq, int Lk,
                     int causal, float scale, int* work, int* status) {
   using C = BwdCfg<D>;
@@ -411,12 +427,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const uint32_t sbase = smem_u32(smem);
   const BwdBars bb = carve_bars(smem + L::OFF_BAR);
-  float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);  // [2 stages][-LSE*log2e | -D][128]
+  float* vec = reinterpret_cast<float*>(smem + L::OFF_VEC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (Lk + T - 1) / T, nq = (Lq + T - 1) / T;
   const int num_items = nk * B * Hkv;
   const int g = Hq / Hkv;
+  const int Lq_pad = nq * T;
   if (!bwd_prologue<NF, NS>(bb, status)) return;
   const uint32_t tmem = *bb.tmem_slot;
   // Tiles: K, V of held slot f at 2f, 2f + 1; Q, dO of ring stage s at
@@ -477,10 +494,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int bhq = w.b * Hq + w.hk * g + n / w.per_head;
           const int i = w.i0 + n % w.per_head;
           uint64_t* rb = &bb.ring_full[st];
-          if (role == 0) mbar_arrive_expect_tx(rb, 2 * C::TILE_BYTES);
+          if (role == 0) mbar_arrive_expect_tx(rb, 2 * C::TILE_BYTES + 2 * T * 4);
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(tile(2 * NF + 2 * st + role) + kb * C::BLOCK_BYTES, role ? &tm_do : &tm_q, rb,
                         kb * 64, i * T, bhq);
+          // The Q tile's -LSE log2e (producer 0) or -D (producer 1).
+          bulk_load(vec + (2 * st + role) * T, (role ? nd : nlse) + static_cast<size_t>(bhq) * Lq_pad + i * T,
+                    T * 4, rb);
         }
         if (!ok) { ++k; break; }
       }
@@ -585,48 +605,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int c = quad * 32 + lane;               // key row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float scale_log2 = scale * attn::kLog2e;
-    // Per-query values of iteration n of item w for query column c, negated
-    // for the packed FMAs: group 0 stages -LSE in the log2 domain (-inf
-    // where the query row does not exist or sees no key, so that P = 0),
-    // group 1 -D.
-    auto fetch = [&](const KvItem& w, int n) -> float {
-      const int bhq = w.b * Hq + w.hk * g + n / w.per_head;
-      const int row = (w.i0 + n % w.per_head) * T + c;
-      if (row >= Lq) return half == 0 ? -INFINITY : 0.f;
-      const size_t at = static_cast<size_t>(bhq) * Lq + row;
-      if (half != 0) return -dd[at];
-      const float x = lse[at];
-      return x == -INFINITY ? -INFINITY : -x * attn::kLog2e;
-    };
     KvItem w, nxt;
     int got = __shfl_sync(FULL, read_item(0, w), 0);
     bool ok = got >= 0;
-    float pre = got > 0 ? fetch(w, 0) : 0.f;
     int it = 0;
     for (int k = 0; ok && got > 0; ++k) {
       int got_next = 0;
+      int i = w.i0;                                // iteration n's Q tile
       for (int n = 0; n < w.n_iter; ++n, ++it) {
         const int st = it & 1;
-        float* l2s = vec + st * 2 * T;
-        float* ds_ = l2s + T;
-        // Every warp writes its 32 values, then waits for the other seven
-        // (an mbarrier, so the wait stays bounded).  A warp's arrival for
-        // it follows its last read of stage it - 1, so once all eight have
-        // arrived for it, stage (it + 1) & 1 may be overwritten.
-        (half == 0 ? l2s : ds_)[c] = pre;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bb.vec_full[st]);
-        ok = __all_sync(FULL, wait(&bb.vec_full[st], it >> 1));
+        // The Q tile's -LSE log2e and -D came with it into ring stage it % NS.
+        ok = __all_sync(FULL, wait(&bb.ring_full[it % NS], it / NS));
         if (!ok) break;
-        if (n + 1 < w.n_iter) {
-          pre = fetch(w, n + 1);
-        } else {                                   // the next item's first values
-          got_next = read_item(k + 1, nxt);
-          ok = __all_sync(FULL, got_next >= 0);
-          if (!ok) break;
-          pre = got_next > 0 ? fetch(nxt, 0) : 0.f;
-        }
-        const int i = w.i0 + n % w.per_head;
+        const float* l2s = vec + (it % NS) * 2 * T;
+        const float* ds_ = l2s + T;
         // P^T row c over this group's query half: P[r] = 2^(S^T[c][r] scale
         // log2e - LSE_r log2e), 0 for queries before key c on the diagonal
         // tile; bf16 pairs over the half's first 32 S^T columns.
@@ -669,6 +661,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bb.p_ready[st]);
+        if (++i == nq) i = w.i0;
+        if (n + 1 == w.n_iter) {                   // the next item, while dP^T is computed
+          got_next = read_item(k + 1, nxt);
+          ok = __all_sync(FULL, got_next >= 0);
+          if (!ok) break;
+        }
         // dS^T row c: dS[r] = P[r] (dP^T[c][r] - D_r), with P as handed to
         // the MMA, over the half's first 32 dP^T columns (already read).
         ok = __all_sync(FULL, wait(bb.dp_full, it));
@@ -737,8 +735,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse,
-                  const float* __restrict__ dd, __nv_bfloat16* __restrict__ dq, int B, int Hq,
+                  const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ nlse,
+                  const float* __restrict__ nd, __nv_bfloat16* __restrict__ dq, int B, int Hq,
                   int Hkv, int Lq, int Lk, int causal, float scale, int* work, int* status) {
   using C = BwdCfg<D>;
   using L = BwdSmem<D>;
@@ -755,6 +753,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (Lk + T - 1) / T, nq = (Lq + T - 1) / T;
   const int num_items = nq * B * Hq;
+  const int Lq_pad = nq * T;
   if (!bwd_prologue<NF, NS>(bb, status)) return;
   const uint32_t tmem = *bb.tmem_slot;
   // Tiles: Q, dO of held slot f at 2f, 2f + 1; K, V of ring stage s at
@@ -904,21 +903,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float2 zero2 = make_float2(0.f, 0.f);
     // -LSE log2e (-inf where the row does not exist or sees no key: P = 0)
     // and -D of this thread's query row in item w.
-    auto fetch = [&](const QItem& w, float& nl, float& nd) {
-      const int qrow = w.i * T + r;
-      nl = -INFINITY;
-      nd = 0.f;
-      if (qrow < Lq) {
-        const float x = lse[static_cast<size_t>(w.bhq) * Lq + qrow];
-        if (x != -INFINITY) nl = -x * attn::kLog2e;
-        nd = -dd[static_cast<size_t>(w.bhq) * Lq + qrow];
-      }
+    // -LSE log2e and -D of this thread's query row in item w (padded
+    // layout: rows past Lq hold -inf and 0).  The next item's values are
+    // loaded in this item's last iteration, which hides their latency.
+    float pre_l = 0.f, pre_d = 0.f;
+    auto fetch = [&](const QItem& w) {
+      const size_t at = static_cast<size_t>(w.bhq) * Lq_pad + w.i * T + r;
+      pre_l = nlse[at];
+      pre_d = nd[at];
     };
     QItem w, nxt;
     int got = __shfl_sync(FULL, read_item(0, w), 0);
     bool ok = got >= 0;
-    float pre_l = 0.f, pre_d = 0.f;
-    if (got > 0) fetch(w, pre_l, pre_d);
+    if (got > 0) fetch(w);
     int it = 0;
     for (int k = 0; ok && got > 0; ++k) {
       const float2 nl2 = make_float2(pre_l, pre_l), nd2 = make_float2(pre_d, pre_d);
@@ -932,7 +929,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           got_next = read_item(k + 1, nxt);
           ok = __all_sync(FULL, got_next >= 0);
           if (!ok) break;
-          if (got_next > 0) fetch(nxt, pre_l, pre_d);
+          if (got_next > 0) fetch(nxt);
         }
         const bool need_mask = (causal && jt == w.i) || (jt + 1) * T > Lk;
         ok = __all_sync(FULL, wait(&bb.s_full[it & 1], it >> 1)) &&
@@ -1043,25 +1040,30 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   if (!make_map_rows(&mq, q, D, Lq, B * Hq) || !make_map_rows(&mk, k, D, Lk, B * Hkv) ||
       !make_map_rows(&mv, v, D, Lk, B * Hkv) || !make_map_rows(&mdo, d_o, D, Lq, B * Hq))
     return ATTN_ERR_CUDA;
-  const long long rows = static_cast<long long>(B) * Hq * Lq;
   const long long nq = (Lq + T - 1) / T, nk = (Lk + T - 1) / T;
   const long long dq_ctas = nq * B * Hq, dkdv_ctas = nk * B * Hkv;
-  if ((rows + 7) / 8 > 0x7fffffffLL || dq_ctas > 0x7fffffffLL || dkdv_ctas > 0x7fffffffLL)
+  if (static_cast<long long>(B) * Hq * nq * T / 8 > 0x7fffffffLL || nq * T > 0x7fffffffLL ||
+      dq_ctas > 0x7fffffffLL || dkdv_ctas > 0x7fffffffLL)
     return ATTN_ERR_UNSUPPORTED;
   int* status = attn_host::device_status_ptr();
-  // The two work counters follow D in the workspace (at the next 256-byte boundary).
-  int* work = reinterpret_cast<int*>(reinterpret_cast<char*>(dd) +
-                                     ((static_cast<size_t>(rows) * sizeof(float) + 255) & ~size_t{255}));
+  // Workspace: -LSE log2e and -D in the padded [B Hq][nq 128] layout, then
+  // the two work counters (each part at a 256-byte boundary).
+  const size_t part = (static_cast<size_t>(B) * Hq * nq * T * sizeof(float) + 255) & ~size_t{255};
+  float* nlse = dd;
+  float* nd = reinterpret_cast<float*>(reinterpret_cast<char*>(dd) + part);
+  int* work = reinterpret_cast<int*>(reinterpret_cast<char*>(dd) + 2 * part);
   const long long sms = attn_host::num_sms();
   if (sms <= 0) return ATTN_ERR_CUDA;
-  bwd_rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), dd, rows, D,
-      work);
+  const long long heads = static_cast<long long>(B) * Hq;
+  const long long rows_pad = heads * nq * T;
+  bwd_rowdot_kernel<<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, nlse, nd,
+      heads, Lq, static_cast<int>(nq * T), D, work);
   bwd_dkdv_kernel<D><<<static_cast<unsigned>(std::min(dkdv_ctas, sms)), THREADS, L::BYTES, stream>>>(
-      mq, mk, mv, mdo, lse, dd, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+      mq, mk, mv, mdo, nlse, nd, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
       B, Hq, Hkv, Lq, Lk, causal, scale, work, status);
   bwd_dq_kernel<D><<<static_cast<unsigned>(std::min(dq_ctas, sms)), THREADS, L::BYTES, stream>>>(
-      mq, mk, mv, mdo, lse, dd, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv, Lq, Lk, causal,
+      mq, mk, mv, mdo, nlse, nd, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv, Lq, Lk, causal,
       scale, work, status);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

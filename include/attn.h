@@ -293,8 +293,9 @@ attn_status_t attn_decode_paged_balanced(const void* q, const void* k_pages, con
  *   q, o, d_o, dq  [B, Hq, Lq, d] bf16     k, v, dk, dv  [B, Hkv, Lk, d] bf16
  *   lse            [B, Hq, Lq] fp32 (natural log, as attn_fwd writes it)
  *   workspace      attn_bwd_workspace_bytes(B, Hq, Lq) bytes, 256-byte
- *                  aligned (holds D and the kernels' work counters, which
- *                  the call resets); device memory owned by the caller.
+ *                  aligned (holds -LSE log2e and -D per query row, padded to
+ *                  128-row tiles, and the kernels' work counters, which the
+ *                  call resets); device memory owned by the caller.
  *                  Calls that may run at the same time need separate
  *                  workspaces.
  *   causal requires Lq == Lk (square rule, as attn_fwd).

@@ -287,7 +287,7 @@ def bwd(**kw):
 
 
 def test_bwd_rejects_on_host():
-    assert ea.lib().attn_bwd_workspace_bytes(2, 4, 100) == 3584   # 800 floats -> 256-byte multiple, + counters
+    assert ea.lib().attn_bwd_workspace_bytes(2, 4, 100) == 8448   # 2 x 8 heads x 128 padded rows x 4 B, + counters
     assert bwd(q=None) == 1
     assert bwd(dv=None) == 1
     assert bwd(Hkv=3) == 1
