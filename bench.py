@@ -178,7 +178,9 @@ def source_sha(files):
 KERNEL_SOURCES = {"prefill": ["prefill_sm103.cu", "sm103_ptx.cuh", "common.cuh"],
                   "prefill_f32": ["prefill_f32.cu", "common.cuh"],
                   "decode": ["decode_paged.cu", "sm103_ptx.cuh", "tma_host.h", "common.cuh"],
-                  "backward": ["backward_sm103.cu", "sm103_ptx.cuh", "tma_host.h", "common.cuh"]}
+                  "backward": ["backward_sm103.cu", "sm103_ptx.cuh", "tma_host.h", "common.cuh"],
+                  "cascade": ["cascade.cu", "prefill_sm103.cu", "decode_paged.cu", "sm103_ptx.cuh",
+                              "tma_host.h", "common.cuh"]}
 
 
 def traffic_for(workload, kind):
@@ -488,7 +490,7 @@ def measure(name, torch, ea, inputs, steps, warmup, flush, peaks, peak_src):
         unit = "GB/s"
         roof = {"bound": "hbm", "achieved": value, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "peak_source": f"hbm_gbs of {peak_src}"}
-        tkind = "decode"
+        tkind = "cascade" if w["kind"] == "cascade" else "decode"
     roof["frac"] = roof["achieved"] / roof["peak"]
     if roof["bound"] in ("tensor", "hbm"):
         roof["datasheet"] = {"peak": DATASHEET[roof["unit"]],
