@@ -497,7 +497,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
     return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (d != 128 || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || page_size != 16) return ATTN_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return ATTN_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -1,4 +1,4 @@
-// Paged grouped-query decode attention, bf16, head dim 128.
+// Paged grouped-query decode attention, bf16, head dim 128 or 64.
 //
 // Follows "FlashAttention and inference operators" (CUDA advanced handbook):
 // "PagedAttention" (token t lives in page block_table[t / 16], slot t % 16),
@@ -19,7 +19,9 @@
 //     device status word and its page is treated as empty (never read).
 //   * consumers: page i of the segment goes to consumer warp i % 4.  Inside a
 //     warp, 4 groups of 8 lanes each take one token at a time and lane l (of
-//     8) owns dims [16l, 16l+16): two 16-byte shared loads per row.  Scores
+//     8) owns dims [l d/8, (l+1) d/8): two 16-byte shared loads per row at
+//     d = 128, one at d = 64 (whose ring has twice the stages, so the same
+//     64 KB per CTA are in flight).  Scores
 //     use the mixed-precision FMA (bf16 x bf16 + fp32), so neither q nor K is
 //     converted; the 4 tokens x HG heads partial dot products of a group are
 //     reduced over its 8 lanes with a transposed butterfly (each step halves
@@ -44,7 +46,7 @@ namespace {
 
 using namespace sm103;
 
-constexpr int D = 128;
+constexpr int D = 128;                      // the balanced kernel's head dim
 constexpr int PAGE = 16;
 constexpr int NCW = 4;                      // consumer warps
 constexpr int HG = 4;                       // query heads per CTA (padded when the group is smaller)
@@ -53,6 +55,21 @@ constexpr int NST = 8;                      // ring stages (one page of K and V 
 constexpr int PAGE_BYTES = PAGE * D * 2;    // 4 KB: 16 rows of one KV head
 constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
 constexpr int SMEM_BYTES = NST * STAGE_BYTES + 1024;
+
+// Head-dim dependent sizes of the plain decode kernel: DL dims per lane
+// (two or one 16-byte loads of a row), ring stages so that 64 KB are in
+// flight per CTA whatever d is.
+template <int DD>
+struct DecCfg {
+  static constexpr int DL = DD / 8;
+  static constexpr int WPL = DL / 2;                    // bf16 pairs per lane and row
+  static constexpr int PAGE_BYTES = PAGE * DD * 2;
+  static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
+  static constexpr int NST = 8 * 128 / DD;
+  static constexpr int SMEM_BYTES = NST * STAGE_BYTES + 1024;
+};
+static_assert(DecCfg<128>::SMEM_BYTES == SMEM_BYTES && DecCfg<64>::SMEM_BYTES == SMEM_BYTES,
+              "the same ring bytes at both head dims");
 constexpr unsigned FULL = 0xffffffffu;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;
@@ -107,24 +124,33 @@ struct SegMap {
 // One page of K and V (16 tokens, the first `valid` of them live) against
 // the query rows in qw: scores, online softmax in base 2 and P V into the
 // lane's accumulators (lane layout as described at the top of the file).
+template <int DD>
 __device__ __forceinline__ void consume_page(const uint8_t* kst, const uint8_t* vst, int valid,
-                                             const uint32_t (&qw)[HG][8], float (&acc)[HG][16],
-                                             float (&m_run)[HG], float& l_own, float scale_log2,
-                                             int lane, int grp, int l8, int own_h) {
+                                             const uint32_t (&qw)[HG][DecCfg<DD>::WPL],
+                                             float (&acc)[HG][DecCfg<DD>::DL], float (&m_run)[HG],
+                                             float& l_own, float scale_log2, int lane, int grp,
+                                             int l8, int own_h) {
+    constexpr int WPL = DecCfg<DD>::WPL, DL = DecCfg<DD>::DL, RS = DD * 2;  // RS: row bytes
 
-    // Partial dots of this lane's 16 dims: value index x = h * 4 + tt.
+    // Partial dots of this lane's DL dims: value index x = h * 4 + tt.
     float part[HG * 4];
 #pragma unroll
     for (int tt = 0; tt < 4; ++tt) {
       const int slot = grp + 4 * tt;
-      const uint4 k0 = *reinterpret_cast<const uint4*>(kst + slot * 256);
-      const uint4 k1 = *reinterpret_cast<const uint4*>(kst + slot * 256 + 16);
-      const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+      uint32_t kw[WPL];
+#pragma unroll
+      for (int c = 0; c < WPL / 4; ++c) {
+        const uint4 k4 = *reinterpret_cast<const uint4*>(kst + slot * RS + 16 * c);
+        kw[4 * c] = k4.x;
+        kw[4 * c + 1] = k4.y;
+        kw[4 * c + 2] = k4.z;
+        kw[4 * c + 3] = k4.w;
+      }
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < WPL; ++w) {
           a0 = fma_bf16_lo(qw[h][w], kw[w], a0);
           a1 = fma_bf16_hi(qw[h][w], kw[w], a1);
         }
@@ -167,7 +193,7 @@ __device__ __forceinline__ void consume_page(const uint8_t* kst, const uint8_t* 
       if (pm > m_run[h] + kRescaleThreshold) {  // warp-uniform
         const float alpha = ex2(m_run[h] - pm);  // 0 on the first page (m_run = -inf)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[h][j] *= alpha;
+        for (int j = 0; j < DL; ++j) acc[h][j] *= alpha;
         if (h == own_h) l_own *= alpha;
         m_run[h] = pm;
       }
@@ -186,17 +212,20 @@ __device__ __forceinline__ void consume_page(const uint8_t* kst, const uint8_t* 
       for (int e = 0; e < 2; ++e) {
         const int tt = 2 * tp + e;
         const int slot = grp + 4 * tt;
-        uint4 v0 = *reinterpret_cast<const uint4*>(vst + slot * 256);
-        uint4 v1 = *reinterpret_cast<const uint4*>(vst + slot * 256 + 16);
-        if (slot >= valid) {  // rows past the segment may hold anything
-          v0 = make_uint4(0u, 0u, 0u, 0u);
-          v1 = v0;
+        uint32_t vw[WPL];
+#pragma unroll
+        for (int c = 0; c < WPL / 4; ++c) {
+          uint4 v4 = *reinterpret_cast<const uint4*>(vst + slot * RS + 16 * c);
+          if (slot >= valid) v4 = make_uint4(0u, 0u, 0u, 0u);  // rows past the segment may hold anything
+          vw[4 * c] = v4.x;
+          vw[4 * c + 1] = v4.y;
+          vw[4 * c + 2] = v4.z;
+          vw[4 * c + 3] = v4.w;
         }
-        const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
         for (int h = 0; h < HG; ++h)
 #pragma unroll
-          for (int w = 0; w < 8; ++w) {
+          for (int w = 0; w < WPL; ++w) {
             if (e == 0) fma_plo_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
             else fma_phi_v(ph[h], vw[w], acc[h][2 * w], acc[h][2 * w + 1]);
           }
@@ -204,6 +233,7 @@ __device__ __forceinline__ void consume_page(const uint8_t* kst, const uint8_t* 
     }
 }
 
+template <int DD>
 __global__ void __launch_bounds__(NUM_THREADS, 3)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -213,6 +243,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
                        float* __restrict__ part_o, float* __restrict__ part_lse, int Hq, int Hkv,
                        int max_pages, int num_pages, float scale_log2, int* status,
                        const __grid_constant__ SegMap map) {
+  using DC = DecCfg<DD>;
+  constexpr int NST = DC::NST, STAGE_BYTES = DC::STAGE_BYTES, PAGE_BYTES = DC::PAGE_BYTES;
+  constexpr int DL = DC::DL, WPL = DC::WPL;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -220,7 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
   __shared__ int skip[NST];
   __shared__ float sm_m[NCW][HG];
   __shared__ float sm_l[NCW][HG];
-  __shared__ __align__(16) float sm_acc[NCW][HG][D];
+  __shared__ __align__(16) float sm_acc[NCW][HG][DD];
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
 
@@ -314,24 +347,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
     // ------------------------------------------------------------ consumers
     const int cw = warp - 1;
     const int grp = lane >> 3;       // token group within the warp
-    const int l8 = lane & 7;         // owns dims [16 l8, 16 l8 + 16)
+    const int l8 = lane & 7;         // owns dims [DL l8, DL l8 + DL)
     const int own_h = l8 >> 1;       // head of the values this lane holds after the reduction
-    uint32_t qw[HG][8];
+    uint32_t qw[HG][WPL];
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
       const int hq = h0 + min(h, nh - 1);  // padded heads reuse a real head's q
-      const uint4* qp = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq) * D + 16 * l8);
-      const uint4 a = qp[0], c = qp[1];
-      qw[h][0] = a.x; qw[h][1] = a.y; qw[h][2] = a.z; qw[h][3] = a.w;
-      qw[h][4] = c.x; qw[h][5] = c.y; qw[h][6] = c.z; qw[h][7] = c.w;
+      const uint4* qp =
+          reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq) * DD + DL * l8);
+#pragma unroll
+      for (int c = 0; c < WPL / 4; ++c) {
+        const uint4 a4 = qp[c];
+        qw[h][4 * c] = a4.x;
+        qw[h][4 * c + 1] = a4.y;
+        qw[h][4 * c + 2] = a4.z;
+        qw[h][4 * c + 3] = a4.w;
+      }
     }
-    float acc[HG][16];
+    float acc[HG][DL];
     float m_run[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
       m_run[h] = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[h][j] = 0.f;
+      for (int j = 0; j < DL; ++j) acc[h][j] = 0.f;
     }
     float l_own = 0.f;
     bool ok = true;
@@ -341,9 +380,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
       ok = __all_sync(FULL, mbar_wait(&full[st], (i / NST) & 1, abort_flag, kWaitLimitNs));
       if (!ok) break;
       if (!skip[st]) {
-        const uint8_t* kst = ring + st * STAGE_BYTES + l8 * 32;
-        consume_page(kst, kst + PAGE_BYTES, t_end - (p_begin + i) * PAGE, qw, acc, m_run, l_own,
-                     scale_log2, lane, grp, l8, own_h);
+        const uint8_t* kst = ring + st * STAGE_BYTES + l8 * (DL * 2);
+        consume_page<DD>(kst, kst + PAGE_BYTES, t_end - (p_begin + i) * PAGE, qw, acc, m_run,
+                         l_own, scale_log2, lane, grp, l8, own_h);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
@@ -357,7 +396,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
 #pragma unroll
     for (int h = 0; h < HG; ++h)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < DL; ++j) {
         acc[h][j] += __shfl_xor_sync(FULL, acc[h][j], 8);
         acc[h][j] += __shfl_xor_sync(FULL, acc[h][j], 16);
       }
@@ -373,19 +412,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
         sm_l[cw][h] = lh;
       }
       if (grp == 0) {
-        float4* dst = reinterpret_cast<float4*>(&sm_acc[cw][h][16 * l8]);
-        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
-        dst[2] = make_float4(acc[h][8], acc[h][9], acc[h][10], acc[h][11]);
-        dst[3] = make_float4(acc[h][12], acc[h][13], acc[h][14], acc[h][15]);
+        float4* dst = reinterpret_cast<float4*>(&sm_acc[cw][h][DL * l8]);
+#pragma unroll
+        for (int c = 0; c < DL / 4; ++c)
+          dst[c] = make_float4(acc[h][4 * c], acc[h][4 * c + 1], acc[h][4 * c + 2], acc[h][4 * c + 3]);
       }
     }
     named_barrier(1, NCW * 32);
 
-    const int t = threadIdx.x - 32;  // output dim
+    const int t = threadIdx.x - 32;  // output dim (threads past d idle)
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
-      if (h >= nh) break;
+      if (h >= nh || t >= DD) break;
       float big = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NCW; ++w) big = fmaxf(big, sm_m[w][h]);
@@ -403,17 +441,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
       const float row_lse = empty_row ? -INFINITY : (big + log2f(lw)) * attn::kLn2;
       const size_t r = static_cast<size_t>(b) * Hq + h0 + h;
       if (part_o == nullptr) {  // one split: the final output
-        o[r * D + t] = __float2bfloat16_rn(out);
+        o[r * DD + t] = __float2bfloat16_rn(out);
         if (t == 0 && lse != nullptr) lse[r] = row_lse;
       } else {
-        part_o[(r * max_splits + s) * D + t] = out;
+        part_o[(r * max_splits + s) * DD + t] = out;
         if (t == 0) part_lse[r * max_splits + s] = row_lse;
         // Compact grid: the request's last segment CTA also writes the empty
         // states (O = 0, LSE = -inf) of the slots past its segment count, so
         // the merge reads max_splits written states per row.
         if (s == n_segs - 1)
           for (int s2 = n_segs; s2 < max_splits; ++s2) {
-            part_o[(r * max_splits + s2) * D + t] = 0.f;
+            part_o[(r * max_splits + s2) * DD + t] = 0.f;
             if (t == 0) part_lse[r * max_splits + s2] = -INFINITY;
           }
       }
@@ -613,7 +651,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
         if (!ok) break;
         if (!skip[st]) {
           const uint8_t* kst = ring + st * STAGE_BYTES + l8 * 32;
-          consume_page(kst, kst + PAGE_BYTES, sg.t_end - (sg.p_begin + i) * PAGE, qw, acc, m_run,
+          consume_page<D>(kst, kst + PAGE_BYTES, sg.t_end - (sg.p_begin + i) * PAGE, qw, acc, m_run,
                        l_own, scale_log2, lane, grp_l, l8, own_h);
         }
         __syncwarp();
@@ -744,17 +782,17 @@ __global__ void __launch_bounds__(128)
   if (lane == 0 && lse != nullptr) lse[r] = empty ? -INFINITY : big + logf(wsum);
 }
 
-// k_pages / v_pages [num_pages, 16, Hkv, 128] bf16 as a 4-D tensor
-// {128, Hkv, 16, num_pages}; box {128, 1, 16, 1} = one page of one KV head.
-bool make_page_map(CUtensorMap* m, const void* base, int Hkv, int num_pages) {
+// k_pages / v_pages [num_pages, 16, Hkv, d] bf16 as a 4-D tensor
+// {d, Hkv, 16, num_pages}; box {d, 1, 16, 1} = one page of one KV head.
+bool make_page_map(CUtensorMap* m, const void* base, int Hkv, int num_pages, int dd = D) {
   attn_host::EncodeTiledFn enc = attn_host::encode_tiled_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(dd), static_cast<cuuint64_t>(Hkv),
                               static_cast<cuuint64_t>(PAGE), static_cast<cuuint64_t>(num_pages)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(Hkv) * D * 2,
-                                 static_cast<cuuint64_t>(PAGE) * Hkv * D * 2};
-  const cuuint32_t box[4] = {D, 1, PAGE, 1};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(dd) * 2,
+                                 static_cast<cuuint64_t>(Hkv) * dd * 2,
+                                 static_cast<cuuint64_t>(PAGE) * Hkv * dd * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(dd), 1, PAGE, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -766,7 +804,9 @@ bool set_smem_attr() {
   const int dev = attn_host::current_device_slot();
   if (dev < 0) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
       return false;
     done[dev] = true;
@@ -838,7 +878,7 @@ int decode_ctas_per_sm() {
   if (cached[dev] == 0) {
     int n = 0;
     if (!set_smem_attr() ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_bf16_kernel, NUM_THREADS,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_bf16_kernel<128>, NUM_THREADS,
                                                       SMEM_BYTES) != cudaSuccess ||
         n < 1)
       n = 1;
@@ -853,11 +893,12 @@ attn_status_t launch_decode_bf16(const void* q, const void* k_pages, const void*
                                  float* part_lse, int B, int Hq, int Hkv, int d, int max_pages,
                                  int num_pages, float scale, const int32_t* lens_host,
                                  cudaStream_t stream) {
-  if (d != D || page_size != PAGE) return ATTN_ERR_UNSUPPORTED;
+  if ((d != 128 && d != 64) || page_size != PAGE) return ATTN_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
   if (!set_smem_attr()) return ATTN_ERR_CUDA;
   CUtensorMap mk, mv;
-  if (!make_page_map(&mk, k_pages, Hkv, num_pages) || !make_page_map(&mv, v_pages, Hkv, num_pages))
+  if (!make_page_map(&mk, k_pages, Hkv, num_pages, d) ||
+      !make_page_map(&mv, v_pages, Hkv, num_pages, d))
     return ATTN_ERR_CUDA;
   const int groups = Hkv * ((group + HG - 1) / HG);
   dim3 grid(max_splits, groups, B);
@@ -875,7 +916,8 @@ attn_status_t launch_decode_bf16(const void* q, const void* k_pages, const void*
     }
     grid = dim3(map.off[B], groups, 1);
   }
-  decode_bf16_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+  auto kernel = d == 64 ? decode_bf16_kernel<64> : decode_bf16_kernel<128>;
+  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
       mk, mv, static_cast<const __nv_bfloat16*>(q), block_table, seq_lens, chunk, max_splits,
       static_cast<__nv_bfloat16*>(o), lse, part_o, part_lse, Hq, Hkv, max_pages, num_pages,
       scale * attn::kLog2e, device_status_ptr(), map);

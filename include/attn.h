@@ -144,7 +144,7 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int max_splits);
  *   o            [B, Hq, d] output, dtype;  lse [B, Hq] fp32 output or NULL
  *   workspace    device buffer of >= attn_decode_workspace_bytes(B, Hq, d, S)
  *                bytes for the plan's S (may be NULL when S == 1)
- *   d == 128 for bf16; d in {64, 128} for fp32 is not offered (bf16 only).
+ *   d in {64, 128} (bf16 only).
  */
 attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                                 const int32_t* block_table, const int32_t* seq_lens,

@@ -75,7 +75,8 @@ def test_decode_rejects_on_host():
     assert dec(Hkv=3) == 1
     assert dec(splits=-1) == 1
     assert dec(page=32) == 2
-    assert dec(d=64) == 2
+    assert dec(d=96) == 2
+    assert dec(d=64) == 3                 # d = 64 is served; here the split plan needs a workspace
     assert dec(dtype=ea.ATTN_F32) == 2
     assert dec(max_pages=2) == 1          # a length exceeds max_pages * page_size
     assert dec() == 3                     # 4 forced segments need a workspace
