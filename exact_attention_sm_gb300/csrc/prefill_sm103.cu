@@ -785,18 +785,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* kdst = smem + C::OFF_K + sk * C::TILE_BYTES;
           uint8_t* vdst = smem + C::OFF_V + st * C::TILE_BYTES;
           if (g >= NSK && !pwait(&k_empty[sk], phk)) return false;
-          if constexpr (kGather) {  // tile j of the item (the cursor's tile)
+          if constexpr (kGather) {  // tile j of the item (the cursor's tile); V: warp 3
             gather_tile<C::KB>(kdst, static_cast<const __nv_bfloat16*>(geo.k_raw), geo, gc, kv_c1,
                                Hkv, lane, status);
             retire.committed(&k_full[sk], lane);
-            if (g >= NS && !pwait(&v_empty[st], ph)) {
-              retire.flush(lane);  // K(j) lands before giving up
-              return false;
-            }
-            gather_tile<C::KB>(vdst, static_cast<const __nv_bfloat16*>(geo.v_raw), geo, gc, kv_c1,
-                               Hkv, lane, status);
-            retire.committed(&v_full[st], lane);
             gc.advance(lane);
+            (void)vdst;
+            (void)ph;
           } else if constexpr (kPaged) {
             int pg[PageCursor::NP];
             pages.take(pg, geo, status);  // tile j (tiles are issued in order)
@@ -854,9 +849,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (nq[x] > 0) mbar_wait(&q_full[x], (nq[x] - 1) & 1, &no_abort, kWaitLimitNs);
       for (int t = g > NSK ? g - NSK : 0; t < g; ++t)
         mbar_wait(&k_full[t % NSK], (t / NSK) & 1, &no_abort, kWaitLimitNs);
-      for (int t = g > NS ? g - NS : 0; t < g; ++t)
-        mbar_wait(&v_full[t % NS], (t / NS) & 1, &no_abort, kWaitLimitNs);
+      if constexpr (!kGather)
+        for (int t = g > NS ? g - NS : 0; t < g; ++t)
+          mbar_wait(&v_full[t % NS], (t / NS) & 1, &no_abort, kWaitLimitNs);
     }
+  } else if (kGather && warp == 3) {
+    // ------------------------------------------------------------ V gatherer
+    // Gathered layouts: this warp copies the V rows, warp 0 the K rows (one
+    // warp's 16-byte copies per tile are what limits a gathered stream).
+    GatherRetire retire;
+    auto pwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (__all_sync(FULL, mbar_test_wait(bar, parity))) return true;
+      retire.flush(lane);
+      return __all_sync(FULL, mbar_wait(bar, parity, abort_flag, kWaitLimitNs));
+    };
+    int g = 0;  // V tiles issued (ring position, as warp 0 counts K/V tiles)
+    bool ok = true;
+    for (int it = sched.first; ok && it < sched.last; it += sched.step) {
+      const Item w = item_of(it);
+      const int nmax = max(w.n[0], w.n[1]);
+      if (nmax == 0) continue;
+      const int kv_c1 = (w.bh % Hq) / group;
+      GatherCursor gc;
+      gc.begin(geo, w.bh / Hq, w.sq.lk, lane);
+      for (int j = 0; j < nmax; ++j, ++g) {
+        const int st = g % NS;
+        if (g >= NS && !pwait(&v_empty[st], ((g / NS) + 1) & 1)) {
+          ok = false;
+          break;
+        }
+        gather_tile<C::KB>(smem + C::OFF_V + st * C::TILE_BYTES,
+                           static_cast<const __nv_bfloat16*>(geo.v_raw), geo, gc, kv_c1, Hkv, lane,
+                           status);
+        retire.committed(&v_full[st], lane);
+        gc.advance(lane);
+      }
+    }
+    if (!ok && lane == 0) {
+      attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+    retire.flush(lane);
+    int no_abort = 0;
+    for (int t = g > NS ? g - NS : 0; t < g; ++t)
+      mbar_wait(&v_full[t % NS], (t / NS) & 1, &no_abort, kWaitLimitNs);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
