@@ -141,43 +141,60 @@ __device__ __forceinline__ void mma_tmem_a_half(uint32_t d_tmem, uint32_t a_tmem
 
 // D = rowsum(dO * O) for every query row: one warp per row, fp32 sums of the
 // bf16 products in a fixed lane order.
-// One warp per query row of the padded [B Hq][nq 128] layout: nd = -D and
-// nl = -LSE log2e (-inf where the row does not exist or sees no key, so that
-// P = 0; nd = 0 there).  Block 0 also zeroes the two work counters of the MMA
-// kernels that follow on the same stream.
-__global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
-                                  const __nv_bfloat16* __restrict__ d_o,
-                                  const float* __restrict__ lse, float* __restrict__ nl,
-                                  float* __restrict__ nd, long long heads, int Lq, int Lq_pad,
-                                  int d, int* work) {
+// D = rowsum(dO * O) for the rows of the padded [B Hq][nq 128] layout,
+// written as nd = -D next to nl = -LSE log2e (-inf where the row does not
+// exist or sees no key, so that P = 0; nd = 0 there).  A row is read by D / 8
+// lanes with one 16-byte load of O and one of dO each, so a warp covers
+// 32 / (D / 8) rows per pass and the loads are whole 128-byte lines; the
+// grid strides over the rows.  The sum runs in a fixed lane order.  Block 0
+// also zeroes the two work counters of the MMA kernels that follow on the
+// same stream.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ d_o,
+                      const float* __restrict__ lse, float* __restrict__ nl,
+                      float* __restrict__ nd, long long heads, int Lq, int Lq_pad, int* work) {
+  constexpr int G = D / 8;     // lanes per row
+  constexpr int RPW = 32 / G;  // rows per warp and pass
   if (blockIdx.x == 0 && threadIdx.x < 2) work[threadIdx.x] = 0;
-  const long long rp = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (rp >= heads * Lq_pad) return;
-  const long long h = rp / Lq_pad;
-  const int row = static_cast<int>(rp - h * Lq_pad);
-  if (row >= Lq) {
-    if (lane == 0) {
-      nl[rp] = -INFINITY;
-      nd[rp] = 0.f;
-    }
-    return;
-  }
-  const long long r = h * Lq + row;
-  const uint32_t* op = reinterpret_cast<const uint32_t*>(o + r * d);
-  const uint32_t* gp = reinterpret_cast<const uint32_t*>(d_o + r * d);
-  float acc = 0.f;
-  for (int c = lane; c < d / 2; c += 32) {
-    const uint32_t a = op[c], b = gp[c];
-    acc = fmaf(attn::bf16_lo(a), attn::bf16_lo(b), acc);
-    acc = fmaf(attn::bf16_hi(a), attn::bf16_hi(b), acc);
-  }
+  const int sub = lane / G, gl = lane % G;
+  const long long total = heads * Lq_pad;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long base = warp_id * RPW; base < total; base += nwarps * RPW) {
+    const long long rp = base + sub;
+    float acc = 0.f;
+    bool live = false;
+    long long r = 0;
+    if (rp < total) {
+      const long long h = rp / Lq_pad;
+      const int row = static_cast<int>(rp - h * Lq_pad);
+      live = row < Lq;
+      r = h * Lq + row;
+      if (live) {
+        const uint4 a = attn::ld_stream_v4(o + r * D + gl * 8);
+        const uint4 g = attn::ld_stream_v4(d_o + r * D + gl * 8);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, gv[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(FULL, acc, off);
-  if (lane == 0) {
-    const float x = lse[r];
-    nl[rp] = x == -INFINITY ? -INFINITY : -x * attn::kLog2e;
-    nd[rp] = -acc;
+        for (int c = 0; c < 4; ++c) {
+          acc = fmaf(attn::bf16_lo(av[c]), attn::bf16_lo(gv[c]), acc);
+          acc = fmaf(attn::bf16_hi(av[c]), attn::bf16_hi(gv[c]), acc);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(FULL, acc, off);
+    if (gl == 0 && rp < total) {
+      if (!live) {
+        nl[rp] = -INFINITY;
+        nd[rp] = 0.f;
+      } else {
+        const float x = lse[r];
+        nl[rp] = x == -INFINITY ? -INFINITY : -x * attn::kLog2e;
+        nd[rp] = -acc;
+      }
+    }
   }
 }
 
@@ -216,9 +233,9 @@ struct BwdBars {
   uint64_t* ring_full;    // [NS] a streamed pair has landed
   uint64_t* ring_empty;   // [NS] the products are done with it
   uint64_t* s_full;       // [2 S buffers]: S (S^T) is in TMEM
-  uint64_t* dp_full;      // dP (dP^T) is in TMEM
-  uint64_t* p_ready;      // [2 iteration parities]: P^T written (bwd_dkdv)
-  uint64_t* ds_ready;     // dS (dS^T) written
+  uint64_t* dp_full;      // [2 dP buffers]: dP (dP^T) is in TMEM
+  uint64_t* p_ready;      // [2 iteration parities]: P^T written (bwd_dkdv); [0]: S read (bwd_dq)
+  uint64_t* ds_ready;     // [2 iteration parities]: dS (dS^T) written
   uint64_t* acc_done;     // the item's accumulators are final
   uint64_t* drain;
   uint64_t* item_full;    // [kItemRing] item id published
@@ -236,10 +253,10 @@ __device__ __forceinline__ BwdBars carve_bars(uint8_t* base) {
   r.ring_empty = b + 8;
   r.s_full = b + 12;
   r.dp_full = b + 14;
-  r.p_ready = b + 15;
-  r.ds_ready = b + 17;
-  r.acc_done = b + 18;
-  r.drain = b + 19;
+  r.p_ready = b + 16;
+  r.ds_ready = b + 18;
+  r.acc_done = b + 20;
+  r.drain = b + 21;
   r.item_full = b + 22;
   r.items = reinterpret_cast<int*>(b + 22 + kItemRing);
   r.tmem_slot = reinterpret_cast<uint32_t*>(r.items + kItemRing);
@@ -266,10 +283,10 @@ __device__ __forceinline__ bool bwd_prologue(const BwdBars& bb, int* status) {
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bb.s_full[s], 1);
+      mbar_init(&bb.dp_full[s], 1);
       mbar_init(&bb.p_ready[s], 8);   // one arrival per elementwise warp
+      mbar_init(&bb.ds_ready[s], 8);
     }
-    mbar_init(bb.dp_full, 1);
-    mbar_init(bb.ds_ready, 8);
     for (int s = 0; s < kItemRing; ++s) mbar_init(&bb.item_full[s], 1);
     mbar_init(bb.acc_done, 1);
     mbar_init(bb.drain, 1);
@@ -540,7 +557,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         auto issue_dp = [&](int n) {
           const uint64_t do_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS) + 1), 16, 1024);
           mma_kmajor_full<D>(tmem + C::DP_COL, v_desc, do_k);
-          mma_commit(bb.dp_full);
+          mma_commit(&bb.dp_full[0]);
         };
         if (!wait(&bb.hold_full[f], k / NF) || !ring_wait(it)) {
           ok = false;
@@ -741,8 +758,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   using C = BwdCfg<D>;
   using L = BwdSmem<D>;
   constexpr int NF = L::NF, NS = L::NS;
-  // Two S buffers (the accumulator takes D columns from 256): S of the next
-  // K/V tile is computed while the elementwise warps work on this one.
+  // One S buffer and two dP buffers (TMEM columns 128 and 384; the
+  // accumulator takes D columns from 256).  The elementwise warps turn S
+  // into P first and signal (p_ready[0]), so S and dP of the next K/V tile
+  // are computed while they work on dS of this one.
   static_assert(C::ACC0_COL + D <= C::S1_COL, "TMEM columns");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -771,7 +790,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     w = q_item(x, nk, nq, B, Hq, Hkv, causal);
     return 1;
   };
-  auto s_col = [&](int it) -> uint32_t { return (it & 1) ? C::S1_COL : C::S_COL; };
+  auto dp_col = [&](int it) -> uint32_t { return (it & 1) ? C::S1_COL : C::DP_COL; };
+  uint64_t* s_read = &bb.p_ready[0];  // every elementwise warp has read S
 
   if (warp == 0 || warp == 2) {
     if (lane == 0) {
@@ -837,19 +857,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int f = k % NF;
         const uint64_t q_desc = smem_desc_sw128(taddr(2 * f), 16, 1024);
         const uint64_t do_desc = smem_desc_sw128(taddr(2 * f + 1), 16, 1024);
-        // S(it) = Q K^T (queries as rows, keys as columns).
+        // S(n) = Q K^T (queries as rows, keys as columns), once the warps
+        // have read S(n - 1).
         auto issue_s = [&](int n) {
           const uint64_t k_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS)), 16, 1024);
-          mma_kmajor_full<D>(tmem + s_col(n), q_desc, k_k);
-          mma_commit(&bb.s_full[n & 1]);
+          mma_kmajor_full<D>(tmem + C::S_COL, q_desc, k_k);
+          mma_commit(&bb.s_full[0]);
         };
-        // dP(it) = dO V^T.
+        // dP(n) = dO V^T into buffer n & 1, whose dS(n - 2) the dQ products
+        // of tile n - 2, issued earlier, read.
         auto issue_dp = [&](int n) {
           const uint64_t v_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS) + 1), 16, 1024);
-          mma_kmajor_full<D>(tmem + C::DP_COL, do_desc, v_k);
-          mma_commit(bb.dp_full);
+          mma_kmajor_full<D>(tmem + dp_col(n), do_desc, v_k);
+          mma_commit(&bb.dp_full[n & 1]);
         };
-        if (!wait(&bb.hold_full[f], k / NF) || !ring_wait(it)) {
+        if (!wait(&bb.hold_full[f], k / NF) || !ring_wait(it) ||
+            (it > 0 && !wait(s_read, it - 1))) {
           ok = false;
           break;
         }
@@ -860,22 +883,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int st = it % NS;
           const bool more = jt + 1 < w.n_iter;
           if (more) {
-            if (!ring_wait(it + 1)) { ok = false; break; }
+            if (!ring_wait(it + 1) || !wait(s_read, it)) { ok = false; break; }
             tc_fence_after();
             issue_s(it + 1);
+            issue_dp(it + 1);
           }
-          // dQ += dS K once both groups have written dS (bf16 pairs in
-          // columns DP_COL + h * 64.. for key half h; K rows h * 64..), then
-          // dP of the next tile over the columns those products read.  The
-          // item's first product overwrites the accumulator: group 0, which
-          // alone stores dQ, has done so before its dS arrival.
+          // dQ += dS K once both groups have written dS (bf16 pairs in the
+          // first 32 columns of each key half of dP buffer it & 1; K rows
+          // h * 64..).  The item's first product overwrites the accumulator:
+          // group 0, which alone stores dQ, has done so before its dS arrival.
           const uint64_t k_mn = smem_desc_sw128(taddr(2 * NF + 2 * st), C::BLOCK_BYTES, 1024);
-          if (!wait(bb.ds_ready, it)) { ok = false; break; }
+          if (!wait(&bb.ds_ready[it & 1], it >> 1)) { ok = false; break; }
           tc_fence_after();
           for (int hh = 0; hh < 2; ++hh)
-            mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + C::DP_COL + hh * H,
+            mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + dp_col(it) + hh * H,
                                k_mn + hh * kHalfStep, jt > 0 || hh > 0);
-          if (more) issue_dp(it + 1);
           mma_commit(&bb.ring_empty[st]);  // K and V of this stage may be refilled
         }
         if (!ok) break;
@@ -932,49 +954,63 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (got_next > 0) fetch(nxt);
         }
         const bool need_mask = (causal && jt == w.i) || (jt + 1) * T > Lk;
-        ok = __all_sync(FULL, wait(&bb.s_full[it & 1], it >> 1)) &&
-             __all_sync(FULL, wait(bb.dp_full, it));
+        // P over this group's 64 keys (rounded to bf16 as in the forward's
+        // P V product and in bwd_dkdv), then the S columns are released.
+        ok = __all_sync(FULL, wait(&bb.s_full[0], it));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t s_addr = tmem + lane_off + s_col(it) + half * H;
-        const uint32_t dp_addr = tmem + lane_off + C::DP_COL + half * H;
-        // dS over 32 keys at a time, written 16 pair columns at a time over
-        // dP columns this thread has already read.
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(s_addr + ch * 32, sr);
-          tmem_ld32(dp_addr + ch * 32, dr);
+        const uint32_t s_addr = tmem + lane_off + C::S_COL + half * H;
+        uint32_t pw[H / 2];
+        {
+          uint32_t sr[2][32];
+          tmem_ld32(s_addr, sr[0]);
+          tmem_ld32(s_addr + 32, sr[1]);
           tmem_ld_wait();
-          float x[32];
+          float x[H];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 p = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+          for (int e = 0; e < H; e += 2) {
+            const float2 p = ffma2(make_float2(__uint_as_float(sr[e >> 5][e & 31]),
+                                               __uint_as_float(sr[e >> 5][(e & 31) + 1])),
                                    sc2, nl2);
             x[e] = p.x;
             x[e + 1] = p.y;
           }
           if (need_mask) {
-            const int kv = kmax - (jt * T + half * H + ch * 32);
+            const int kv = kmax - (jt * T + half * H);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = neg_inf_if_gt(x[e], e, kv);
+            for (int e = 0; e < H; ++e) x[e] = neg_inf_if_gt(x[e], e, kv);
           }
-          uint32_t sw[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            // P is rounded to bf16 as in the forward's P V product and in bwd_dkdv.
-            const uint32_t pw = attn::pack_bf16x2(ex2(x[e]), ex2(x[e + 1]));
-            const float2 xd = fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                    nd2);
-            const float2 ds2 = ffma2(make_float2(attn::bf16_lo(pw), attn::bf16_hi(pw)), xd, zero2);
-            sw[e >> 1] = attn::pack_bf16x2(ds2.x, ds2.y);
-          }
-          tmem_st16(dp_addr + ch * 16, sw);
+          for (int e = 0; e < H; e += 2) pw[e >> 1] = attn::pack_bf16x2(ex2(x[e]), ex2(x[e + 1]));
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_read);
+        // dS = P (dP - D) over the half's first 32 columns of dP buffer it & 1
+        // (already read).
+        ok = __all_sync(FULL, wait(&bb.dp_full[it & 1], it >> 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t dp_addr = tmem + lane_off + dp_col(it) + half * H;
+        uint32_t dr[2][32];
+        tmem_ld32(dp_addr, dr[0]);
+        tmem_ld32(dp_addr + 32, dr[1]);
+        tmem_ld_wait();
+        uint32_t sw[H / 2];
+#pragma unroll
+        for (int e = 0; e < H; e += 2) {
+          const float2 xd = fadd2(make_float2(__uint_as_float(dr[e >> 5][e & 31]),
+                                              __uint_as_float(dr[e >> 5][(e & 31) + 1])),
+                                  nd2);
+          const uint32_t p = pw[e >> 1];
+          const float2 ds2 = ffma2(make_float2(attn::bf16_lo(p), attn::bf16_hi(p)), xd, zero2);
+          sw[e >> 1] = attn::pack_bf16x2(ds2.x, ds2.y);
+        }
+        tmem_st32(dp_addr, sw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bb.ds_ready);
+        if (lane == 0) mbar_arrive(&bb.ds_ready[it & 1]);
       }
       if (!ok) break;
       if (half == 0) {
@@ -1056,9 +1092,10 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   if (sms <= 0) return ATTN_ERR_CUDA;
   const long long heads = static_cast<long long>(B) * Hq;
   const long long rows_pad = heads * nq * T;
-  bwd_rowdot_kernel<<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
+  const long long rd_blocks = std::min((rows_pad + 8 * (256 / D) - 1) / (8 * (256 / D)), sms * 16);
+  bwd_rowdot_kernel<D><<<static_cast<unsigned>(rd_blocks), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, nlse, nd,
-      heads, Lq, static_cast<int>(nq * T), D, work);
+      heads, Lq, static_cast<int>(nq * T), work);
   bwd_dkdv_kernel<D><<<static_cast<unsigned>(std::min(dkdv_ctas, sms)), THREADS, L::BYTES, stream>>>(
       mq, mk, mv, mdo, nlse, nd, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
       B, Hq, Hkv, Lq, Lk, causal, scale, work, status);
