@@ -212,17 +212,26 @@ namespace {
 // another (about 24 bytes per clock from L2), so one thread alone would not
 // keep up with the tensor core at d = 64.  Producer 0 arms each pair's
 // barrier for both tiles; producer 1's copy only completes bytes on it.
-template <int D>
+// At d = 64 the item's gradient tiles (STG of them: dV and dK, or dQ) are
+// staged in shared memory in the 128-byte swizzle and written by one TMA
+// store each, instead of one 128-byte row per thread; bwd_dkdv gives up a
+// ring stage for its two staging tiles.
+template <int D, int STG>
 struct BwdSmem {
   using C = BwdCfg<D>;
   static constexpr int NF = D == 64 ? 2 : 1;
-  static constexpr int NS = D == 64 ? 4 : 2;
+  static constexpr int NS = D == 64 ? (STG == 2 ? 3 : 4) : 2;
   static constexpr int TILES = 2 * NF + 2 * NS;
-  static constexpr int OFF_VEC = TILES * C::TILE_BYTES;  // [NS][-LSE log2e | -D][128] fp32
+  static constexpr int OFF_STG = TILES * C::TILE_BYTES;  // STG staging tiles
+  static constexpr int OFF_VEC = OFF_STG + STG * C::TILE_BYTES;  // [NS][-LSE log2e | -D][128] fp32
   static constexpr int OFF_BAR = OFF_VEC + NS * 2 * T * 4;
   static constexpr int BYTES = OFF_BAR + 512 + 1024;  // barriers, item ring, alignment slack
 };
-static_assert(BwdSmem<64>::BYTES <= 227 * 1024 && BwdSmem<128>::BYTES <= 227 * 1024,
+// Staging tiles of each kernel: only at d = 64 (one tile holds a 64-column row block).
+template <int D> constexpr int kDkdvStg = D == 64 ? 2 : 0;
+template <int D> constexpr int kDqStg = D == 64 ? 1 : 0;
+static_assert(BwdSmem<64, 2>::BYTES <= 227 * 1024 && BwdSmem<64, 1>::BYTES <= 227 * 1024 &&
+                  BwdSmem<128, 0>::BYTES <= 227 * 1024,
               "shared memory of one CTA");
 
 constexpr int kItemRing = 8;  // published work items in flight
@@ -238,6 +247,8 @@ struct BwdBars {
   uint64_t* ds_ready;     // [2 iteration parities]: dS (dS^T) written
   uint64_t* acc_done;     // the item's accumulators are final
   uint64_t* drain;
+  uint64_t* st_ready;     // [2 groups] the group's rows are in its staging tile
+  uint64_t* st_free;      // [2 groups] the group's last tile store has read its staging tile
   uint64_t* item_full;    // [kItemRing] item id published
   int* items;             // [kItemRing]
   uint32_t* tmem_slot;
@@ -257,15 +268,17 @@ __device__ __forceinline__ BwdBars carve_bars(uint8_t* base) {
   r.ds_ready = b + 18;
   r.acc_done = b + 20;
   r.drain = b + 21;
-  r.item_full = b + 22;
-  r.items = reinterpret_cast<int*>(b + 22 + kItemRing);
+  r.st_ready = b + 22;
+  r.st_free = b + 24;
+  r.item_full = b + 26;
+  r.items = reinterpret_cast<int*>(b + 26 + kItemRing);
   r.tmem_slot = reinterpret_cast<uint32_t*>(r.items + kItemRing);
   r.abort_flag = reinterpret_cast<volatile int*>(r.tmem_slot + 1);
   return r;
 }
-static_assert((22 + kItemRing) * 8 + kItemRing * 4 + 8 <= 512, "barrier area");
-static_assert(BwdSmem<64>::NF <= 2 && BwdSmem<64>::NS <= 4 && BwdSmem<128>::NF <= 2 &&
-                  BwdSmem<128>::NS <= 4,
+static_assert((26 + kItemRing) * 8 + kItemRing * 4 + 8 <= 512, "barrier area");
+static_assert(BwdSmem<64, 1>::NF <= 2 && BwdSmem<64, 1>::NS <= 4 && BwdSmem<128, 0>::NF <= 2 &&
+                  BwdSmem<128, 0>::NS <= 4,
               "barrier counts");
 
 // Barrier set-up, the pending-timeout check and the TMEM allocation shared
@@ -286,6 +299,8 @@ __device__ __forceinline__ bool bwd_prologue(const BwdBars& bb, int* status) {
       mbar_init(&bb.dp_full[s], 1);
       mbar_init(&bb.p_ready[s], 8);   // one arrival per elementwise warp
       mbar_init(&bb.ds_ready[s], 8);
+      mbar_init(&bb.st_ready[s], 4);  // one arrival per warp of the group
+      mbar_init(&bb.st_free[s], 1);
     }
     for (int s = 0; s < kItemRing; ++s) mbar_init(&bb.item_full[s], 1);
     mbar_init(bb.acc_done, 1);
@@ -337,6 +352,27 @@ __device__ __forceinline__ void store_cols_bf16(uint32_t taddr, float mul, __nv_
         *reinterpret_cast<uint4*>(dst + c * 32 + v8 * 8) = w;
       }
     }
+  }
+}
+
+// One 64-column fp32 TMEM row (from `taddr`) times `mul` as bf16 into row r
+// of a staging tile in the 128-byte swizzle the TMA store expects (16-byte
+// chunk q of row r at position q ^ (r % 8)).
+__device__ __forceinline__ void stage_row64_bf16(uint32_t taddr, float mul, uint8_t* tile, int r) {
+  uint32_t v[2][32];
+  tmem_ld32(taddr, v[0]);
+  tmem_ld32(taddr + 32, v[1]);
+  tmem_ld_wait();
+  uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t* x = &v[q >> 2][(q & 3) * 8];
+    uint4 w;
+    w.x = attn::pack_bf16x2(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul);
+    w.y = attn::pack_bf16x2(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul);
+    w.z = attn::pack_bf16x2(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul);
+    w.w = attn::pack_bf16x2(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul);
+    *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) << 4)) = w;
   }
 }
 
@@ -427,12 +463,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ nlse,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const float* __restrict__ nlse,
                     const float* __restrict__ nd, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int B, int Hq, int Hkv, int Lq, int Lk,
                     int causal, float scale, int* work, int* status) {
   using C = BwdCfg<D>;
-  using L = BwdSmem<D>;
+  using L = BwdSmem<D, kDkdvStg<D>>;
+  constexpr bool kTmaEpi = kDkdvStg<D> > 0;
   constexpr int NF = L::NF, NS = L::NS;
   // Two S^T buffers where TMEM has room (d = 64): S^T of the next Q tile is
   // computed while the elementwise warps still work on this one.  At d = 128
@@ -722,13 +761,40 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = __all_sync(FULL, wait(bb.acc_done, k));
       if (!ok) break;
       tc_fence_after();
-      const int kk = w.j * T + c;
-      const bool live = kk < Lk;
-      const size_t out_row = (static_cast<size_t>(w.bhk) * Lk + (live ? kk : 0)) * D;
-      if (half == 0)
-        store_cols_bf16<D / 32>(tmem + lane_off + C::ACC1_COL, 1.f, dv + out_row, live);
-      else
-        store_cols_bf16<D / 32>(tmem + lane_off + C::ACC0_COL, scale, dk + out_row, live);
+      const uint32_t acc_col = half == 0 ? C::ACC1_COL : C::ACC0_COL;
+      const float mul = half == 0 ? 1.f : scale;
+      if constexpr (kTmaEpi) {
+        // Into the group's staging tile (once the previous item's store has
+        // read it), then the group's first warp stores the tile with TMA;
+        // rows past Lk are clipped by the tensor map.
+        if (k > 0) {
+          ok = __all_sync(FULL, wait(&bb.st_free[half], k - 1));
+          if (!ok) break;
+        }
+        uint8_t* stg = smem + L::OFF_STG + half * C::TILE_BYTES;
+        stage_row64_bf16(tmem + lane_off + acc_col, mul, stg, c);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bb.st_ready[half]);
+        if (quad == 0 && lane == 0) {
+          if (wait(&bb.st_ready[half], k)) {
+            tma_store_3d(half == 0 ? &tm_dv : &tm_dk, stg, 0, w.j * T, w.bhk);
+            bulk_commit_group();
+            bulk_wait_read_all();
+            mbar_arrive(&bb.st_free[half]);
+          } else {
+            ok = false;
+          }
+        }
+        ok = __shfl_sync(FULL, ok, 0);
+        if (!ok) break;
+      } else {
+        const int kk = w.j * T + c;
+        const bool live = kk < Lk;
+        const size_t out_row = (static_cast<size_t>(w.bhk) * Lk + (live ? kk : 0)) * D;
+        store_cols_bf16<D / 32>(tmem + lane_off + acc_col, mul, (half == 0 ? dv : dk) + out_row,
+                                live);
+      }
       tc_fence_before();
       w = nxt;
       got = got_next;
@@ -737,6 +803,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
       *bb.abort_flag = 1;
     }
+    if constexpr (kTmaEpi)
+      if (quad == 0 && lane == 0) bulk_wait_all();  // the tile stores have completed
   }
   bwd_epilogue(bb);
 }
@@ -752,11 +820,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ nlse,
+                  const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ nlse,
                   const float* __restrict__ nd, __nv_bfloat16* __restrict__ dq, int B, int Hq,
                   int Hkv, int Lq, int Lk, int causal, float scale, int* work, int* status) {
   using C = BwdCfg<D>;
-  using L = BwdSmem<D>;
+  using L = BwdSmem<D, kDqStg<D>>;
+  constexpr bool kTmaEpi = kDqStg<D> > 0;
   constexpr int NF = L::NF, NS = L::NS;
   // One S buffer and two dP buffers (TMEM columns 128 and 384; the
   // accumulator takes D columns from 256).  The elementwise warps turn S
@@ -1014,13 +1084,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       if (half == 0) {
-        // Group 0 writes dQ row qrow (all D columns).
+        // Group 0 writes dQ row qrow (all D columns): at d = 64 through its
+        // staging tile and one TMA store by warp 4 (rows past Lq clipped).
         ok = __all_sync(FULL, wait(bb.acc_done, k));
         if (!ok) break;
         tc_fence_after();
-        const bool live = qrow < Lq;
-        const size_t out_row = (static_cast<size_t>(w.bhq) * Lq + (live ? qrow : 0)) * D;
-        store_cols_bf16<D / 32>(tmem + lane_off + C::ACC0_COL, scale, dq + out_row, live);
+        if constexpr (kTmaEpi) {
+          if (k > 0) {
+            ok = __all_sync(FULL, wait(&bb.st_free[0], k - 1));
+            if (!ok) break;
+          }
+          uint8_t* stg = smem + L::OFF_STG;
+          stage_row64_bf16(tmem + lane_off + C::ACC0_COL, scale, stg, r);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bb.st_ready[0]);
+          if (quad == 0 && lane == 0) {
+            if (wait(&bb.st_ready[0], k)) {
+              tma_store_3d(&tm_dq, stg, 0, w.i * T, w.bhq);
+              bulk_commit_group();
+              bulk_wait_read_all();
+              mbar_arrive(&bb.st_free[0]);
+            } else {
+              ok = false;
+            }
+          }
+          ok = __shfl_sync(FULL, ok, 0);
+          if (!ok) break;
+        } else {
+          const bool live = qrow < Lq;
+          const size_t out_row = (static_cast<size_t>(w.bhq) * Lq + (live ? qrow : 0)) * D;
+          store_cols_bf16<D / 32>(tmem + lane_off + C::ACC0_COL, scale, dq + out_row, live);
+        }
         tc_fence_before();
       }
       w = nxt;
@@ -1030,6 +1125,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) attn::record_status(status, ATTN_ERR_DEVICE_TIMEOUT);
       *bb.abort_flag = 1;
     }
+    if constexpr (kTmaEpi)
+      if (half == 0 && quad == 0 && lane == 0) bulk_wait_all();  // the tile stores have completed
   }
   bwd_epilogue(bb);
 }
@@ -1060,21 +1157,24 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
                          float* dd, int B, int Hq, int Hkv, int Lq, int Lk, int causal,
                          float scale, cudaStream_t stream) {
-  using L = BwdSmem<D>;
+  using LK = BwdSmem<D, kDkdvStg<D>>;
+  using LQ = BwdSmem<D, kDqStg<D>>;
   static bool attr_set[64] = {};  // per device: kernel attributes are per device
   const int dev = attn_host::current_device_slot();
   if (dev < 0) return ATTN_ERR_CUDA;
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::BYTES) != cudaSuccess ||
+                             LK::BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::BYTES) != cudaSuccess)
+                             LQ::BYTES) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_set[dev] = true;
   }
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if (!make_map_rows(&mq, q, D, Lq, B * Hq) || !make_map_rows(&mk, k, D, Lk, B * Hkv) ||
-      !make_map_rows(&mv, v, D, Lk, B * Hkv) || !make_map_rows(&mdo, d_o, D, Lq, B * Hq))
+      !make_map_rows(&mv, v, D, Lk, B * Hkv) || !make_map_rows(&mdo, d_o, D, Lq, B * Hq) ||
+      !make_map_rows(&mdq, dq, D, Lq, B * Hq) || !make_map_rows(&mdk, dk, D, Lk, B * Hkv) ||
+      !make_map_rows(&mdv, dv, D, Lk, B * Hkv))
     return ATTN_ERR_CUDA;
   const long long nq = (Lq + T - 1) / T, nk = (Lk + T - 1) / T;
   const long long dq_ctas = nq * B * Hq, dkdv_ctas = nk * B * Hkv;
@@ -1096,11 +1196,11 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   bwd_rowdot_kernel<D><<<static_cast<unsigned>(rd_blocks), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, nlse, nd,
       heads, Lq, static_cast<int>(nq * T), work);
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>(std::min(dkdv_ctas, sms)), THREADS, L::BYTES, stream>>>(
-      mq, mk, mv, mdo, nlse, nd, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>(std::min(dkdv_ctas, sms)), THREADS, LK::BYTES, stream>>>(
+      mq, mk, mv, mdo, mdk, mdv, nlse, nd, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
       B, Hq, Hkv, Lq, Lk, causal, scale, work, status);
-  bwd_dq_kernel<D><<<static_cast<unsigned>(std::min(dq_ctas, sms)), THREADS, L::BYTES, stream>>>(
-      mq, mk, mv, mdo, nlse, nd, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv, Lq, Lk, causal,
+  bwd_dq_kernel<D><<<static_cast<unsigned>(std::min(dq_ctas, sms)), THREADS, LQ::BYTES, stream>>>(
+      mq, mk, mv, mdo, mdq, nlse, nd, static_cast<__nv_bfloat16*>(dq), B, Hq, Hkv, Lq, Lk, causal,
       scale, work, status);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
