@@ -765,9 +765,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float mul = half == 0 ? 1.f : scale;
       if constexpr (kTmaEpi) {
         // Into the group's staging tile (once the previous item's store has
-        // read it), then the group's first warp stores the tile with TMA;
-        // rows past Lk are clipped by the tensor map.
+        // read it: its issuing thread checks and signals here, an item
+        // later, so the store overlaps that item), then the group's first
+        // warp stores the tile with TMA; rows past Lk are clipped by the map.
         if (k > 0) {
+          if (quad == 0 && lane == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&bb.st_free[half]);
+          }
           ok = __all_sync(FULL, wait(&bb.st_free[half], k - 1));
           if (!ok) break;
         }
@@ -780,8 +785,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (wait(&bb.st_ready[half], k)) {
             tma_store_3d(half == 0 ? &tm_dv : &tm_dk, stg, 0, w.j * T, w.bhk);
             bulk_commit_group();
-            bulk_wait_read_all();
-            mbar_arrive(&bb.st_free[half]);
           } else {
             ok = false;
           }
@@ -1090,7 +1093,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         if constexpr (kTmaEpi) {
-          if (k > 0) {
+          if (k > 0) {  // the previous item's store has read the staging tile
+            if (quad == 0 && lane == 0) {
+              bulk_wait_read_all();
+              mbar_arrive(&bb.st_free[0]);
+            }
             ok = __all_sync(FULL, wait(&bb.st_free[0], k - 1));
             if (!ok) break;
           }
@@ -1103,8 +1110,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (wait(&bb.st_ready[0], k)) {
               tma_store_3d(&tm_dq, stg, 0, w.i * T, w.bhq);
               bulk_commit_group();
-              bulk_wait_read_all();
-              mbar_arrive(&bb.st_free[0]);
             } else {
               ok = false;
             }
