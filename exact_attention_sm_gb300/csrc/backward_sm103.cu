@@ -831,10 +831,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   using L = BwdSmem<D, kDqStg<D>>;
   constexpr bool kTmaEpi = kDqStg<D> > 0;
   constexpr int NF = L::NF, NS = L::NS;
-  // One S buffer and two dP buffers (TMEM columns 128 and 384; the
+  // d = 64: one S buffer and two dP buffers (TMEM columns 128 and 384; the
   // accumulator takes D columns from 256).  The elementwise warps turn S
   // into P first and signal (p_ready[0]), so S and dP of the next K/V tile
-  // are computed while they work on dS of this one.
+  // are computed while they work on dS of this one.  d = 128 (long
+  // products): two S buffers (0 and 384) and one dP buffer; S of the next
+  // tile is issued early, its dP after the dQ products that read dS.
+  constexpr bool kEarlyS = D == 64;
   static_assert(C::ACC0_COL + D <= C::S1_COL, "TMEM columns");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -863,8 +866,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     w = q_item(x, nk, nq, B, Hq, Hkv, causal);
     return 1;
   };
-  auto dp_col = [&](int it) -> uint32_t { return (it & 1) ? C::S1_COL : C::DP_COL; };
-  uint64_t* s_read = &bb.p_ready[0];  // every elementwise warp has read S
+  auto dp_col = [&](int it) -> uint32_t {
+    return (kEarlyS && (it & 1)) ? C::S1_COL : C::DP_COL;
+  };
+  auto s_col = [&](int it) -> uint32_t {
+    return (!kEarlyS && (it & 1)) ? C::S1_COL : C::S_COL;
+  };
+  // S(it) / dP(it): barrier and phase.
+  auto s_bar = [&](int it) { return &bb.s_full[kEarlyS ? 0 : (it & 1)]; };
+  auto s_ph = [&](int it) { return kEarlyS ? it : (it >> 1); };
+  auto dp_bar = [&](int it) { return &bb.dp_full[kEarlyS ? (it & 1) : 0]; };
+  auto dp_ph = [&](int it) { return kEarlyS ? (it >> 1) : it; };
+  uint64_t* s_read = &bb.p_ready[0];  // every elementwise warp has read S (d = 64)
 
   if (warp == 0 || warp == 2) {
     if (lane == 0) {
@@ -930,22 +943,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int f = k % NF;
         const uint64_t q_desc = smem_desc_sw128(taddr(2 * f), 16, 1024);
         const uint64_t do_desc = smem_desc_sw128(taddr(2 * f + 1), 16, 1024);
-        // S(n) = Q K^T (queries as rows, keys as columns), once the warps
-        // have read S(n - 1).
+        // S(n) = Q K^T (queries as rows, keys as columns); at d = 64 once
+        // the warps have read S(n - 1).
         auto issue_s = [&](int n) {
           const uint64_t k_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS)), 16, 1024);
-          mma_kmajor_full<D>(tmem + C::S_COL, q_desc, k_k);
-          mma_commit(&bb.s_full[0]);
+          mma_kmajor_full<D>(tmem + s_col(n), q_desc, k_k);
+          mma_commit(s_bar(n));
         };
-        // dP(n) = dO V^T into buffer n & 1, whose dS(n - 2) the dQ products
-        // of tile n - 2, issued earlier, read.
+        // dP(n) = dO V^T into its buffer, whose dS the dQ products issued
+        // earlier read.
         auto issue_dp = [&](int n) {
           const uint64_t v_k = smem_desc_sw128(taddr(2 * NF + 2 * (n % NS) + 1), 16, 1024);
           mma_kmajor_full<D>(tmem + dp_col(n), do_desc, v_k);
-          mma_commit(&bb.dp_full[n & 1]);
+          mma_commit(dp_bar(n));
         };
         if (!wait(&bb.hold_full[f], k / NF) || !ring_wait(it) ||
-            (it > 0 && !wait(s_read, it - 1))) {
+            (kEarlyS && it > 0 && !wait(s_read, it - 1))) {
           ok = false;
           break;
         }
@@ -956,10 +969,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int st = it % NS;
           const bool more = jt + 1 < w.n_iter;
           if (more) {
-            if (!ring_wait(it + 1) || !wait(s_read, it)) { ok = false; break; }
+            if (!ring_wait(it + 1) || (kEarlyS && !wait(s_read, it))) { ok = false; break; }
             tc_fence_after();
             issue_s(it + 1);
-            issue_dp(it + 1);
+            if (kEarlyS) issue_dp(it + 1);
           }
           // dQ += dS K once both groups have written dS (bf16 pairs in the
           // first 32 columns of each key half of dP buffer it & 1; K rows
@@ -971,6 +984,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int hh = 0; hh < 2; ++hh)
             mma_tmem_a_half<D>(tmem + C::ACC0_COL, tmem + dp_col(it) + hh * H,
                                k_mn + hh * kHalfStep, jt > 0 || hh > 0);
+          if (!kEarlyS && more) issue_dp(it + 1);  // over dS(it), after the products above
           mma_commit(&bb.ring_empty[st]);  // K and V of this stage may be refilled
         }
         if (!ok) break;
@@ -1029,10 +1043,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool need_mask = (causal && jt == w.i) || (jt + 1) * T > Lk;
         // P over this group's 64 keys (rounded to bf16 as in the forward's
         // P V product and in bwd_dkdv), then the S columns are released.
-        ok = __all_sync(FULL, wait(&bb.s_full[0], it));
+        ok = __all_sync(FULL, wait(s_bar(it), s_ph(it)));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t s_addr = tmem + lane_off + C::S_COL + half * H;
+        const uint32_t s_addr = tmem + lane_off + s_col(it) + half * H;
         uint32_t pw[H / 2];
         {
           uint32_t sr[2][32];
@@ -1061,7 +1075,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(s_read);
         // dS = P (dP - D) over the half's first 32 columns of dP buffer it & 1
         // (already read).
-        ok = __all_sync(FULL, wait(&bb.dp_full[it & 1], it >> 1));
+        ok = __all_sync(FULL, wait(dp_bar(it), dp_ph(it)));
         if (!ok) break;
         tc_fence_after();
         const uint32_t dp_addr = tmem + lane_off + dp_col(it) + half * H;
