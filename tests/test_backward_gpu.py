@@ -86,6 +86,28 @@ def test_deterministic():
         assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_more_items_than_ctas_ragged(d):
+    """288 K/V tiles and 288 Q tiles (2 x 16 heads x 9 tiles, the last 76 rows
+    long): more work items than persistent CTAs, so CTAs take several items,
+    some of them ragged, through the item ring and the staged stores."""
+    run(2, 16, 16, 1100, 1100, d, True, seed=8)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_workspace_reused_across_calls(d):
+    """One workspace for several calls: the work counters in it are reset by
+    every call (the persistent CTAs claim all items again), results equal."""
+    args, (dq, dk, dv) = run(2, 4, 2, 300, 300, d, True, seed=7)
+    B, Hq, Lq = args[0].shape[0], args[0].shape[1], args[0].shape[2]
+    ws = torch.empty(ea.lib().attn_bwd_workspace_bytes(B, Hq, Lq), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        dq2, dk2, dv2 = ea.attn_bwd(*args, causal=True, scale=1.0 / math.sqrt(d), workspace=ws)
+        torch.cuda.synchronize()
+        assert ea.attn_get_device_status() == "ATTN_OK"
+        assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
 def run_sampled_groups(B, Hq, Hkv, L, d, groups, seed):
     """Full-size causal backward on the GPU; the oracle checks the sampled
     (batch, KV head) groups: dQ of every query head of the group, and the
