@@ -590,6 +590,11 @@ int cascade_prefix_chunks(int prefix_len, int rows_per_kvh, int Hkv, int slots) 
   return best;
 }
 
+// The prefix pass runs beside the suffix decode, whose CTAs need the SMs the
+// prefill leaves free (a d = 128 prefill CTA takes a whole SM's shared
+// memory), so the chunk plan is made for half the SMs.
+int cascade_prefix_slots(int sms) { return sms / 2 > 0 ? sms / 2 : 1; }
+
 // One side stream and its fork / join events per device, created on first
 // use and kept for the process.  Concurrent callers share them: the side
 // stream then runs their suffix passes one after another, and a join event
@@ -650,8 +655,9 @@ attn_status_t attn_cascade_plan(int B, int Hq, int Hkv, int prefix_len,
       suffix_chunk_out == nullptr || suffix_splits_out == nullptr)
     return ATTN_ERR_INVALID_ARG;
   if (prefix_slots <= 0) {
-    prefix_slots = attn_host::num_sms();
-    if (prefix_slots <= 0) return ATTN_ERR_CUDA;
+    const int sms = attn_host::num_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    prefix_slots = cascade_prefix_slots(sms);
   }
   *prefix_chunks_out = cascade_prefix_chunks(prefix_len, B * (Hq / Hkv), Hkv, prefix_slots);
   return attn_decode_plan(suffix_lens_host, B, Hkv, page_size, num_splits, suffix_slots,
@@ -689,7 +695,8 @@ attn_status_t attn_decode_cascade(const void* q, const void* prefix_k, const voi
       return ATTN_ERR_INVALID_ARG;
   const int sms = attn_host::num_sms();
   if (sms <= 0) return ATTN_ERR_CUDA;
-  const int prefix_chunks = cascade_prefix_chunks(prefix_len, B * (Hq / Hkv), Hkv, sms);
+  const int prefix_chunks =
+      cascade_prefix_chunks(prefix_len, B * (Hq / Hkv), Hkv, cascade_prefix_slots(sms));
   int32_t chunk = max_pages_per_seq * page_size, smax = 1;
   if (num_splits != 1)
     plan_cached(seq_lens_host, B, Hkv, page_size, num_splits,

@@ -36,13 +36,16 @@ __global__ void cascade_gather_q_kernel(const uint4* __restrict__ q, uint4* __re
 }
 
 constexpr int kRowsPerBlock = 4;  // one warp per output row
+constexpr int kBatch = 24;        // states whose O slices are in flight at once
 constexpr unsigned kFull = 0xffffffffu;
 
 // One warp per output row.  The row's S = S_pre + S_suf states are numbered
-// prefix chunks first, then suffix segments; lane l holds the LSE (and later
-// the weight) of states l, l + 32, ...  The max and the weight sum are
-// butterfly reductions and the weighted sum of the O_s runs over s in
-// ascending order, so the result depends on (S_pre, S_suf) alone.
+// prefix chunks first, then suffix segments.  The row is latency-bound (a few
+// KB per row), so every load it needs is issued before any is used: the O
+// slices of the first kBatch states and the LSEs of the first 32 go out
+// together, and the max is reduced while they are in flight.  The weighted
+// sum of the O_s and the weight sum run over s in ascending order, so the
+// result depends on (S_pre, S_suf) alone.
 __global__ void __launch_bounds__(kRowsPerBlock * 32)
     cascade_merge_kernel(const __nv_bfloat16* __restrict__ o_pre, const float* __restrict__ lse_pre,
                          int S_pre, const float* __restrict__ o_suf,
@@ -61,53 +64,61 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
     return s < S_pre ? lse_pre[(static_cast<long long>(h) * S_pre + s) * lq + prow]
                      : lse_suf[static_cast<long long>(r) * S_suf + (s - S_pre)];
   };
+  // The lane's 4 dims of state s: bf16 (prefix, in .x .y) or fp32 bits (suffix).
+  auto load_o = [&](int s) {
+    if (s < S_pre) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(
+          o_pre + ((static_cast<long long>(h) * S_pre + s) * lq + prow) * D + 4 * lane);
+      return make_uint4(raw.x, raw.y, 0u, 0u);
+    }
+    return *reinterpret_cast<const uint4*>(
+        o_suf + (static_cast<long long>(r) * S_suf + (s - S_pre)) * D + 4 * lane);
+  };
+  auto as_float4 = [&](int s, uint4 x) {
+    return s < S_pre ? make_float4(attn::bf16_lo(x.x), attn::bf16_hi(x.x), attn::bf16_lo(x.y),
+                                   attn::bf16_hi(x.y))
+                     : make_float4(__uint_as_float(x.x), __uint_as_float(x.y),
+                                   __uint_as_float(x.z), __uint_as_float(x.w));
+  };
 
-  float big = -INFINITY;
-  for (int s = lane; s < S; s += 32) big = fmaxf(big, state_lse(s));
+  uint4 x[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u)
+    if (u < S) x[u] = load_o(u);
+  const float ls0 = lane < S ? state_lse(lane) : -INFINITY;
+  float big = ls0;
+  for (int s = lane + 32; s < S; s += 32) big = fmaxf(big, state_lse(s));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) big = fmaxf(big, __shfl_xor_sync(kFull, big, off));
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (big != -INFINITY) {
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      const int mine = s0 + lane;
-      const float ls = mine < S ? state_lse(mine) : -INFINITY;
-      const float wl = ls == -INFINITY ? 0.f : expf(ls - big);  // empty state: weight 0
-      float part = wl;
+    const float wl = ls0 == -INFINITY ? 0.f : expf(ls0 - big);  // weight of state `lane`
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+      if (s0 > 0) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
-      wsum += part;
-      const int n = min(32, S - s0);
-      // Batches of 8 states: all loads first, then the FMAs in state order.
-      // Empty states hold O = 0 (both producers write it), so their weight 0
-      // needs no branch.
-      for (int j0 = 0; j0 < n; j0 += 8) {
-        float4 x[8];
+        for (int u = 0; u < kBatch; ++u)
+          if (s0 + u < S) x[u] = load_o(s0 + u);
+      }
+      // Empty states hold O = 0 (both producers write it) and weigh 0.
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int s = s0 + j0 + u;
-          if (j0 + u >= n) {
-            x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          } else if (s < S_pre) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(
-                o_pre + ((static_cast<long long>(h) * S_pre + s) * lq + prow) * D + 4 * lane);
-            x[u] = make_float4(attn::bf16_lo(raw.x), attn::bf16_hi(raw.x), attn::bf16_lo(raw.y),
-                               attn::bf16_hi(raw.y));
-          } else {
-            x[u] = *reinterpret_cast<const float4*>(
-                o_suf + (static_cast<long long>(r) * S_suf + (s - S_pre)) * D + 4 * lane);
-          }
+      for (int u = 0; u < kBatch; ++u) {
+        const int s = s0 + u;  // warp-uniform
+        if (s >= S) break;
+        float w;
+        if (s < 32) {
+          w = __shfl_sync(kFull, wl, s);
+        } else {
+          const float l = state_lse(s);
+          w = l == -INFINITY ? 0.f : expf(l - big);
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float w = __shfl_sync(kFull, wl, (j0 + u) & 31);
-          if (j0 + u >= n) break;
-          acc.x = fmaf(w, x[u].x, acc.x);
-          acc.y = fmaf(w, x[u].y, acc.y);
-          acc.z = fmaf(w, x[u].z, acc.z);
-          acc.w = fmaf(w, x[u].w, acc.w);
-        }
+        const float4 v = as_float4(s, x[u]);
+        wsum += w;
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
       }
     }
   }

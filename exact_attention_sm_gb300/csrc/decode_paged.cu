@@ -276,7 +276,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
   const int h0 = kvh * group + gi * HG;
   const int nh = min(HG, group - gi * HG);  // real heads in this CTA (the rest is padding)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p_begin = s * chunk / PAGE;
 
+  // The loads that start the CTA go out together, before the length is
+  // known: the producer's first 32 block-table entries (inside the row,
+  // used only below the page count), the consumers' query rows, the length.
+  const int32_t* row = block_table + static_cast<size_t>(b) * max_pages + p_begin;
+  int entry0 = 0;
+  if (warp == 0 && lane < max_pages - p_begin) entry0 = row[lane];
+  uint32_t qw[HG][WPL];
+  if (warp != 0) {
+    const int l8 = lane & 7;
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      const int hq = h0 + min(h, nh - 1);  // padded heads reuse a real head's q
+      const uint4* qp =
+          reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq) * DD + DL * l8);
+#pragma unroll
+      for (int c = 0; c < WPL / 4; ++c) {
+        const uint4 a4 = qp[c];
+        qw[h][4 * c] = a4.x;
+        qw[h][4 * c + 1] = a4.y;
+        qw[h][4 * c + 2] = a4.z;
+        qw[h][4 * c + 3] = a4.w;
+      }
+    }
+  }
   // A length past the table's capacity is reported and clamped, so the
   // block-table row is never read out of bounds.
   int len = seq_lens[b];
@@ -286,7 +311,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
   }
   const int t_begin = s * chunk;
   const int t_end = min(len, t_begin + chunk);
-  const int p_begin = t_begin / PAGE;
   const int n_pages = t_end > t_begin ? (t_end + PAGE - 1) / PAGE - p_begin : 0;
 
   if (threadIdx.x == 0) {
@@ -305,9 +329,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
     prefetch_tmap(&tm_v);
     bool ok = true;
     int issued = 0;
-    const int32_t* row = block_table + static_cast<size_t>(b) * max_pages + p_begin;
     for (int i0 = 0; ok && i0 < n_pages; i0 += 32) {
-      const int entry = i0 + lane < n_pages ? row[i0 + lane] : 0;
+      const int entry = i0 + lane < n_pages ? (i0 == 0 ? entry0 : row[i0 + lane]) : 0;
       const int cnt = min(32, n_pages - i0);
       for (int k = 0; k < cnt; ++k) {
         const int page = __shfl_sync(FULL, entry, k);
@@ -349,21 +372,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 3)
     const int grp = lane >> 3;       // token group within the warp
     const int l8 = lane & 7;         // owns dims [DL l8, DL l8 + DL)
     const int own_h = l8 >> 1;       // head of the values this lane holds after the reduction
-    uint32_t qw[HG][WPL];
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      const int hq = h0 + min(h, nh - 1);  // padded heads reuse a real head's q
-      const uint4* qp =
-          reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq) * DD + DL * l8);
-#pragma unroll
-      for (int c = 0; c < WPL / 4; ++c) {
-        const uint4 a4 = qp[c];
-        qw[h][4 * c] = a4.x;
-        qw[h][4 * c + 1] = a4.y;
-        qw[h][4 * c + 2] = a4.z;
-        qw[h][4 * c + 3] = a4.w;
-      }
-    }
     float acc[HG][DL];
     float m_run[HG];
 #pragma unroll

@@ -408,7 +408,9 @@ attn_status_t attn_prefill_bsr(const void* q, const void* k_blocks, const void* 
  *   the waves of prefill items times their K/V tiles plus a 2-tile per-item
  *   overhead; ties go to fewer chunks.  The suffix split plan is
  *   attn_decode_plan with suffix_slots.  prefix_slots <= 0 / suffix_slots <= 0 query the
- *   current device (SMs / resident decode CTAs), as attn_decode_cascade does.
+ *   current device, as attn_decode_cascade does: half its SMs for the prefix
+ *   pass (the suffix decode runs beside it on the other half) / its resident
+ *   decode CTAs.
  * attn_cascade_workspace_bytes: bytes attn_decode_cascade needs for the plan
  *   (stacked queries, prefix-chunk states, suffix states), 256-byte aligned.
  * attn_decode_cascade: q [B, Hq, d], o [B, Hq, d] bf16, lse [B, Hq] fp32 or
