@@ -30,11 +30,13 @@ def run_cascade(prefix_len, suffix_lens, Hq=32, Hkv=8, num_splits=0, seed=0):
     return o, lse
 
 
+@pytest.mark.parametrize("splits", [0, 1])
 @pytest.mark.parametrize("prefix_len", [1, 100, 128, 300, 1000])
-def test_small_prefixes_and_ragged_suffixes(prefix_len):
+def test_small_prefixes_and_ragged_suffixes(prefix_len, splits):
     """Prefixes below, at and past one 128-key tile (ragged chunks), suffixes
-    of 0 (prefix only), 1, 17 and 200 tokens."""
-    run_cascade(prefix_len, [0, 1, 17, 200], seed=prefix_len)
+    of 0 (prefix only), 1, 17 and 200 tokens; one suffix state per row, and
+    the planned splits (several per row for these short batches)."""
+    run_cascade(prefix_len, [0, 1, 17, 200], num_splits=splits, seed=prefix_len)
 
 
 @pytest.mark.parametrize("splits", [1, 3])
@@ -42,9 +44,10 @@ def test_forced_suffix_splits(splits):
     run_cascade(512, [5, 700, 64], num_splits=splits, seed=5)
 
 
+@pytest.mark.parametrize("splits", [0, 1])
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4), (64, 8)])
-def test_group_sizes(hq, hkv):
-    run_cascade(256, [33, 0, 129], Hq=hq, Hkv=hkv, seed=7)
+def test_group_sizes(hq, hkv, splits):
+    run_cascade(256, [33, 0, 129], Hq=hq, Hkv=hkv, num_splits=splits, seed=7)
 
 
 def test_lecture_demo_shape_B64_prefix4096_suffix256():
@@ -90,11 +93,53 @@ def orc_gather(pages, table_row, n):
     return pages[table_row[t // 16].long(), t % 16]
 
 
-def test_cascade_is_deterministic():
+@pytest.mark.parametrize("splits", [0, 1])
+def test_cascade_is_deterministic(splits):
     q, pk, pv, kp, vp, table, sl = inputs.cascade_inputs(2048, [300, 5, 0, 1200], 32, 8, 128,
                                                          seed=9)
     args = [t.cuda() for t in (q, pk, pv, kp, vp, table, sl)]
-    outs = [ea.attn_decode_cascade(*args, seq_lens_host=[300, 5, 0, 1200]) for _ in range(3)]
+    outs = [ea.attn_decode_cascade(*args, seq_lens_host=[300, 5, 0, 1200], num_splits=splits)
+            for _ in range(3)]
     torch.cuda.synchronize()
     for o, lse in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
+@pytest.mark.parametrize("splits", [0, 1])
+def test_graph_replay_with_new_queries(splits):
+    """The cascade captured once in a CUDA graph (its side stream forks from
+    the capturing stream and joins back before the merge pass) and replayed
+    with new query values in the same buffer: every replay matches the oracle."""
+    P, lens, Hq, Hkv = 1000, [256] * 20 + [3, 0, 77], 32, 8
+    q, pk, pv, kp, vp, table, sl = inputs.cascade_inputs(P, lens, Hq, Hkv, 128, seed=11)
+    scale = 1.0 / math.sqrt(128)
+    qc = q.cuda()
+    dev = [t.cuda() for t in (pk, pv, kp, vp, table, sl)]
+    o = torch.empty_like(qc)
+    lse = torch.empty(len(lens), Hq, dtype=torch.float32, device="cuda")
+    pc, _, ss = ea.attn_cascade_plan(len(lens), Hq, Hkv, P, lens, 16, splits)
+    ws = torch.empty(ea.attn_cascade_workspace_bytes(len(lens), Hq, 128, pc, ss), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        ea.attn_decode_cascade(qc, *dev, seq_lens_host=lens, num_splits=splits, scale=scale, out=o,
+                               lse=lse, workspace=ws)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    f = lambda t: t.float().numpy()
+    for rep in range(3):
+        qn = torch.randn(q.shape, generator=torch.Generator().manual_seed(100 + rep)).to(q.dtype)
+        qc.copy_(qn)
+        g.replay()
+        torch.cuda.synchronize()
+        assert ea.attn_get_device_status() == "ATTN_OK"
+        o_ref, lse_ref = orc.decode_cascade(f(qn), f(pk), f(pv), f(kp), f(vp), table.numpy(), lens,
+                                            scale)
+        check_o(to_np(o), o_ref, "bf16")
+        check_lse(to_np(lse), lse_ref, "bf16")
