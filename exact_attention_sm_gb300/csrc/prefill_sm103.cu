@@ -1035,11 +1035,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         ++ns;
         tc_fence_after();
-        uint32_t sr[4][32];
+        // S and, from the load itself, the maximum of each 32-column chunk.
+        float sr[4][32], cmax[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32_max(s_addr + c * 32, sr[c], cmax[c]);
         tmem_ld_wait();
-        float* s = reinterpret_cast<float*>(&sr[0][0]);
+        float* s = &sr[0][0];
 
         const bool need_mask = kPacked ? tile_needs_mask(w.sq, w.qt[x], j, causal)
                                        : (j == n - 1) && (causal || (geo.Lk % BN) != 0);
@@ -1049,16 +1050,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = mask_col(s[c], c, kv);
         }
-        // Row max as 8 independent chains (short dependency depth).
-        float mx[8];
+        // Row max: an unmasked tile takes it from the load; a masked one
+        // reduces the masked scores as 8 independent chains.
+        float mt = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
+        if (need_mask) {
+          float mx[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-        for (int c = 16; c < BN; c += 16)
+          for (int c = 16; c < BN; c += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
-        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                               fmaxf(mx[6], mx[7]));
+            for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        }
         const float mt_s = mt * scale_log2;
         float alpha = 1.f;
         if (mt_s > m_s + kRescaleThreshold) {
@@ -1715,11 +1719,12 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
         ok = __all_sync(FULL, wait(s_full, tt));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[4][32];
+        // S and, from the load itself, the maximum of each 32-column chunk.
+        float sr[4][32], cmax[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32_max(s_addr + c * 32, sr[c], cmax[c]);
         tmem_ld_wait();
-        float* s = reinterpret_cast<float*>(&sr[0][0]);
+        float* s = &sr[0][0];
         // S is in registers: S(tt + 1) may overwrite it.
         tc_fence_before();
         __syncwarp();
@@ -1733,15 +1738,19 @@ __global__ void __launch_bounds__(Cfg64::THREADS, 2)
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = mask_col(s[c], c, kv);
         }
-        float mx[8];
+        // Row max: an unmasked tile takes it from the load; a masked one
+        // reduces the masked scores as 8 independent chains.
+        float mt = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
+        if (need_mask) {
+          float mx[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-        for (int c = 16; c < BN; c += 16)
+          for (int c = 16; c < BN; c += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
-        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                               fmaxf(mx[6], mx[7]));
+            for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        }
         const float mt_s = mt * scale_log2;
         float alpha = 1.f;
         if (mt_s > m_s + kRescaleThreshold) {
