@@ -758,9 +758,16 @@ __global__ void __launch_bounds__(128)
     const int u = plan.seg_units[s];
     return (u >= 0 && u < U) ? u : -1;
   };
-  float big = -INFINITY;
-  for (int s = s0 + lane; s < s1; s += 32) {
-    const int u = unit_of(s);
+  // The row is latency-bound (a few KB over many segments), so loads go out
+  // together: lane l holds the unit and LSE of segments s0 + l, s0 + l + 32,
+  // ... (the first 32 kept in registers), and the O slices are read in
+  // batches of 8 segments, all 8 loads issued before the first is used.
+  const int n = s1 - s0;
+  const int u_first = lane < n ? unit_of(s0 + lane) : -1;
+  const float ls_first = u_first >= 0 ? part_lse[static_cast<size_t>(u_first) * HG + h] : -INFINITY;
+  float big = ls_first;
+  for (int i = lane + 32; i < n; i += 32) {
+    const int u = unit_of(s0 + i);
     if (u >= 0) big = fmaxf(big, part_lse[static_cast<size_t>(u) * HG + h]);
   }
 #pragma unroll
@@ -768,19 +775,40 @@ __global__ void __launch_bounds__(128)
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (big != -INFINITY) {
-    for (int s = s0; s < s1; ++s) {
-      const int u = unit_of(s);
-      if (u < 0) continue;
-      const size_t slot = static_cast<size_t>(u) * HG + h;
-      const float ls = part_lse[slot];
-      if (ls == -INFINITY) continue;  // an empty segment: weight 0, O not read
-      const float w = expf(ls - big);
-      const float4 x = *reinterpret_cast<const float4*>(part_o + slot * D + 4 * lane);
-      wsum += w;
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
+    for (int base = 0; base < n; base += 32) {
+      int u_l = u_first;
+      float ls_l = ls_first;
+      if (base > 0) {
+        u_l = base + lane < n ? unit_of(s0 + base + lane) : -1;
+        ls_l = u_l >= 0 ? part_lse[static_cast<size_t>(u_l) * HG + h] : -INFINITY;
+      }
+      // An empty segment (LSE = -inf) weighs 0 and its O is not read.
+      const float w_l = (u_l >= 0 && ls_l != -INFINITY) ? expf(ls_l - big) : 0.f;
+      const int cnt = min(32, n - base);
+      for (int j0 = 0; j0 < cnt; j0 += 8) {
+        float4 x[8];
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int j = j0 + k;  // warp-uniform
+          const int u = __shfl_sync(FULL, u_l, j & 31);
+          w[k] = __shfl_sync(FULL, w_l, j & 31);
+          if (j >= cnt) w[k] = 0.f;
+          x[k] = w[k] > 0.f ? *reinterpret_cast<const float4*>(
+                                  part_o + (static_cast<size_t>(u) * HG + h) * D + 4 * lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (j0 + k >= cnt) break;
+          if (!(w[k] > 0.f)) continue;
+          wsum += w[k];
+          acc.x = fmaf(w[k], x[k].x, acc.x);
+          acc.y = fmaf(w[k], x[k].y, acc.y);
+          acc.z = fmaf(w[k], x[k].z, acc.z);
+          acc.w = fmaf(w[k], x[k].w, acc.w);
+        }
+      }
     }
   }
   const bool empty = !(wsum > 0.f);
