@@ -93,3 +93,32 @@ def test_lse_optional():
     o2, _ = ea.attn_fwd(q, k, v, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_max_is_exact(d, causal):
+    """Scores of about 200 (natural-log units) where key j matches query row
+    i (j = i mod d) and 0 elsewhere: the matching columns fall in every
+    32-column chunk of a 128-key tile as i runs.  Softmax is only safe if the
+    tile's row max is the true maximum: a maximum that missed one chunk
+    would leave exp2 arguments near +290, which overflow to inf and turn O
+    into NaN.  Covers the maximum taken from the S load (unmasked tiles), the
+    masked-tile maximum (diagonal and tail tiles) and rescales by 2^-290."""
+    B, H, L = 1, 2, 300
+    a = 40.0  # q and k entries, exact in bf16: score a * a * scale
+    q = torch.zeros(B, H, L, d)
+    k = torch.zeros(B, H, L, d)
+    idx = torch.arange(L)
+    q[:, :, idx, idx % d] = a
+    k[:, :, idx, idx % d] = a
+    v = torch.randn(B, H, L, d, generator=torch.Generator().manual_seed(12))
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = ea.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ea.attn_get_device_status() == "ATTN_OK"
+    o_ref, lse_ref = orc.prefill(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale,
+                                 causal)
+    check_o(to_np(o), o_ref, "bf16")
+    check_lse(to_np(lse), lse_ref, "bf16")
