@@ -685,7 +685,7 @@ attn_status_t attn_decode_cascade(const void* q, const void* prefix_k, const voi
     return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (d != 128 || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if ((d != 128 && d != 64) || page_size != 16) return ATTN_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535 || (int64_t)B * Hq > (1 << 24)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(prefix_k) || !aligned16(prefix_v) || !aligned16(k_pages) ||
       !aligned16(v_pages) || !aligned16(o))

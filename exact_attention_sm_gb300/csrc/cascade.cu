@@ -39,19 +39,22 @@ constexpr int kRowsPerBlock = 4;  // one warp per output row
 constexpr int kBatch = 24;        // states whose O slices are in flight at once
 constexpr unsigned kFull = 0xffffffffu;
 
-// One warp per output row.  The row's S = S_pre + S_suf states are numbered
-// prefix chunks first, then suffix segments.  The row is latency-bound (a few
-// KB per row), so every load it needs is issued before any is used: the O
-// slices of the first kBatch states and the LSEs of the first 32 go out
-// together, and the max is reduced while they are in flight.  The weighted
-// sum of the O_s and the weight sum run over s in ascending order, so the
-// result depends on (S_pre, S_suf) alone.
+// One warp per output row (lane l owns dims DL l .. DL l + DL - 1, DL = D /
+// 32).  The row's S = S_pre + S_suf states are numbered prefix chunks first,
+// then suffix segments.  The row is latency-bound (a few KB per row), so
+// every load it needs is issued before any is used: the O slices of the
+// first kBatch states and the LSEs of the first 32 go out together, and the
+// max is reduced while they are in flight.  The weighted sum of the O_s and
+// the weight sum run over s in ascending order, so the result depends on
+// (S_pre, S_suf) alone.
+template <int D>
 __global__ void __launch_bounds__(kRowsPerBlock * 32)
     cascade_merge_kernel(const __nv_bfloat16* __restrict__ o_pre, const float* __restrict__ lse_pre,
                          int S_pre, const float* __restrict__ o_suf,
                          const float* __restrict__ lse_suf, int S_suf, int B, int Hq, int Hkv,
                          __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
-  constexpr int D = 128;  // lane l owns dims 4l .. 4l+3
+  constexpr int DL = D / 32;
+  static_assert(DL == 2 || DL == 4, "d = 64 or 128");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kRowsPerBlock + warp;
   if (r >= B * Hq) return;
@@ -64,34 +67,43 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
     return s < S_pre ? lse_pre[(static_cast<long long>(h) * S_pre + s) * lq + prow]
                      : lse_suf[static_cast<long long>(r) * S_suf + (s - S_pre)];
   };
-  // The lane's 4 dims of state s: bf16 (prefix, in .x .y) or fp32 bits (suffix).
-  auto load_o = [&](int s) {
+  // The lane's DL dims of state s, as floats: bf16 (prefix) or fp32 (suffix).
+  auto load_o = [&](int s, float (&x)[DL]) {
     if (s < S_pre) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(
-          o_pre + ((static_cast<long long>(h) * S_pre + s) * lq + prow) * D + 4 * lane);
-      return make_uint4(raw.x, raw.y, 0u, 0u);
+      const __nv_bfloat16* src = o_pre + ((static_cast<long long>(h) * S_pre + s) * lq + prow) * D + DL * lane;
+      if constexpr (DL == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src);
+        x[0] = attn::bf16_lo(raw.x); x[1] = attn::bf16_hi(raw.x);
+        x[2] = attn::bf16_lo(raw.y); x[3] = attn::bf16_hi(raw.y);
+      } else {
+        const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+        x[0] = attn::bf16_lo(raw); x[1] = attn::bf16_hi(raw);
+      }
+    } else {
+      const float* src = o_suf + (static_cast<long long>(r) * S_suf + (s - S_pre)) * D + DL * lane;
+      if constexpr (DL == 4) {
+        const float4 f = *reinterpret_cast<const float4*>(src);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+      } else {
+        const float2 f = *reinterpret_cast<const float2*>(src);
+        x[0] = f.x; x[1] = f.y;
+      }
     }
-    return *reinterpret_cast<const uint4*>(
-        o_suf + (static_cast<long long>(r) * S_suf + (s - S_pre)) * D + 4 * lane);
-  };
-  auto as_float4 = [&](int s, uint4 x) {
-    return s < S_pre ? make_float4(attn::bf16_lo(x.x), attn::bf16_hi(x.x), attn::bf16_lo(x.y),
-                                   attn::bf16_hi(x.y))
-                     : make_float4(__uint_as_float(x.x), __uint_as_float(x.y),
-                                   __uint_as_float(x.z), __uint_as_float(x.w));
   };
 
-  uint4 x[kBatch];
+  float x[kBatch][DL];
 #pragma unroll
   for (int u = 0; u < kBatch; ++u)
-    if (u < S) x[u] = load_o(u);
+    if (u < S) load_o(u, x[u]);
   const float ls0 = lane < S ? state_lse(lane) : -INFINITY;
   float big = ls0;
   for (int s = lane + 32; s < S; s += 32) big = fmaxf(big, state_lse(s));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) big = fmaxf(big, __shfl_xor_sync(kFull, big, off));
 
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float acc[DL];
+#pragma unroll
+  for (int e = 0; e < DL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (big != -INFINITY) {
     const float wl = ls0 == -INFINITY ? 0.f : expf(ls0 - big);  // weight of state `lane`
@@ -99,7 +111,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
       if (s0 > 0) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-          if (s0 + u < S) x[u] = load_o(s0 + u);
+          if (s0 + u < S) load_o(s0 + u, x[u]);
       }
       // Empty states hold O = 0 (both producers write it) and weigh 0.
 #pragma unroll
@@ -113,20 +125,22 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
           const float l = state_lse(s);
           w = l == -INFINITY ? 0.f : expf(l - big);
         }
-        const float4 v = as_float4(s, x[u]);
         wsum += w;
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
       }
     }
   }
   const bool empty = !(wsum > 0.f);
   const float inv = empty ? 0.f : 1.f / wsum;
-  const uint2 packed = make_uint2(attn::pack_bf16x2(acc.x * inv, acc.y * inv),
-                                  attn::pack_bf16x2(acc.z * inv, acc.w * inv));
-  *reinterpret_cast<uint2*>(o + static_cast<long long>(r) * D + 4 * lane) = packed;
+  if constexpr (DL == 4) {
+    *reinterpret_cast<uint2*>(o + static_cast<long long>(r) * D + DL * lane) =
+        make_uint2(attn::pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                   attn::pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(o + static_cast<long long>(r) * D + DL * lane) =
+        attn::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
   if (lane == 0 && lse != nullptr) lse[r] = empty ? -INFINITY : big + logf(wsum);
 }
 
@@ -150,11 +164,12 @@ attn_status_t launch_cascade_merge(const void* o_pre, const float* lse_pre, int 
                                    const float* o_suf, const float* lse_suf, int S_suf, int B,
                                    int Hq, int Hkv, int d, void* o, float* lse,
                                    cudaStream_t stream) {
-  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128 && d != 64) return ATTN_ERR_UNSUPPORTED;
   const int rows = B * Hq;
-  cascade_merge_kernel<<<(rows + kRowsPerBlock - 1) / kRowsPerBlock, kRowsPerBlock * 32, 0,
-                         stream>>>(static_cast<const __nv_bfloat16*>(o_pre), lse_pre, S_pre, o_suf,
-                                   lse_suf, S_suf, B, Hq, Hkv, static_cast<__nv_bfloat16*>(o), lse);
+  auto kernel = d == 64 ? cascade_merge_kernel<64> : cascade_merge_kernel<128>;
+  kernel<<<(rows + kRowsPerBlock - 1) / kRowsPerBlock, kRowsPerBlock * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o_pre), lse_pre, S_pre, o_suf, lse_suf, S_suf, B, Hq, Hkv,
+      static_cast<__nv_bfloat16*>(o), lse);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

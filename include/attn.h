@@ -414,13 +414,13 @@ attn_status_t attn_prefill_bsr(const void* q, const void* k_blocks, const void* 
  * attn_cascade_workspace_bytes: bytes attn_decode_cascade needs for the plan
  *   (stacked queries, prefix-chunk states, suffix states), 256-byte aligned.
  * attn_decode_cascade: q [B, Hq, d], o [B, Hq, d] bf16, lse [B, Hq] fp32 or
- *   NULL.  d = 128, page_size = 16, bf16 only.  seq_lens_host (host copy of
+ *   NULL.  d = 64 or 128, page_size = 16, bf16 only.  seq_lens_host (host copy of
  *   the suffix lengths) is required: it fixes the plan.  prefix_len >= 1.
  *   Pointers: device, 16-byte aligned (workspace 256-byte aligned), owned
  *   by the caller.  Errors: ATTN_ERR_INVALID_ARG for bad sizes, NULLs,
  *   misalignment or a suffix length outside [0, max_pages_per_seq * 16];
  *   ATTN_ERR_WORKSPACE if the workspace is missing, short or misaligned;
- *   ATTN_ERR_UNSUPPORTED for d != 128, page_size != 16 or non-bf16; device
+ *   ATTN_ERR_UNSUPPORTED for other d, page_size != 16 or non-bf16; device
  *   errors as attn_fwd / attn_decode_paged (status word).
  */
 attn_status_t attn_cascade_plan(int B, int Hq, int Hkv, int prefix_len,

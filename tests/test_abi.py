@@ -148,7 +148,8 @@ def test_cascade_rejects_on_host():
     assert casc(P=0) == 1
     assert casc(Hkv=3) == 1
     assert casc(splits=-1) == 1
-    assert casc(d=64) == 2
+    assert casc(d=96) == 2
+    assert casc(d=64) != 2                    # d = 64 is served
     assert casc(page=32) == 2
     assert casc(dtype=ea.ATTN_F32) == 2
     assert casc(pk=MISALIGNED) == 1

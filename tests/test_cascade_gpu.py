@@ -13,10 +13,10 @@ from tests.gpu_util import check_lse, check_o, to_np
 pytestmark = pytest.mark.gpu
 
 
-def run_cascade(prefix_len, suffix_lens, Hq=32, Hkv=8, num_splits=0, seed=0):
-    q, pk, pv, kp, vp, table, sl = inputs.cascade_inputs(prefix_len, suffix_lens, Hq, Hkv, 128,
+def run_cascade(prefix_len, suffix_lens, Hq=32, Hkv=8, num_splits=0, seed=0, d=128):
+    q, pk, pv, kp, vp, table, sl = inputs.cascade_inputs(prefix_len, suffix_lens, Hq, Hkv, d,
                                                          seed=seed)
-    scale = 1.0 / math.sqrt(128)
+    scale = 1.0 / math.sqrt(d)
     o, lse = ea.attn_decode_cascade(q.cuda(), pk.cuda(), pv.cuda(), kp.cuda(), vp.cuda(),
                                     table.cuda(), sl.cuda(), seq_lens_host=suffix_lens,
                                     num_splits=num_splits, scale=scale)
@@ -143,3 +143,14 @@ def test_graph_replay_with_new_queries(splits):
                                             scale)
         check_o(to_np(o), o_ref, "bf16")
         check_lse(to_np(lse), lse_ref, "bf16")
+
+
+@pytest.mark.parametrize("splits", [0, 1])
+@pytest.mark.parametrize("prefix_len,lens,Hq,Hkv", [(1, [0, 1, 17, 200], 32, 8),
+                                                    (300, [5, 700, 64], 32, 8),
+                                                    (1000, [33, 0, 129], 12, 4),
+                                                    (4096, [256] * 16, 32, 8)])
+def test_head_dim_64(prefix_len, lens, Hq, Hkv, splits):
+    """d = 64: the prefix pass on the d = 64 prefill kernel, the suffixes on
+    the d = 64 decode, the merge with two dims per lane."""
+    run_cascade(prefix_len, lens, Hq=Hq, Hkv=Hkv, num_splits=splits, seed=prefix_len + 1, d=64)
