@@ -15,6 +15,8 @@
 //                     the S_suf suffix states (fp32 O, fp32 LSE; from the
 //                     decode) are merged in a fixed order (prefix chunks
 //                     ascending, then suffix segments ascending), no atomics.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace {
@@ -67,34 +69,49 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
     return s < S_pre ? lse_pre[(static_cast<long long>(h) * S_pre + s) * lq + prow]
                      : lse_suf[static_cast<long long>(r) * S_suf + (s - S_pre)];
   };
-  // The lane's DL dims of state s, as floats: bf16 (prefix) or fp32 (suffix).
-  auto load_o = [&](int s, float (&x)[DL]) {
+  // The lane's DL dims of state s as raw words (bf16 pairs for a prefix
+  // state, fp32 bits for a suffix state), converted only where they are
+  // used, so that every load of a batch is in flight before the first use.
+  using Raw = typename std::conditional<DL == 4, uint4, uint2>::type;
+  auto load_o = [&](int s) {
+    Raw x;
     if (s < S_pre) {
-      const __nv_bfloat16* src = o_pre + ((static_cast<long long>(h) * S_pre + s) * lq + prow) * D + DL * lane;
+      const __nv_bfloat16* src =
+          o_pre + ((static_cast<long long>(h) * S_pre + s) * lq + prow) * D + DL * lane;
       if constexpr (DL == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(src);
-        x[0] = attn::bf16_lo(raw.x); x[1] = attn::bf16_hi(raw.x);
-        x[2] = attn::bf16_lo(raw.y); x[3] = attn::bf16_hi(raw.y);
+        const uint2 w = *reinterpret_cast<const uint2*>(src);
+        x = make_uint4(w.x, w.y, 0u, 0u);
       } else {
-        const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
-        x[0] = attn::bf16_lo(raw); x[1] = attn::bf16_hi(raw);
+        x = make_uint2(*reinterpret_cast<const uint32_t*>(src), 0u);
       }
     } else {
       const float* src = o_suf + (static_cast<long long>(r) * S_suf + (s - S_pre)) * D + DL * lane;
-      if constexpr (DL == 4) {
-        const float4 f = *reinterpret_cast<const float4*>(src);
-        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+      x = *reinterpret_cast<const Raw*>(src);
+    }
+    return x;
+  };
+  auto to_float = [&](int s, const Raw& x, float (&f)[DL]) {
+    if constexpr (DL == 4) {
+      if (s < S_pre) {
+        f[0] = attn::bf16_lo(x.x); f[1] = attn::bf16_hi(x.x);
+        f[2] = attn::bf16_lo(x.y); f[3] = attn::bf16_hi(x.y);
       } else {
-        const float2 f = *reinterpret_cast<const float2*>(src);
-        x[0] = f.x; x[1] = f.y;
+        f[0] = __uint_as_float(x.x); f[1] = __uint_as_float(x.y);
+        f[2] = __uint_as_float(x.z); f[3] = __uint_as_float(x.w);
+      }
+    } else {
+      if (s < S_pre) {
+        f[0] = attn::bf16_lo(x.x); f[1] = attn::bf16_hi(x.x);
+      } else {
+        f[0] = __uint_as_float(x.x); f[1] = __uint_as_float(x.y);
       }
     }
   };
 
-  float x[kBatch][DL];
+  Raw x[kBatch];
 #pragma unroll
   for (int u = 0; u < kBatch; ++u)
-    if (u < S) load_o(u, x[u]);
+    if (u < S) x[u] = load_o(u);
   const float ls0 = lane < S ? state_lse(lane) : -INFINITY;
   float big = ls0;
   for (int s = lane + 32; s < S; s += 32) big = fmaxf(big, state_lse(s));
@@ -111,7 +128,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
       if (s0 > 0) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-          if (s0 + u < S) load_o(s0 + u, x[u]);
+          if (s0 + u < S) x[u] = load_o(s0 + u);
       }
       // Empty states hold O = 0 (both producers write it) and weigh 0.
 #pragma unroll
@@ -125,9 +142,11 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
           const float l = state_lse(s);
           w = l == -INFINITY ? 0.f : expf(l - big);
         }
+        float v[DL];
+        to_float(s, x[u], v);
         wsum += w;
 #pragma unroll
-        for (int e = 0; e < DL; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
+        for (int e = 0; e < DL; ++e) acc[e] = fmaf(w, v[e], acc[e]);
       }
     }
   }
