@@ -176,8 +176,10 @@ def test_cascade_plan(B, Hq, Hkv, P, slots):
     assert (sc, ss) == ea.attn_decode_plan(lens, Hkv, 16, 0, 456)
     rows = B * Hq
     r = lambda x: -(-x // 256) * 256
-    want = r(rows * 128 * 2) + r(rows * pc * 128 * 2) + r(rows * pc * 4) + r(rows * ss * 128 * 4) + r(rows * ss * 4)
-    assert ea.attn_cascade_workspace_bytes(B, Hq, 128, pc, ss) == want
+    for d in (64, 128):
+        want = (r(rows * d * 2) + r(rows * pc * d * 2) + r(rows * pc * 4) + r(rows * ss * d * 4)
+                + r(rows * ss * 4))
+        assert ea.attn_cascade_workspace_bytes(B, Hq, d, pc, ss) == want
 
 
 def varlen(**kw):
